@@ -1,0 +1,343 @@
+/*
+ * h2o_oracle.c -- plain, slow CPU oracle of the H2O budgeted KV-cache eviction step.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load this library. The product path never calls it; it shares no code with the CUDA path.
+ *
+ * What it restates (web pages on H2O, "Heavy-Hitter Oracle"; Zhang et al., NeurIPS 2023):
+ *   [post]   the ttsmallhot.github.io H2O summary post:
+ *            §2.1.1  attention weights are Softmax(QK^T / sqrt(d)) (the paper drops sqrt(d) for
+ *                    brevity; the post states it, and so does this oracle);
+ *            §2.1.2  a token's accumulated attention score = the sum of the attention it receives;
+ *            §2.2    budget k split into k_local recent tokens and k_heavy heavy hitters; after each
+ *                    new token its attention to every cached token is added to that token's running
+ *                    score; when the cache is full the recent tokens are kept and the cached token
+ *                    with the lowest accumulated score among the rest is evicted;
+ *            §2.3    the new token's K/V is written into the evicted slot (no compaction).
+ *   [note]   "H2O Heavy-Hitter Oracle 分析" (liuhc.cn):
+ *            §3.1    scores are kept per head; heavy hitters = top-k of the cumulative attention
+ *                    (argsort of the negated sums);
+ *            §3.2    victim = argmin(score); the new token is always admitted.
+ *
+ * Readings where the pages leave a step open (each also listed in the design notes):
+ *   - scale: logits are (q . k) / sqrt(D), in float64;
+ *   - attended set of step t: the n = min(t, budget) cached slots plus the new token itself; the new
+ *     token's own weight becomes its initial score (prefill column sums include the diagonal too);
+ *   - order: scores are accumulated first, then the victim is chosen on the updated scores;
+ *   - protection: after step t the positions t-k_local+1 .. t must be resident, so cached slots with
+ *     position <= t - k_local are the eviction candidates (k_local <= 1 leaves every cached slot a
+ *     candidate, which is the unprotected argmin of [note] §3.2; k_heavy = 0 is a sliding window);
+ *   - ties: the lowest score is evicted, equal scores evict the lowest position; prefill keeps the
+ *     top k_heavy column sums ranked (sum desc, position desc), i.e. the same order read backwards;
+ *   - prefill selection = column sums of the full causal prompt softmax, then one top-k ([note] §3.1),
+ *     with the last k_local prompt positions always kept; kept tokens fill slots 0.. in ascending
+ *     position, unused slots get position -1, score 0 and zero K/V rows;
+ *   - precision: float64 for dot products, softmax and column sums; the score table is float32 and
+ *     each step adds float32(p) to it with one float32 addition (the storage the method keeps).
+ *
+ * Near ties. Another implementation computing in float32 may order two nearly equal scores the other
+ * way. When the caller passes that implementation's choice ("prefer"), the oracle adopts it only if it
+ * is a valid choice whose score is within tie_rel (reported as NEAR_TIE) or err_rel (ERROR_BOUND) of
+ * the rule's choice, relative to the larger magnitude; an exact tie is always decided by position.
+ * The adoption changes which slot is overwritten, never any arithmetic.
+ */
+#include "h2o_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- element access: exact widening of the stored values ---------------------------------- */
+
+static size_t elem_bytes(int32_t dtype) { return dtype == H2O_ORACLE_F32 ? 4 : 2; }
+
+static double elem(const void* base, int32_t dtype, size_t i) {
+  if (dtype == H2O_ORACLE_F32) return (double)((const float*)base)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* (q . k_row) in float64, d = 0 .. D-1 in order. */
+static double dot(const double* q, const void* rows, int32_t dtype, size_t row, int32_t D) {
+  double acc = 0.0;
+  for (int32_t d = 0; d < D; ++d) acc += q[d] * elem(rows, dtype, row * (size_t)D + (size_t)d);
+  return acc;
+}
+
+static int check_dims(int32_t units, int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local,
+                      int32_t dtype) {
+  if (units < 0 || D < 1 || budget < 1 || k_heavy < 0 || k_local < 0) return -1;
+  if (k_heavy + k_local != budget) return -2;
+  if (dtype != H2O_ORACLE_F32 && dtype != H2O_ORACLE_BF16) return -3;
+  return 0;
+}
+
+static double rel_gap(double lo, double hi) {
+  double scale = fmax(fabs(lo), fabs(hi));
+  if (scale == 0.0) return 0.0;
+  return (hi - lo) / scale;
+}
+
+/* ---- prefill: column sums of the causal softmax, then the heavy-hitter selection ----------- */
+
+typedef struct {
+  double c;
+  int32_t pos;
+} ranked;
+
+/* Rank for keeping: larger column sum first; on equal sums the later position first (so that the
+ * dropped side is "lowest score, then lowest position", the decode eviction order). */
+static int keep_order(const void* a, const void* b) {
+  const ranked* x = (const ranked*)a;
+  const ranked* y = (const ranked*)b;
+  if (x->c > y->c) return -1;
+  if (x->c < y->c) return 1;
+  return (x->pos > y->pos) ? -1 : (x->pos < y->pos) ? 1 : 0;
+}
+
+/* c_j = sum over rows i >= j of softmax_i(j), softmax over the causal row i: j' = 0..i. */
+static void causal_column_sums(int32_t D, int32_t dtype, int32_t P, const void* q, const void* k,
+                               double scale, double* c, double* qrow, double* s) {
+  for (int32_t j = 0; j < P; ++j) c[j] = 0.0;
+  for (int32_t i = 0; i < P; ++i) {
+    for (int32_t d = 0; d < D; ++d) qrow[d] = elem(q, dtype, (size_t)i * D + d);
+    double m = -INFINITY;
+    for (int32_t j = 0; j <= i; ++j) {
+      s[j] = dot(qrow, k, dtype, (size_t)j, D) * scale;
+      if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int32_t j = 0; j <= i; ++j) l += exp(s[j] - m);
+    for (int32_t j = 0; j <= i; ++j) c[j] += exp(s[j] - m) / l;
+  }
+}
+
+/* Decide whether a preferred kept set (slot_pos layout) may replace the rule's. */
+static int32_t judge_prefill_preference(int32_t budget, int32_t k_local, int32_t P,
+                                        const double* c, const unsigned char* keep_rule,
+                                        const int32_t* prefer, double tie_rel, double err_rel,
+                                        unsigned char* keep_pref) {
+  memset(keep_pref, 0, (size_t)P);
+  for (int32_t s = 0; s < budget; ++s) {
+    int32_t p = prefer[s];
+    if (p < 0 || p >= P || keep_pref[p]) return H2O_ORACLE_REJECTED;
+    keep_pref[p] = 1;
+  }
+  for (int32_t p = P - k_local; p < P; ++p)
+    if (!keep_pref[p]) return H2O_ORACLE_REJECTED;
+  double max_dropped_by_pref = -INFINITY, min_added_by_pref = INFINITY;
+  int differs = 0;
+  for (int32_t p = 0; p < P - k_local; ++p) {
+    if (keep_rule[p] && !keep_pref[p]) { differs = 1; if (c[p] > max_dropped_by_pref) max_dropped_by_pref = c[p]; }
+    if (!keep_rule[p] && keep_pref[p]) { differs = 1; if (c[p] < min_added_by_pref) min_added_by_pref = c[p]; }
+  }
+  if (!differs) return H2O_ORACLE_RULE;
+  if (max_dropped_by_pref == min_added_by_pref) return H2O_ORACLE_REJECTED; /* exact tie: by position */
+  double g = rel_gap(min_added_by_pref, max_dropped_by_pref);
+  if (g <= tie_rel) return H2O_ORACLE_NEAR_TIE;
+  if (g <= err_rel) return H2O_ORACLE_ERROR_BOUND;
+  return H2O_ORACLE_REJECTED;
+}
+
+int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                              int32_t k_local, int32_t dtype, int32_t P, const void* q,
+                              const void* k, const void* v, void* k_cache, void* v_cache,
+                              float* scores, int32_t* slot_pos, double* colsum,
+                              const int32_t* prefer_pos, double tie_rel, double err_rel,
+                              h2o_oracle_prefill_info* infos) {
+  int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
+  if (rc) return rc;
+  if (P < 1) return -4;
+  const size_t eb = elem_bytes(dtype);
+  const size_t row = (size_t)D * eb;
+  const double scale = 1.0 / sqrt((double)D);
+
+  double* c = (double*)malloc(sizeof(double) * (size_t)P);
+  double* s = (double*)malloc(sizeof(double) * (size_t)P);
+  double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
+  ranked* cand = (ranked*)malloc(sizeof(ranked) * (size_t)P);
+  unsigned char* keep = (unsigned char*)malloc((size_t)P);
+  unsigned char* keep_pref = (unsigned char*)malloc((size_t)P);
+  if (!c || !s || !qrow || !cand || !keep || !keep_pref) {
+    free(c); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
+    return -9;
+  }
+
+  for (int32_t u = 0; u < units; ++u) {
+    const char* qu = (const char*)q + (size_t)u * P * row;
+    const char* ku = (const char*)k + (size_t)u * P * row;
+    const char* vu = (const char*)v + (size_t)u * P * row;
+    char* kc = (char*)k_cache + (size_t)u * budget * row;
+    char* vc = (char*)v_cache + (size_t)u * budget * row;
+    float* sc = scores + (size_t)u * budget;
+    int32_t* sp = slot_pos + (size_t)u * budget;
+    h2o_oracle_prefill_info info = {H2O_ORACLE_NO_EVICTION, 0, INFINITY};
+
+    causal_column_sums(D, dtype, P, qu, ku, scale, c, qrow, s);
+    if (colsum) memcpy(colsum + (size_t)u * P, c, sizeof(double) * (size_t)P);
+
+    /* Which prompt positions stay. */
+    if (P <= budget) {
+      memset(keep, 1, (size_t)P);
+    } else {
+      memset(keep, 0, (size_t)P);
+      for (int32_t p = P - k_local; p < P; ++p) keep[p] = 1;     /* the k_local most recent */
+      int32_t nc = P - k_local;                                 /* older positions compete */
+      for (int32_t p = 0; p < nc; ++p) { cand[p].c = c[p]; cand[p].pos = p; }
+      qsort(cand, (size_t)nc, sizeof(ranked), keep_order);
+      for (int32_t r = 0; r < k_heavy; ++r) keep[cand[r].pos] = 1;
+      info.kind = H2O_ORACLE_RULE;
+      if (k_heavy > 0 && k_heavy < nc) info.gap_rel = rel_gap(cand[k_heavy].c, cand[k_heavy - 1].c);
+      if (prefer_pos) {
+        int32_t kind = judge_prefill_preference(budget, k_local, P, c, keep,
+                                                prefer_pos + (size_t)u * budget, tie_rel, err_rel,
+                                                keep_pref);
+        info.kind = kind;
+        if (kind == H2O_ORACLE_NEAR_TIE || kind == H2O_ORACLE_ERROR_BOUND)
+          memcpy(keep, keep_pref, (size_t)P);
+      }
+    }
+
+    /* Kept tokens fill slots in ascending position; the rest of the slots are empty. */
+    int32_t slot = 0;
+    for (int32_t p = 0; p < P; ++p) {
+      if (!keep[p]) continue;
+      memcpy(kc + (size_t)slot * row, ku + (size_t)p * row, row);
+      memcpy(vc + (size_t)slot * row, vu + (size_t)p * row, row);
+      sc[slot] = (float)c[p];
+      sp[slot] = p;
+      ++slot;
+    }
+    info.kept = slot;
+    for (; slot < budget; ++slot) {
+      memset(kc + (size_t)slot * row, 0, row);
+      memset(vc + (size_t)slot * row, 0, row);
+      sc[slot] = 0.0f;
+      sp[slot] = -1;
+    }
+    if (infos) infos[u] = info;
+  }
+  free(c); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
+  return 0;
+}
+
+/* ---- decode: attend, accumulate, evict, overwrite in place --------------------------------- */
+
+int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                           int32_t k_local, int32_t dtype, int32_t t, const void* q,
+                           const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           float* scores, int32_t* slot_pos, double* out, double* probs,
+                           int32_t* evicted_slot, int32_t* evicted_pos,
+                           const int32_t* prefer_victim, double tie_rel, double err_rel,
+                           h2o_oracle_step_info* infos) {
+  int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
+  if (rc) return rc;
+  if (t < 1) return -4;
+  const int32_t n = t < budget ? t : budget;   /* valid cached slots before this step */
+  const size_t eb = elem_bytes(dtype);
+  const size_t row = (size_t)D * eb;
+  const double scale = 1.0 / sqrt((double)D);
+
+  /* Every unit's slot map must hold exactly n valid, distinct-looking entries. */
+  for (int32_t u = 0; u < units; ++u) {
+    const int32_t* sp = slot_pos + (size_t)u * budget;
+    for (int32_t j = 0; j < budget; ++j) {
+      if (j < n && (sp[j] < 0 || sp[j] >= t)) return -5;
+      if (j >= n && sp[j] != -1) return -5;
+    }
+  }
+
+  double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+  double* s = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+  double* p = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+  if (!qv || !s || !p) { free(qv); free(s); free(p); return -9; }
+
+  for (int32_t u = 0; u < units; ++u) {
+    const size_t ub = (size_t)u * budget;
+    char* kc = (char*)k_cache + ub * row;
+    char* vc = (char*)v_cache + ub * row;
+    float* sc = scores + ub;
+    int32_t* sp = slot_pos + ub;
+    h2o_oracle_step_info info = {H2O_ORACLE_NO_EVICTION, -1, -1, -1, -1, 0, INFINITY};
+
+    /* Logits over the n cached slots and the new token (index n): [post] §2.1.1. */
+    for (int32_t d = 0; d < D; ++d) qv[d] = elem(q, dtype, (size_t)u * D + d);
+    for (int32_t j = 0; j < n; ++j) s[j] = dot(qv, kc, dtype, (size_t)j, D) * scale;
+    s[n] = dot(qv, k_new, dtype, (size_t)u, D) * scale;
+
+    double m = -INFINITY;
+    for (int32_t j = 0; j <= n; ++j) if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int32_t j = 0; j <= n; ++j) l += exp(s[j] - m);
+    for (int32_t j = 0; j <= n; ++j) p[j] = exp(s[j] - m) / l;
+    if (probs) memcpy(probs + (size_t)u * (budget + 1), p, sizeof(double) * ((size_t)n + 1));
+
+    /* Output o = sum_j p_j v_j over the same n + 1 keys. */
+    for (int32_t d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (int32_t j = 0; j < n; ++j) acc += p[j] * elem(vc, dtype, (size_t)j * D + d);
+      acc += p[n] * elem(v_new, dtype, (size_t)u * D + d);
+      out[(size_t)u * D + d] = acc;
+    }
+
+    /* Local statistic: every cached token's score grows by the attention it just received
+     * ([post] §2.2, [note] §3.2), as one float32 addition of the float32 weight. */
+    for (int32_t j = 0; j < n; ++j) {
+      float add = (float)p[j];
+      sc[j] = sc[j] + add;
+    }
+
+    int32_t target;
+    if (n < budget) {
+      target = n;                                           /* free slot: no eviction */
+    } else {
+      /* Greedy eviction: the recent tokens are protected; among the rest the lowest updated
+       * score goes, equal scores evict the lowest position ([post] §2.2, [note] §3.2). */
+      const int64_t last_candidate = (int64_t)t - k_local;
+      int32_t best = -1, second = -1;
+      for (int32_t j = 0; j < n; ++j) {
+        if ((int64_t)sp[j] > last_candidate) continue;
+        ++info.n_candidates;
+        if (best < 0 || sc[j] < sc[best] || (sc[j] == sc[best] && sp[j] < sp[best])) {
+          second = best;
+          best = j;
+        } else if (second < 0 || sc[j] < sc[second] || (sc[j] == sc[second] && sp[j] < sp[second])) {
+          second = j;
+        }
+      }
+      if (best < 0) { free(qv); free(s); free(p); return -6; }  /* impossible when kl <= budget */
+      info.rule_victim = best;
+      if (second >= 0) info.gap_rel = rel_gap((double)sc[best], (double)sc[second]);
+      info.kind = H2O_ORACLE_RULE;
+      target = best;
+      if (prefer_victim && prefer_victim[u] != best) {
+        int32_t w = prefer_victim[u];
+        info.kind = H2O_ORACLE_REJECTED;
+        if (w >= 0 && w < n && (int64_t)sp[w] <= last_candidate && sc[w] != sc[best]) {
+          double g = rel_gap((double)sc[best], (double)sc[w]);
+          if (g <= tie_rel) info.kind = H2O_ORACLE_NEAR_TIE;
+          else if (g <= err_rel) info.kind = H2O_ORACLE_ERROR_BOUND;
+          if (info.kind != H2O_ORACLE_REJECTED) target = w;
+        }
+      }
+      info.victim = target;
+      info.evicted_pos = sp[target];
+    }
+
+    /* In-place overwrite, no compaction ([post] §2.3): the new token takes the slot, starting
+     * from its own attention weight as score. */
+    memcpy(kc + (size_t)target * row, (const char*)k_new + (size_t)u * row, row);
+    memcpy(vc + (size_t)target * row, (const char*)v_new + (size_t)u * row, row);
+    sc[target] = (float)p[n];
+    sp[target] = t;
+    info.written_slot = target;
+
+    if (evicted_slot) evicted_slot[u] = info.victim;
+    if (evicted_pos) evicted_pos[u] = info.evicted_pos;
+    if (infos) infos[u] = info;
+  }
+  free(qv); free(s); free(p);
+  return 0;
+}

@@ -1,0 +1,322 @@
+"""Pins of the CPU oracle: checks against what the H2O pages and plain mathematics fix.
+
+Each ``pin_*`` takes the path of an oracle shared library and raises ``AssertionError`` when the
+oracle disagrees with an independent fact. They are run on the real oracle by
+``test_oracle_pins.py`` and on deliberately broken copies of it by ``test_oracle_mutants.py``,
+which shows that each plausible mistake is caught by at least one pin.
+
+Sources of the facts (web pages on H2O):
+  * ttsmallhot.github.io H2O post, §3.1.1 baselines: the Full KV cache (no eviction) and Local
+    (sliding window) policies are the limits H2O must reduce to when the budget covers everything
+    or when no heavy-hitter slots exist;
+  * same post §2.1.2 / §2.2 and "H2O Heavy-Hitter Oracle 分析" §3.2: the score is the accumulated
+    attention, the victim is its argmin outside the recent tokens, the new token is always kept;
+  * "H2O Heavy-Hitter Oracle 分析" §3.1: heavy hitters are the top-k of the cumulative attention.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import bruteforce as bf
+import oracle
+import trajectory as tj
+
+
+def _close(a, b, rtol, atol, what):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    if not np.allclose(a, b, rtol=rtol, atol=atol):
+        err = np.max(np.abs(a - b))
+        raise AssertionError(f"{what}: max abs diff {err:.3e}\n{a}\n{b}")
+
+
+def _cases(seed: int, count: int, max_p=10, max_s=10, max_budget=6, dims=(1, 4, 8)):
+    rng = np.random.default_rng(seed)
+    for _ in range(count):
+        D = int(rng.choice(dims))
+        P = int(rng.integers(1, max_p + 1))
+        S = int(rng.integers(1, max_s + 1))
+        budget = int(rng.integers(1, max_budget + 1))
+        kl = int(rng.integers(0, budget + 1))
+        dtype = "f32" if rng.random() < 0.5 else "bf16"
+        yield rng, D, P, S, budget, budget - kl, kl, dtype
+
+
+def pin_full_budget_is_dense(lib):
+    """Budget >= every token: no eviction ever, and each output equals dense causal attention."""
+    rng = np.random.default_rng(11)
+    for _ in range(12):
+        D = int(rng.choice([1, 4, 8]))
+        P, S = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        budget = P + S + int(rng.integers(0, 3))
+        kl = int(rng.integers(0, budget + 1))
+        dtype = "f32" if rng.random() < 0.5 else "bf16"
+        q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, budget - kl, kl)
+        Q, K, V = bf.widen(q), bf.widen(k), bf.widen(v)
+        for rec in tr.steps:
+            assert rec.evicted_slot == -1 and rec.evicted_pos == -1, "evicted under a full budget"
+            _close(rec.out, bf.dense_causal_attention(Q, K, V, rec.t), 1e-12, 1e-13,
+                   f"full-budget output at t={rec.t}")
+            expect = np.full(budget, -1)
+            expect[: rec.t + 1] = np.arange(rec.t + 1)
+            assert np.array_equal(rec.slot_pos_after, expect), "slot map under a full budget"
+
+
+def pin_no_heavy_is_sliding_window(lib):
+    """k_heavy = 0: H2O is the Local baseline, a window over positions t-k .. t."""
+    rng = np.random.default_rng(12)
+    for _ in range(16):
+        D = int(rng.choice([1, 4, 8]))
+        budget = int(rng.integers(1, 7))
+        P, S = int(rng.integers(1, 13)), int(rng.integers(1, 13))
+        dtype = "f32" if rng.random() < 0.5 else "bf16"
+        q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=3)
+        tr = tj.run(lib, q, k, v, P, S, budget, 0, budget)
+        Q, K, V = bf.widen(q), bf.widen(k), bf.widen(v)
+        kept = sorted(p for p in tr.prefill_state.slot_pos[0] if p >= 0)
+        assert kept == list(range(max(0, P - budget), P)), "prefill window"
+        for rec in tr.steps:
+            _close(rec.out, bf.window_attention(Q, K, V, rec.t, budget), 1e-12, 1e-13,
+                   f"window output at t={rec.t}")
+            pos = sorted(p for p in rec.slot_pos_after if p >= 0)
+            assert pos == list(range(max(0, rec.t - budget + 1), rec.t + 1)), "window slot set"
+            for j, p in enumerate(rec.slot_pos_after):
+                if p >= 0:
+                    assert np.array_equal(rec.k_after[j], k[p]) and np.array_equal(rec.v_after[j], v[p])
+
+
+def pin_victim_is_argmin_of_recomputed_scores(lib):
+    """Scores recomputed from scratch out of the attended-set history match the table, the prefill
+    keeps the top column sums (full sort), and every victim is the argmin of the recomputed scores
+    among positions <= t - k_local, equal scores evicting the lowest position."""
+    checked = 0
+    for rng, D, P, S, budget, kh, kl, dtype in _cases(13, 40, max_p=12, max_s=12):
+        q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, kh, kl)
+        Q, K = bf.widen(q), bf.widen(k)
+        c = bf.causal_column_sums(Q[:P], K[:P])
+        _close(tr.colsum, c, 1e-12, 1e-12, "prefill column sums")
+        kept = bf.heavy_selection(c, budget, kh, kl)
+        got = [int(p) for p in tr.prefill_state.slot_pos[0] if p >= 0]
+        if P > budget and 0 < kh < P - kl:
+            older = sorted(c[: P - kl], reverse=True)
+            near = abs(older[kh - 1] - older[kh]) <= 1e-9 * max(abs(older[kh - 1]), 1e-300)
+        else:
+            near = False
+        if not near:
+            assert got == kept, f"prefill kept set {got} != {kept}"
+        _close(tr.prefill_state.scores[0][: len(got)], c[got], 1e-6, 1e-7, "prefill scores")
+        history = []
+        for rec in tr.steps:
+            attended = [int(p) for p in rec.slot_pos_before if p >= 0] + [rec.t]
+            history.append((rec.t, attended))
+            resident = [int(p) for p in rec.slot_pos_before if p >= 0]
+            rs = bf.recomputed_scores(Q, K, P, history, resident + [rec.t])
+            if rec.evicted_pos >= 0:
+                cands = [p for p in resident if p <= rec.t - kl]
+                order = sorted(cands, key=lambda p: (rs[p], p))
+                if len(order) > 1:
+                    a, b = rs[order[0]], rs[order[1]]
+                    if abs(b - a) <= 1e-6 * max(abs(a), abs(b)):
+                        continue  # fp32 table vs float64 recomputation may order a near tie
+                assert rec.evicted_pos == order[0], (
+                    f"t={rec.t}: evicted {rec.evicted_pos}, recomputed argmin {order[0]}")
+                checked += 1
+            for j, p in enumerate(rec.slot_pos_after):
+                if p >= 0:
+                    _close(rec.scores_after[j], rs[int(p)], 2e-6, 1e-7, f"score of position {p}")
+    assert checked > 50, f"too few eviction decisions checked ({checked})"
+
+
+def pin_uniform_attention_closed_form(lib):
+    """All-zero queries: every weight is 1/(attended count), prefill column sums are the harmonic
+    differences H_P - H_j, the oldest positions are the heavy hitters, outputs are plain means."""
+    for P, budget, kh, S in [(9, 4, 2, 6), (5, 4, 2, 5), (12, 6, 3, 8), (7, 3, 0, 4)]:
+        kl = budget - kh
+        D = 4
+        rng = np.random.default_rng(P * 100 + budget)
+        q = np.zeros((P + S, D), dtype=np.float32)
+        k = rng.standard_normal((P + S, D)).astype(np.float32)
+        v = rng.standard_normal((P + S, D)).astype(np.float32)
+        tr = tj.run(lib, q, k, v, P, S, budget, kh, kl)
+        HP = bf.harmonic(P)
+        _close(tr.colsum, [HP - bf.harmonic(j) for j in range(P)], 1e-13, 1e-14, "harmonic colsum")
+        kept = [p for p in tr.prefill_state.slot_pos[0] if p >= 0]
+        want = list(range(P)) if P <= budget else sorted(set(range(kh)) | set(range(P - kl, P)))
+        assert kept == want, f"uniform prefill keeps {kept}, expected {want}"
+        for rec in tr.steps:
+            n = min(rec.t, budget)
+            _close(rec.probs, np.full(n + 1, 1.0 / (n + 1)), 1e-14, 0, "uniform weights")
+            rows = [v[p] for p in rec.slot_pos_before if p >= 0] + [v[rec.t]]
+            _close(rec.out, np.mean(np.asarray(rows, dtype=np.float64), axis=0), 1e-13, 1e-14,
+                   "uniform output")
+
+
+def pin_mass_and_slot_invariants(lib):
+    """Softmax mass 1 per step, prefill column sums add to P, the table gains 1 minus the evicted
+    score each step, and the slot map stays a valid budgeted, windowed set of positions."""
+    for rng, D, P, S, budget, kh, kl, dtype in _cases(14, 30, max_p=12, max_s=12):
+        q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, kh, kl)
+        assert math.isclose(float(tr.colsum.sum()), P, rel_tol=1e-12), "sum of column sums != P"
+        for rec in tr.steps:
+            t, n = rec.t, min(rec.t, budget)
+            assert math.isclose(float(rec.probs.sum()), 1.0, rel_tol=1e-12), "softmax mass"
+            before = float(np.sum(rec.scores_before, dtype=np.float64))
+            after = float(np.sum(rec.scores_after, dtype=np.float64))
+            lost = 0.0
+            if rec.evicted_slot >= 0:
+                j = rec.evicted_slot
+                lost = float(np.float32(rec.scores_before[j]) + np.float32(rec.probs[j]))
+            tol = (n + 3) * 2.0 ** -23 * max(1.0, before + 1.0)
+            assert abs(after - (before + 1.0 - lost)) <= tol, (
+                f"t={t}: mass {after} vs {before} + 1 - {lost}")
+            pos = [int(p) for p in rec.slot_pos_after if p >= 0]
+            assert len(pos) == len(set(pos)) == min(t + 1, budget), "slot count / duplicates"
+            for p in range(max(0, t - kl + 1), t + 1):
+                assert p in pos, f"t={t}: recent position {p} not resident"
+            written = rec.evicted_slot if rec.evicted_slot >= 0 else n
+            assert rec.slot_pos_after[written] == t, "new token not in the freed slot"
+            if rec.evicted_slot >= 0:
+                assert rec.evicted_pos == rec.slot_pos_before[rec.evicted_slot]
+                assert rec.evicted_pos <= t - kl, "evicted a protected position"
+            else:
+                assert n < budget and rec.evicted_pos == -1
+            changed = [j for j in range(budget) if rec.slot_pos_after[j] != rec.slot_pos_before[j]]
+            assert changed == [written], "more than one slot rewritten (compaction?)"
+            for j, p in enumerate(rec.slot_pos_after):
+                if p >= 0:
+                    assert np.array_equal(rec.k_after[j], k[p]) and np.array_equal(rec.v_after[j], v[p])
+            assert np.float32(rec.scores_after[written]) == np.float32(rec.probs[n]), \
+                "new token's score is not its own weight"
+
+
+def pin_small_local_is_unprotected_argmin(lib):
+    """k_local in {0, 1}: no cached slot is protected, so the victim is the plain argmin of the
+    updated table over all slots (the rule as written in "H2O Heavy-Hitter Oracle 分析" §3.2)."""
+    seen = 0
+    for rng, D, P, S, budget, _, _, dtype in _cases(15, 30, max_p=12, max_s=12):
+        for kl in (0, 1):
+            if kl > budget:
+                continue
+            q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=2)
+            tr = tj.run(lib, q, k, v, P, S, budget, budget - kl, kl)
+            for rec in tr.steps:
+                if rec.evicted_slot < 0:
+                    continue
+                upd = rec.scores_before + rec.probs[:-1].astype(np.float32)
+                order = sorted(range(budget), key=lambda j: (upd[j], rec.slot_pos_before[j]))
+                assert rec.evicted_slot == order[0], f"t={rec.t}: victim {rec.evicted_slot} != {order[0]}"
+                seen += 1
+    assert seen > 30
+
+
+def _hand_state(lib, slot_pos, scores, t, kl, D=2):
+    """One step from a hand-built full cache with all-zero keys and queries (uniform weights)."""
+    budget = len(slot_pos)
+    orc = oracle.Oracle(budget, budget - kl, kl, lib_path=lib)
+    st = orc.new_state(1, D, np.float32)
+    st.slot_pos[0] = slot_pos
+    st.scores[0] = scores
+    z = np.zeros((1, D), dtype=np.float32)
+    out, es, ep, probs, infos = orc.decode_step(t, z, z, z + 1, st, want_probs=True)
+    return int(es[0]), int(ep[0]), st
+
+
+def pin_hand_built_ties_and_protection(lib):
+    """Exact ties evict the lowest position; recent positions are never candidates."""
+    # all scores equal -> uniform weights keep them equal -> lowest position among candidates
+    assert _hand_state(lib, [7, 3, 9, 5], [0.0] * 4, 10, kl=1)[:2] == (1, 3)
+    assert _hand_state(lib, [7, 3, 9, 5], [0.0] * 4, 10, kl=0)[:2] == (1, 3)
+    # position 9 (score 0, the lowest) is protected with k_local = 2 (t = 10 keeps 9 and 10)
+    assert _hand_state(lib, [7, 3, 9, 5], [0.1, 0.5, 0.0, 0.2], 10, kl=2)[:2] == (0, 7)
+    # with k_local = 1 nothing is protected: position 9 goes
+    assert _hand_state(lib, [7, 3, 9, 5], [0.1, 0.5, 0.0, 0.2], 10, kl=1)[:2] == (2, 9)
+    # k_local = budget: only t - budget is a candidate (sliding window), whatever the scores
+    assert _hand_state(lib, [7, 6, 9, 8], [0.0, 9.0, 0.0, 0.0], 10, kl=4)[:2] == (1, 6)
+    # equal lowest scores at positions 5 and 2: position 2 goes
+    assert _hand_state(lib, [5, 8, 2, 9], [0.25, 0.5, 0.25, 0.75], 10, kl=1)[:2] == (2, 2)
+    _, _, st = _hand_state(lib, [5, 8, 2, 9], [0.25, 0.5, 0.25, 0.75], 10, kl=1)
+    assert list(st.slot_pos[0]) == [5, 8, 10, 9]
+    assert np.float32(st.scores[0][2]) == np.float32(0.2)  # the new token's own weight, 1/5
+    assert np.allclose(st.scores[0][[0, 1, 3]], np.float32([0.25, 0.5, 0.75]) + np.float32(0.2))
+
+
+def pin_prefill_equal_sums_keep_later(lib):
+    """Equal column sums: the later position is kept (the decode order read backwards). Built with
+    one key that takes all attention so every other column sum is exactly zero."""
+    for P, budget, kh in [(8, 4, 3), (10, 5, 2), (6, 6, 0), (9, 3, 3)]:
+        kl = budget - kh
+        q = np.ones((P, 1), dtype=np.float32)
+        k = np.full((P, 1), -1000.0, dtype=np.float32)
+        k[0] = 30.0
+        v = np.arange(P, dtype=np.float32)[:, None]
+        orc = oracle.Oracle(budget, kh, kl, lib_path=lib)
+        st = orc.new_state(1, 1, np.float32)
+        c, _ = orc.prefill_select(q[None], k[None], v[None], st, want_colsum=True)
+        assert c[0, 0] == P and not c[0, 1:].any()
+        tail = list(range(P - kl, P))
+        heavy = ([0] + list(range(P - kl - 1, P - kl - kh, -1)))[:kh] if kh else []
+        want = sorted(set(heavy) | set(tail)) if P > budget else list(range(P))
+        got = [int(p) for p in st.slot_pos[0] if p >= 0]
+        assert got == want, f"P={P} k={budget} kh={kh}: kept {got}, expected {want}"
+
+
+def pin_prompt_fits_budget(lib):
+    """A prompt no longer than the budget is kept whole, in order; unused slots are empty."""
+    rng = np.random.default_rng(16)
+    for P, budget in [(1, 1), (3, 5), (5, 5), (4, 9)]:
+        D = 4
+        q, k, v = tj.random_sequence(rng, P + 1, D, "bf16")
+        orc = oracle.Oracle(budget, budget // 2, budget - budget // 2, lib_path=lib)
+        st = orc.new_state(1, D, np.uint16)
+        st.k_cache[:] = 7
+        orc.prefill_select(q[None, :P], k[None, :P], v[None, :P], st)
+        assert list(st.slot_pos[0]) == list(range(P)) + [-1] * (budget - P)
+        assert np.array_equal(st.k_cache[0, :P], k[:P]) and np.array_equal(st.v_cache[0, :P], v[:P])
+        assert not st.k_cache[0, P:].any() and not st.scores[0, P:].any()
+
+
+def pin_bf16_is_exact_widening(lib):
+    """bf16 inputs give exactly the results of the same values passed as float32."""
+    rng = np.random.default_rng(17)
+    D, P, S, budget, kh, kl = 8, 10, 10, 5, 3, 2
+    q, k, v = tj.random_sequence(rng, P + S, D, "bf16", hh=2)
+    a = tj.run(lib, q, k, v, P, S, budget, kh, kl)
+    w = lambda x: bf.widen(x).astype(np.float32)
+    b = tj.run(lib, w(q), w(k), w(v), P, S, budget, kh, kl)
+    assert np.array_equal(a.colsum, b.colsum)
+    for ra, rb in zip(a.steps, b.steps):
+        assert np.array_equal(ra.out, rb.out) and np.array_equal(ra.scores_after, rb.scores_after)
+        assert np.array_equal(ra.slot_pos_after, rb.slot_pos_after)
+
+
+def pin_near_tie_adoption(lib):
+    """A preferred victim is adopted only when its score is within the tie tolerance."""
+    base = dict(slot_pos=[5, 8, 2, 9], t=10, kl=1)
+    budget = 4
+    orc = oracle.Oracle(budget, 3, 1, lib_path=lib)
+    for scores, prefer, tie, kind, victim in [
+        ([0.25, 0.5, 0.2500001, 0.75], 2, 1e-6, oracle.NEAR_TIE, 2),
+        ([0.25, 0.5, 0.2500001, 0.75], 2, 1e-8, oracle.REJECTED, 0),
+        ([0.25, 0.5, 0.25, 0.75], 0, 1e-6, oracle.REJECTED, 2),  # exact tie: by position
+        ([0.25, 0.5, 0.3, 0.75], 1, 1e-6, oracle.REJECTED, 0),
+    ]:
+        st = orc.new_state(1, 2, np.float32)
+        st.slot_pos[0] = base["slot_pos"]
+        st.scores[0] = scores
+        z = np.zeros((1, 2), dtype=np.float32)
+        _, es, _, _, infos = orc.decode_step(base["t"], z, z, z, st,
+                                             prefer_victim=np.array([prefer]), tie_rel=tie,
+                                             err_rel=tie)
+        assert infos[0].kind == kind and es[0] == victim, (scores, prefer, infos[0].kind, es[0])
+
+
+PINS = [pin_full_budget_is_dense, pin_no_heavy_is_sliding_window,
+        pin_victim_is_argmin_of_recomputed_scores, pin_uniform_attention_closed_form,
+        pin_mass_and_slot_invariants, pin_small_local_is_unprotected_argmin,
+        pin_hand_built_ties_and_protection, pin_prefill_equal_sums_keep_later, pin_prompt_fits_budget, pin_bf16_is_exact_widening,
+        pin_near_tie_adoption]
