@@ -1,0 +1,165 @@
+/*
+ * h2o.h -- C ABI of libh2o.so, the GB300 (sm_103a) hot path of H2O ("Heavy-Hitter Oracle")
+ * budgeted KV-cache eviction.
+ *
+ * The method (web pages on H2O, Zhang et al., NeurIPS 2023):
+ *   - ttsmallhot.github.io H2O post, §2.1.1: attention weights are Softmax(QK^T / sqrt(d));
+ *     §2.1.2: a token's accumulated attention score is the attention it has received;
+ *     §2.2: the KV budget k is split into k_local recent tokens and k_heavy heavy hitters; after each
+ *     new token its attention to every cached token is added to that token's score; when the cache is
+ *     full the recent tokens are kept and the lowest-scoring other token is evicted;
+ *     §2.3: the new token's K/V overwrites the evicted slot in place (no compaction);
+ *   - "H2O Heavy-Hitter Oracle 分析" (liuhc.cn), §3.1: per-head cumulative attention, heavy hitters
+ *     are its top-k; §3.2: victim = argmin(score), the new token is always admitted.
+ *
+ * Terms. A "unit" is one (layer, sequence, head); units are independent. dims.units_b counts
+ * (layer, sequence) rows, so there are units_b * heads units, laid out [units_b][heads].
+ * D = head_dim. Positions are absolute token indices (0-based); every unit has the same prompt
+ * length and the same current position (fixed-length padded prompts, as in the post's §3.2.2).
+ *
+ * Readings of the pages used throughout (the pages leave these open):
+ *   - logits are (q . k) / sqrt(D);
+ *   - step t attends the n = min(t, budget) cached slots plus the new token; the new token's own
+ *     weight is its initial score;
+ *   - scores are accumulated first, then the victim is chosen among cached slots whose position is
+ *     <= t - k_local (so positions t-k_local+1 .. t stay resident); the lowest updated score goes,
+ *     equal scores evict the lowest position;
+ *   - prefill keeps the last k_local prompt positions plus the k_heavy largest causal column sums of
+ *     Softmax(QK^T/sqrt(D)) among the rest (equal sums keep the later position); kept tokens fill
+ *     slots 0.. in ascending position, unused slots get position -1, score 0 and zero K/V rows.
+ *
+ * Memory. Every pointer argument is DEVICE memory owned by the caller, row-major and contiguous,
+ * 16-byte aligned (cudaMalloc / torch allocations are). Element type of q/k/v/out/caches is
+ * dims.dtype (H2O_F32: float, H2O_BF16: bfloat16); scores are float32; positions and indices are
+ * int32. The library allocates nothing per call; it keeps one 4-byte device error word per device,
+ * created on first use.
+ *
+ * Streams and errors. `stream` is a cudaStream_t (NULL = the legacy default stream); every call only
+ * enqueues work on it and returns without synchronising. Argument errors return
+ * H2O_ERR_INVALID_ARG or H2O_ERR_UNSUPPORTED before anything is launched; a failed launch returns
+ * H2O_ERR_CUDA. Conditions detected on the device (a bounded wait that ran out) are recorded in the
+ * device error word and reported by h2o_get_device_error. No C++ exception crosses this ABI.
+ * Calls that overlap on the GPU and touch the same cache race; order them on one stream.
+ */
+#ifndef H2O_H
+#define H2O_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define H2O_API __attribute__((visibility("default")))
+#else
+#define H2O_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  H2O_OK = 0,
+  H2O_ERR_INVALID_ARG = 1,  /* bad pointer, alignment, size or budget split                 */
+  H2O_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement (e.g. D = 96)    */
+  H2O_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed                          */
+  H2O_ERR_DEVICE = 4        /* the device error word was set (see h2o_get_device_error)      */
+} h2o_status;
+
+typedef enum { H2O_F32 = 0, H2O_BF16 = 1 } h2o_dtype;
+
+typedef struct {
+  int32_t units_b;   /* layers * batch: (layer, sequence) rows; 0 makes every call a no-op     */
+  int32_t heads;     /* heads per row, >= 1                                                   */
+  int32_t head_dim;  /* D: 64 or 128                                                          */
+  int32_t budget;    /* k: cached slots per unit, >= 1                                        */
+  int32_t k_heavy;   /* heavy-hitter share of the budget, >= 0                                */
+  int32_t k_local;   /* recent-token share, >= 0; k_heavy + k_local == budget                 */
+  int32_t dtype;     /* h2o_dtype of q/k/v/out and the K/V caches                             */
+} h2o_dims;
+
+/* Device error word values. */
+#define H2O_DEVERR_NONE 0
+#define H2O_DEVERR_WAIT_TIMEOUT 1   /* a bounded wait on a copy or a peer block gave up       */
+#define H2O_DEVERR_NO_CANDIDATE 2   /* no eviction candidate (cannot happen with valid state) */
+
+/* Bytes of device workspace h2o_prefill_scores / h2o_prefill_select need for this shape:
+ * three float32 arrays [units, prompt_len] (row max, row normaliser, column sums), each rounded
+ * up to 256 bytes. Returns 0 for invalid dims. */
+H2O_API size_t h2o_prefill_workspace_bytes(const h2o_dims* dims, int32_t prompt_len);
+
+/*
+ * Prefill score pass (the rows P1-P2 of the hot path): for every unit, the causal column sums
+ *   colsum[j] = sum_{i >= j} softmax_i(j),  softmax_i over j' <= i of (q_i . k_j') / sqrt(D),
+ * written as float32 [units, prompt_len] into `colsum` (device). Source: the post's §2.1.2 and §2.2
+ * (accumulated attention) and "H2O Heavy-Hitter Oracle 分析" §3.1 (cum_attn per head).
+ *   q, k        [units, prompt_len, D]  prompt queries and keys (device)
+ *   workspace   >= h2o_prefill_workspace_bytes(dims, prompt_len) bytes of device memory; its
+ *               contents on entry are ignored and on return are scratch
+ * 1 <= prompt_len <= 16384.
+ */
+H2O_API h2o_status h2o_prefill_scores(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                              const void* k, float* colsum, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Prefill score pass + selection + gather (rows P1-P4): computes the column sums as
+ * h2o_prefill_scores does, keeps min(prompt_len, budget) prompt tokens per unit (the last k_local
+ * positions plus the k_heavy largest column sums among the older ones) and fills the caches:
+ *   k_cache, v_cache   [units, budget, D]  kept K/V rows in ascending position, zero rows after
+ *   scores             [units, budget]     float32 column sum of each kept token, 0 after
+ *   slot_pos           [units, budget]     kept positions, ascending, -1 after
+ * Afterwards the caches are ready for h2o_decode_step at position = prompt_len.
+ * On return the workspace's column-sum array (offset 2 * round_up(4 * units * prompt_len, 256))
+ * holds the float32 column sums.
+ */
+H2O_API h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                              const void* k, const void* v, void* k_cache, void* v_cache,
+                              float* scores, int32_t* slot_pos, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * One budgeted decode step (rows D1-D7) at absolute position `position` (>= 1) for every unit,
+ * fused into one kernel launch. With n = min(position, budget) valid cached slots 0..n-1:
+ *   D2-D4  attends q over the n cached keys plus k_new:  out = softmax(q.K^T/sqrt(D)) V  [units, D]
+ *   D5     scores[j] += p_j (float32) for every cached slot j
+ *   D6     if n == budget: victim = argmin over slots with slot_pos <= position - k_local of
+ *          (updated score, position); evicted_slot = victim, evicted_pos = its old position;
+ *          otherwise no eviction: evicted_slot = evicted_pos = -1 and the new token goes to slot n
+ *   D7     the chosen slot gets K = k_new, V = v_new, score = p_new, slot_pos = position, in place
+ *   q, k_new, v_new    [units, D]
+ *   k_cache, v_cache   [units, budget, D]   read and updated in place
+ *   scores, slot_pos   [units, budget]      read and updated in place
+ *   out                [units, D]           written (dtype of q)
+ *   evicted_slot,
+ *   evicted_pos        [units] int32        written
+ * The cache state must be the one left by h2o_prefill_select (prompt_len <= position) and the
+ * previous decode steps, called with consecutive positions.
+ */
+H2O_API h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q,
+                           const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           float* scores, int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                           int32_t* evicted_pos, void* stream);
+
+/*
+ * Synchronises `stream`, reads the current device's error word into *code (if code != NULL) and
+ * clears it. Returns H2O_OK when the word was H2O_DEVERR_NONE, H2O_ERR_DEVICE when it was set, and
+ * H2O_ERR_CUDA if the synchronisation or copy failed.
+ */
+H2O_API h2o_status h2o_get_device_error(void* stream, int32_t* code);
+
+/*
+ * Self-test of the device-side bounded wait: launches one block that waits on a shared-memory
+ * barrier nothing ever completes, with a 50 ms limit. The wait gives up, sets the device error word
+ * to H2O_DEVERR_WAIT_TIMEOUT and the kernel returns normally; a following h2o_get_device_error
+ * reports it (and clears it). Nothing else is touched. Returns H2O_ERR_CUDA if the launch fails.
+ */
+H2O_API h2o_status h2o_selftest_wait_timeout(void* stream);
+
+/* Static, human-readable name of a status. */
+H2O_API const char* h2o_status_string(h2o_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H2O_H */

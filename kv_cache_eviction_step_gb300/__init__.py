@@ -1,0 +1,196 @@
+"""H2O (Heavy-Hitter Oracle) budgeted KV-cache eviction on GB300: Python binding of libh2o.so.
+
+Every step of the path runs in the library's CUDA kernels; this module only marshals arguments
+(device pointers taken from torch tensors, the current torch stream) into the C ABI declared in
+``include/h2o.h`` and turns a non-zero status into an exception. There is no CPU fallback: if the
+library cannot be loaded, every call raises.
+
+    dims = Dims(units_b=layers * batch, heads=H, head_dim=128, budget=204, k_heavy=102,
+                k_local=102, dtype=BF16)
+    cache = H2OCache(dims, prompt_len=512, device="cuda")
+    cache.prefill(q, k, v)                 # [units, P, D] each
+    out, ev_slot, ev_pos = cache.step(q_t, k_t, v_t)   # [units, D] each, position advances
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = range(5)
+DEVERR_NONE, DEVERR_WAIT_TIMEOUT, DEVERR_NO_CANDIDATE = range(3)
+
+EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
+           "h2o_decode_step", "h2o_get_device_error", "h2o_selftest_wait_timeout",
+           "h2o_status_string")
+
+
+class Dims(ctypes.Structure):
+    """``h2o_dims``: units_b = layers * batch rows of ``heads`` units each."""
+
+    _fields_ = [("units_b", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("budget", ctypes.c_int32),
+                ("k_heavy", ctypes.c_int32), ("k_local", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+    @property
+    def units(self) -> int:
+        return self.units_b * self.heads
+
+    def __repr__(self):
+        return ("Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
+
+
+class H2OError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+
+
+_lib: ctypes.CDLL | None = None
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libh2o.so from this package's ``_build`` directory (building it first if it is missing
+    and nvcc is available). Raises if the library cannot be loaded."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"libh2o.so not built ({path}); run kv_cache_eviction_step_gb300.build")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    dp = ctypes.POINTER(Dims)
+    lib.h2o_prefill_workspace_bytes.argtypes = [dp, i32]
+    lib.h2o_prefill_workspace_bytes.restype = sz
+    lib.h2o_prefill_scores.argtypes = [dp, i32, vp, vp, vp, vp, sz, vp]
+    lib.h2o_prefill_scores.restype = ctypes.c_int
+    lib.h2o_prefill_select.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.h2o_prefill_select.restype = ctypes.c_int
+    lib.h2o_decode_step.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.h2o_decode_step.restype = ctypes.c_int
+    lib.h2o_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.h2o_get_device_error.restype = ctypes.c_int
+    lib.h2o_selftest_wait_timeout.argtypes = [vp]
+    lib.h2o_selftest_wait_timeout.restype = ctypes.c_int
+    lib.h2o_status_string.argtypes = [ctypes.c_int]
+    lib.h2o_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().h2o_status_string(status).decode()
+
+
+def _ptr(x) -> int | None:
+    """Device address of a tensor (or an int address / None)."""
+    if x is None or isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _nbytes(x) -> int:
+    return x.numel() * x.element_size()
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise H2OError(fn, status)
+
+
+def h2o_prefill_workspace_bytes(dims: Dims, prompt_len: int) -> int:
+    return int(load().h2o_prefill_workspace_bytes(ctypes.byref(dims), prompt_len))
+
+
+def h2o_prefill_scores(dims: Dims, prompt_len: int, q, k, colsum, workspace, stream=None,
+                       workspace_bytes: int | None = None):
+    """Causal column sums of Softmax(QK^T/sqrt(D)) per unit into ``colsum`` [units, P] float32."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check("h2o_prefill_scores", load().h2o_prefill_scores(
+        ctypes.byref(dims), prompt_len, _ptr(q), _ptr(k), _ptr(colsum), _ptr(workspace), wb,
+        _stream(stream)))
+
+
+def h2o_prefill_select(dims: Dims, prompt_len: int, q, k, v, k_cache, v_cache, scores, slot_pos,
+                       workspace, stream=None, workspace_bytes: int | None = None):
+    """Prefill score pass, heavy-hitter + recent selection and gather into the budgeted caches."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check("h2o_prefill_select", load().h2o_prefill_select(
+        ctypes.byref(dims), prompt_len, _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+        _ptr(scores), _ptr(slot_pos), _ptr(workspace), wb, _stream(stream)))
+
+
+def h2o_decode_step(dims: Dims, position: int, q, k_new, v_new, k_cache, v_cache, scores,
+                    slot_pos, out, evicted_slot, evicted_pos, stream=None):
+    """One fused budgeted decode step at absolute ``position`` for every unit."""
+    _check("h2o_decode_step", load().h2o_decode_step(
+        ctypes.byref(dims), position, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+        _ptr(v_cache), _ptr(scores), _ptr(slot_pos), _ptr(out), _ptr(evicted_slot),
+        _ptr(evicted_pos), _stream(stream)))
+
+
+def h2o_get_device_error(stream=None) -> int:
+    """Synchronise ``stream``, return and clear the device error word (0 = none)."""
+    code = ctypes.c_int32(0)
+    st = load().h2o_get_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (OK, ERR_DEVICE):
+        raise H2OError("h2o_get_device_error", st)
+    return int(code.value)
+
+
+def h2o_selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (sets the device error word to DEVERR_WAIT_TIMEOUT)."""
+    _check("h2o_selftest_wait_timeout", load().h2o_selftest_wait_timeout(_stream(stream)))
+
+
+class H2OCache:
+    """Device buffers of one budgeted cache (caller-owned memory, allocated here with torch) and the
+    running position. A convenience wrapper over the ABI calls; it computes nothing itself."""
+
+    def __init__(self, dims: Dims, prompt_len: int, device="cuda"):
+        import torch
+        self.dims = dims
+        self.prompt_len = prompt_len
+        self.position = prompt_len
+        dt = torch.float32 if dims.dtype == F32 else torch.bfloat16
+        u, k, d = dims.units, dims.budget, dims.head_dim
+        self.dtype = dt
+        self.k_cache = torch.empty((u, k, d), dtype=dt, device=device)
+        self.v_cache = torch.empty((u, k, d), dtype=dt, device=device)
+        self.scores = torch.empty((u, k), dtype=torch.float32, device=device)
+        self.slot_pos = torch.empty((u, k), dtype=torch.int32, device=device)
+        self.workspace = torch.empty(h2o_prefill_workspace_bytes(dims, prompt_len), dtype=torch.uint8,
+                                     device=device)
+        self.out = torch.empty((u, d), dtype=dt, device=device)
+        self.evicted_slot = torch.empty(u, dtype=torch.int32, device=device)
+        self.evicted_pos = torch.empty(u, dtype=torch.int32, device=device)
+
+    def prefill(self, q, k, v, stream=None):
+        h2o_prefill_select(self.dims, self.prompt_len, q, k, v, self.k_cache, self.v_cache,
+                           self.scores, self.slot_pos, self.workspace, stream)
+        self.position = self.prompt_len
+
+    def step(self, q, k_new, v_new, out=None, evicted_slot=None, evicted_pos=None, stream=None):
+        out = self.out if out is None else out
+        es = self.evicted_slot if evicted_slot is None else evicted_slot
+        ep = self.evicted_pos if evicted_pos is None else evicted_pos
+        h2o_decode_step(self.dims, self.position, q, k_new, v_new, self.k_cache, self.v_cache,
+                        self.scores, self.slot_pos, out, es, ep, stream)
+        self.position += 1
+        return out, es, ep

@@ -1,0 +1,222 @@
+// h2o_abi.cu -- the extern "C" entry points of libh2o.so (declared in include/h2o.h): argument
+// validation, the per-device error word, workspace carving and the launches. Every check that can
+// fail happens before the first launch, so a rejected call has no effect on the GPU.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "h2o_internal.cuh"
+
+namespace h2o {
+namespace {
+
+__device__ int32_t g_error_word;
+
+// Device address of the error word for the current device (resolved once per device).
+int32_t* error_word() {
+  static std::mutex mu;
+  static std::vector<std::pair<int, int32_t*>> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& c : cache)
+    if (c.first == dev) return c.second;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+  cache.emplace_back(dev, static_cast<int32_t*>(ptr));
+  return static_cast<int32_t*>(ptr);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+h2o_status check_dims(const h2o_dims* d) {
+  if (d == nullptr) return H2O_ERR_INVALID_ARG;
+  if (d->units_b < 0 || d->heads < 1 || d->budget < 1 || d->k_heavy < 0 || d->k_local < 0)
+    return H2O_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(d->k_heavy) + d->k_local != d->budget) return H2O_ERR_INVALID_ARG;
+  if (d->dtype != H2O_F32 && d->dtype != H2O_BF16) return H2O_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return H2O_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->units_b) * d->heads > INT32_MAX / 16) return H2O_ERR_UNSUPPORTED;
+  return H2O_OK;
+}
+
+int elem_bytes(const h2o_dims* d) { return d->dtype == H2O_F32 ? 4 : 2; }
+
+h2o_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H2O_OK : H2O_ERR_CUDA; }
+
+// Waits on an mbarrier that nothing ever arrives at, with a short limit: exercises the bounded-wait
+// path (error word set, clean return) without any copy in flight.
+__global__ void wait_timeout_probe_kernel(int32_t* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err, limit_ns);
+}
+
+}  // namespace
+}  // namespace h2o
+
+using namespace h2o;
+
+extern "C" {
+
+const char* h2o_status_string(h2o_status status) {
+  switch (status) {
+    case H2O_OK: return "ok";
+    case H2O_ERR_INVALID_ARG: return "invalid argument";
+    case H2O_ERR_UNSUPPORTED: return "unsupported shape";
+    case H2O_ERR_CUDA: return "CUDA error";
+    case H2O_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+size_t h2o_prefill_workspace_bytes(const h2o_dims* dims, int32_t prompt_len) {
+  if (check_dims(dims) != H2O_OK || prompt_len < 1) return 0;
+  const size_t units = static_cast<size_t>(dims->units_b) * dims->heads;
+  return 3 * round256(units * static_cast<size_t>(prompt_len) * 4);
+}
+
+static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                                      const void* k, float* colsum, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+  const int units = dims->units_b * dims->heads;
+  const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
+  PrefillParams p = {};
+  p.q = q;
+  p.k = k;
+  p.row_max = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace));
+  p.row_sum = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + arr);
+  p.colsum = colsum;
+  p.err = error_word();
+  if (p.err == nullptr) return H2O_ERR_CUDA;
+  p.units = units;
+  p.P = prompt_len;
+  p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
+  (void)workspace_bytes;
+  return from_cuda(launch_prefill_scores_simt(p, dims->head_dim, dims->dtype, stream));
+}
+
+static h2o_status check_prefill(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                                const void* k, void* workspace, size_t workspace_bytes) {
+  h2o_status st = check_dims(dims);
+  if (st != H2O_OK) return st;
+  if (prompt_len < 1) return H2O_ERR_INVALID_ARG;
+  if (prompt_len > select_max_prompt()) return H2O_ERR_UNSUPPORTED;
+  if (dims->units_b == 0) return H2O_OK;
+  if (!q || !k || !workspace || !aligned16(q) || !aligned16(k) || !aligned16(workspace))
+    return H2O_ERR_INVALID_ARG;
+  if (workspace_bytes < h2o_prefill_workspace_bytes(dims, prompt_len)) return H2O_ERR_INVALID_ARG;
+  return H2O_OK;
+}
+
+h2o_status h2o_prefill_scores(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                              const void* k, float* colsum, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
+  if (st != H2O_OK) return st;
+  if (dims->units_b == 0) return H2O_OK;
+  if (!colsum || !aligned16(colsum)) return H2O_ERR_INVALID_ARG;
+  return prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes,
+                             static_cast<cudaStream_t>(stream));
+}
+
+h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                              const void* k, const void* v, void* k_cache, void* v_cache,
+                              float* scores, int32_t* slot_pos, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
+  if (st != H2O_OK) return st;
+  if (dims->budget > select_max_budget()) return H2O_ERR_UNSUPPORTED;
+  if (dims->units_b == 0) return H2O_OK;
+  if (!v || !k_cache || !v_cache || !scores || !slot_pos) return H2O_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(scores) ||
+      !aligned16(slot_pos))
+    return H2O_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int units = dims->units_b * dims->heads;
+  const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
+  float* colsum = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + 2 * arr);
+  st = prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes, s);
+  if (st != H2O_OK) return st;
+  SelectParams p = {};
+  p.colsum = colsum;
+  p.k = k;
+  p.v = v;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.scores = scores;
+  p.slot_pos = slot_pos;
+  p.units = units;
+  p.P = prompt_len;
+  p.budget = dims->budget;
+  p.k_heavy = dims->k_heavy;
+  p.k_local = dims->k_local;
+  p.row_bytes = dims->head_dim * elem_bytes(dims);
+  return from_cuda(launch_select(p, s));
+}
+
+h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q,
+                           const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           float* scores, int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                           int32_t* evicted_pos, void* stream) {
+  h2o_status st = check_dims(dims);
+  if (st != H2O_OK) return st;
+  if (position < 1) return H2O_ERR_INVALID_ARG;
+  if (dims->units_b == 0) return H2O_OK;
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, scores, slot_pos, out, evicted_slot, evicted_pos};
+  for (const void* ptr : ptrs)
+    if (ptr == nullptr || !aligned16(ptr)) return H2O_ERR_INVALID_ARG;
+  DecodeParams p = {};
+  p.q = q;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.scores = scores;
+  p.slot_pos = slot_pos;
+  p.out = out;
+  p.evicted_slot = evicted_slot;
+  p.evicted_pos = evicted_pos;
+  p.err = error_word();
+  if (p.err == nullptr) return H2O_ERR_CUDA;
+  p.units = dims->units_b * dims->heads;
+  p.budget = dims->budget;
+  p.k_local = dims->k_local;
+  p.position = position;
+  p.n = position < dims->budget ? position : dims->budget;
+  p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
+  size_t smem = 0;
+  if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem))
+    return H2O_ERR_UNSUPPORTED;
+  return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+h2o_status h2o_selftest_wait_timeout(void* stream) {
+  int32_t* word = error_word();
+  if (word == nullptr) return H2O_ERR_CUDA;
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word, 50000000ull);
+  return from_cuda(cudaGetLastError());
+}
+
+h2o_status h2o_get_device_error(void* stream, int32_t* code) {
+  int32_t* word = error_word();
+  if (word == nullptr) return H2O_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess) return H2O_ERR_CUDA;
+  if (cudaMemsetAsync(word, 0, sizeof host, s) != cudaSuccess) return H2O_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return H2O_ERR_CUDA;
+  if (code) *code = host;
+  return host == H2O_DEVERR_NONE ? H2O_OK : H2O_ERR_DEVICE;
+}
+
+}  // extern "C"

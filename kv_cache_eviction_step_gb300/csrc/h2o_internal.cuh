@@ -1,0 +1,171 @@
+// h2o_internal.cuh -- shared internals of libh2o.so: launch-parameter structs, launcher
+// declarations and the small PTX helpers (mbarrier, bulk async copy, bounded waits) the sm_103a
+// kernels use. Not part of the public ABI (include/h2o.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/h2o.h"
+
+namespace h2o {
+
+// ---- launch parameters --------------------------------------------------------------------
+
+struct DecodeParams {
+  const void* q;        // [units, D]
+  const void* k_new;    // [units, D]
+  const void* v_new;    // [units, D]
+  void* k_cache;        // [units, budget, D]
+  void* v_cache;        // [units, budget, D]
+  float* scores;        // [units, budget]
+  int32_t* slot_pos;    // [units, budget]
+  void* out;            // [units, D]
+  int32_t* evicted_slot;  // [units]
+  int32_t* evicted_pos;   // [units]
+  int32_t* err;         // device error word
+  int32_t units;
+  int32_t budget;
+  int32_t k_local;
+  int32_t position;     // t
+  int32_t n;            // min(t, budget) valid cached slots
+  int32_t splits;       // CTAs (one cluster) per unit
+  int32_t chunk;        // cached slots per CTA
+  int32_t stages;       // ring depth in tiles
+  float scale;          // 1/sqrt(D)
+};
+
+struct PrefillParams {
+  const void* q;        // [units, P, D]
+  const void* k;        // [units, P, D]
+  float* row_max;       // [units, P]
+  float* row_sum;       // [units, P]
+  float* colsum;        // [units, P]
+  int32_t* err;
+  int32_t units;
+  int32_t P;
+  float scale;
+};
+
+struct SelectParams {
+  const float* colsum;  // [units, P]
+  const void* k;        // [units, P, D]
+  const void* v;        // [units, P, D]
+  void* k_cache;        // [units, budget, D]
+  void* v_cache;
+  float* scores;        // [units, budget]
+  int32_t* slot_pos;    // [units, budget]
+  int32_t units;
+  int32_t P;
+  int32_t budget;
+  int32_t k_heavy;
+  int32_t k_local;
+  int32_t row_bytes;    // D * element size
+};
+
+// ---- launchers (host) ---------------------------------------------------------------------
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int dtype, cudaStream_t s);
+cudaError_t launch_prefill_scores_simt(const PrefillParams& p, int head_dim, int dtype, cudaStream_t s);
+cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
+int select_max_prompt();
+int select_max_budget();
+
+// Chooses how many CTAs (one thread-block cluster) share one unit's decode step and how many slots
+// each CTA owns; also the ring depth. Returns false if no launchable shape exists.
+bool plan_decode(int units, int n, int head_dim, int elem_bytes, int* splits, int* chunk,
+                 int* stages, size_t* smem_bytes);
+
+// ---- device helpers -----------------------------------------------------------------------
+
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One bulk (TMA-engine) copy of `bytes` contiguous bytes global -> this CTA's shared memory;
+// completion is signalled on `bar` as transaction bytes. Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns` of wall time (2 s by
+// default): then the device error word is set and false is returned, so no wait in this library
+// can hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          uint64_t limit_ns = 2000000000ull) {
+  const uint32_t addr = smem_u32(bar);
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (it == 0) start = now;
+      else if (now - start > limit_ns) {
+        atomicCAS(err, H2O_DEVERR_NONE, H2O_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Address of the same shared-memory object in the CTA of rank `rank` of this cluster.
+template <typename T>
+__device__ __forceinline__ const T* peer_ptr(const T* local, uint32_t rank) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<const T*>(out);
+}
+
+// bf16 -> f32 of the low / high half of a 32-bit word (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+#endif  // __CUDACC__
+
+}  // namespace h2o

@@ -64,6 +64,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.h2o_oracle_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                            vp, vp, vp, vp, vp, vp, f64, f64, vp]
     lib.h2o_oracle_decode_step.restype = ctypes.c_int
+    lib.h2o_oracle_run_unit.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                        ctypes.c_int64, vp, vp, vp, vp, vp]
+    lib.h2o_oracle_run_unit.restype = ctypes.c_int
     return lib
 
 
@@ -154,3 +157,20 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"h2o_oracle_decode_step rejected its arguments (code {rc})")
         return out, ev_slot, ev_pos, probs, infos[:units]
+
+    def run_unit(self, q, k, v, q_dec, k_dec, v_dec, state: State, unit: int = 0):
+        """One unit's prefill + decode steps in one call (for timing). q/k/v: [P, D] of the unit;
+        q_dec/k_dec/v_dec: [S, units, D] arrays, the unit's rows taken at index ``unit``."""
+        q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+        P, D = q.shape
+        S, nu, _ = q_dec.shape
+        for a in (q_dec, k_dec, v_dec):
+            assert a.flags.c_contiguous
+        off = unit * D * q_dec.itemsize
+        base = lambda a: ctypes.c_void_p(a.ctypes.data + off)
+        rc = self.lib.h2o_oracle_run_unit(
+            D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), P, S, _ptr(q), _ptr(k),
+            _ptr(v), base(q_dec), base(k_dec), base(v_dec), nu * D, _ptr(state.k_cache),
+            _ptr(state.v_cache), _ptr(state.scores), _ptr(state.slot_pos), None)
+        if rc != 0:
+            raise ValueError(f"h2o_oracle_run_unit failed (code {rc})")

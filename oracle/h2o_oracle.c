@@ -341,3 +341,28 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
   free(qv); free(s); free(p);
   return 0;
 }
+
+/* ---- timing driver: one unit's prefill and decode steps back to back ----------------------- */
+
+int h2o_oracle_run_unit(int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local, int32_t dtype,
+                        int32_t P, int32_t steps, const void* q, const void* k, const void* v,
+                        const void* q_dec, const void* k_dec, const void* v_dec, int64_t dec_stride,
+                        void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
+                        double* out) {
+  int rc = h2o_oracle_prefill_select(1, D, budget, k_heavy, k_local, dtype, P, q, k, v, k_cache,
+                                     v_cache, scores, slot_pos, NULL, NULL, 0.0, 0.0, NULL);
+  if (rc) return rc;
+  const size_t eb = elem_bytes(dtype);
+  double* tmp = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!tmp) return -9;
+  for (int32_t s = 0; s < steps && rc == 0; ++s) {
+    const size_t off = (size_t)s * (size_t)dec_stride * eb;
+    rc = h2o_oracle_decode_step(1, D, budget, k_heavy, k_local, dtype, P + s,
+                                (const char*)q_dec + off, (const char*)k_dec + off,
+                                (const char*)v_dec + off, k_cache, v_cache, scores, slot_pos,
+                                out ? out + (size_t)s * D : tmp, NULL, NULL, NULL, NULL, 0.0, 0.0,
+                                NULL);
+  }
+  free(tmp);
+  return rc;
+}

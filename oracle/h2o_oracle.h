@@ -84,6 +84,20 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
                            const int32_t* prefer_victim, double tie_rel, double err_rel,
                            h2o_oracle_step_info* infos);
 
+/*
+ * Convenience driver for timing: one unit's whole job, i.e. h2o_oracle_prefill_select on its prompt
+ * followed by `steps` calls of h2o_oracle_decode_step at positions P, P+1, ... It adds no arithmetic.
+ *   q, k, v                [P, D]         the unit's prompt
+ *   q_dec, k_dec, v_dec    step s's row at offset s * dec_stride elements
+ *   k_cache, v_cache       [budget, D];  scores, slot_pos [budget]   the unit's state (written)
+ *   out                    [steps, D] float64 or NULL
+ */
+int h2o_oracle_run_unit(int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local, int32_t dtype,
+                        int32_t P, int32_t steps, const void* q, const void* k, const void* v,
+                        const void* q_dec, const void* k_dec, const void* v_dec, int64_t dec_stride,
+                        void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
+                        double* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,195 @@
+"""GPU-vs-oracle parity harness (test infrastructure).
+
+The CUDA path (through the C ABI, ``kv_cache_eviction_step_gb300``) runs every unit of a workload
+in the real launch shape; the CPU oracle runs a chosen subset of units on the same seeded inputs,
+step by step. Per step the harness compares the attention outputs (within the dtype's tolerance)
+and the eviction decisions (exactly). Where the oracle's two lowest candidate scores differ by less
+than ``TIE_REL`` (relative) the decision is a logged near-tie: the oracle follows the GPU's choice
+if, and only if, that choice is one of the near-tied candidates, so that one benign tie does not
+desynchronise every later step. Decisions within the wider float32 error bound ``ERR_REL`` are
+logged separately ("error-bound ties"). Anything else is a mismatch.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle
+import synth
+
+TIE_REL = 1e-6  # near-tie threshold on scores (relative)
+ERR_REL = 2e-5  # float32 accumulation-order bound: adopted but counted separately
+OUT_TOL = {"bf16": 2e-2, "f32": 1e-5}
+
+
+def score_rtol(steps: int) -> float:
+    """Relative tolerance of a float32 accumulated score after ``steps`` additions: each addition
+    rounds once on each side (2^-24 each) and the GPU's float32 p_j differs from the oracle's
+    float64-rounded p_j by a few ulps; the bound grows linearly in the worst case."""
+    return 1e-6 + 8.0 * (steps + 1) * 2.0 ** -24
+
+
+@dataclasses.dataclass
+class Report:
+    workload: str
+    units_checked: int
+    steps: int
+    decisions: int = 0
+    near_ties: int = 0
+    error_bound_ties: int = 0
+    mismatches: int = 0
+    prefill_near_ties: int = 0
+    prefill_error_bound: int = 0
+    prefill_mismatches: int = 0
+    max_out_err: float = 0.0
+    max_score_rel_err: float = 0.0
+    notes: list = dataclasses.field(default_factory=list)
+
+    def ok(self) -> bool:
+        return self.mismatches == 0 and self.prefill_mismatches == 0 and not self.notes
+
+
+def dims_of(w: synth.Workload):
+    import kv_cache_eviction_step_gb300 as h2o
+    return h2o.Dims(units_b=w.units_b, heads=w.heads, head_dim=w.head_dim, budget=w.budget,
+                    k_heavy=w.k_heavy, k_local=w.k_local,
+                    dtype=h2o.F32 if w.dtype == "f32" else h2o.BF16)
+
+
+def to_device(a: np.ndarray, dtype: str):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                         np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.bfloat16)
+    return t.cuda()
+
+
+def to_host(t, dtype: str) -> np.ndarray:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def widen(a: np.ndarray) -> np.ndarray:
+    return synth.bf16_bits_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int = synth.DEFAULT_SEED,
+        chunk_steps: int = 4096, state_every: int = 0, property_checks=None) -> Report:
+    """Run ``steps`` decode steps (default: all) of workload ``w`` on the GPU for every unit, and the
+    oracle in lockstep on ``check_units`` (default: all units)."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+
+    steps = w.decode_steps if steps is None else steps
+    if state_every:
+        chunk_steps = min(chunk_steps, state_every)  # the GPU state is read at chunk ends
+    U, D, P, k = w.units, w.head_dim, w.prompt_len, w.budget
+    check_units = np.arange(U) if check_units is None else np.asarray(check_units)
+    rep = Report(w.name, len(check_units), steps)
+    dims = dims_of(w)
+    cache = h2o.H2OCache(dims, P)
+
+    # Prefill for every unit on the GPU.
+    prompt = synth.generate(w, seed, steps=0)
+    q, kk, v = (to_device(a, w.dtype) for a in (prompt.q_prompt, prompt.k_prompt, prompt.v_prompt))
+    cache.prefill(q, kk, v)
+    del q, kk, v
+    torch.cuda.synchronize()
+    assert h2o.h2o_get_device_error() == 0
+
+    # Oracle prefill on the checked units, following the GPU's kept set only at near ties.
+    follow = len(check_units) > 0
+    orc = oracle.Oracle(k, w.k_heavy, w.k_local)
+    st = orc.new_state(len(check_units), D, synth.storage_dtype(w))
+    if follow:
+        gpu_pos = to_host(cache.slot_pos, "i32")[check_units]
+        _, pinfo = orc.prefill_select(prompt.q_prompt[check_units], prompt.k_prompt[check_units],
+                                      prompt.v_prompt[check_units], st, prefer_pos=gpu_pos,
+                                      tie_rel=TIE_REL, err_rel=ERR_REL)
+        for i in pinfo:
+            rep.prefill_near_ties += i.kind == oracle.NEAR_TIE
+            rep.prefill_error_bound += i.kind == oracle.ERROR_BOUND
+            rep.prefill_mismatches += i.kind == oracle.REJECTED
+        compare_state(rep, w, cache, st, check_units, 0)
+    del prompt
+
+    idx = torch.as_tensor(check_units, device="cuda", dtype=torch.long)
+    s0 = 0
+    while s0 < steps:
+        ns = min(chunk_steps, steps - s0)
+        chunk = synth.generate(w, seed, step0=s0, steps=ns, prompt=False)
+        dq, dk, dv = (to_device(a, w.dtype) for a in (chunk.q_dec, chunk.k_dec, chunk.v_dec))
+        outs = torch.empty((ns, len(check_units), D), dtype=cache.dtype, device="cuda")
+        evs = torch.empty((ns, U), dtype=torch.int32, device="cuda")
+        evp = torch.empty((ns, U), dtype=torch.int32, device="cuda")
+        for s in range(ns):
+            cache.step(dq[s], dk[s], dv[s], evicted_slot=evs[s], evicted_pos=evp[s])
+            if follow:
+                outs[s] = cache.out.index_select(0, idx)
+        torch.cuda.synchronize()
+        err = h2o.h2o_get_device_error()
+        if err:
+            rep.notes.append(f"device error word {err}")
+            return rep
+        outs_h = widen(to_host(outs, w.dtype))
+        evs_h, evp_h = to_host(evs, "i32"), to_host(evp, "i32")
+        for s in range(ns if follow else 0):
+            t = P + s0 + s
+            o_out, o_es, o_ep, _, infos = orc.decode_step(
+                t, chunk.q_dec[s][check_units], chunk.k_dec[s][check_units],
+                chunk.v_dec[s][check_units], st, prefer_victim=evs_h[s][check_units],
+                tie_rel=TIE_REL, err_rel=ERR_REL)
+            e = float(np.max(np.abs(outs_h[s] - o_out)))
+            rep.max_out_err = max(rep.max_out_err, e)
+            if e > OUT_TOL[w.dtype] and len(rep.notes) < 10:
+                rep.notes.append(f"t={t}: output error {e:.3e}")
+            for j, inf in enumerate(infos):
+                if inf.kind == oracle.NO_EVICTION:
+                    if evs_h[s][check_units[j]] != -1 or evp_h[s][check_units[j]] != -1:
+                        rep.mismatches += 1
+                    continue
+                rep.decisions += 1
+                rep.near_ties += inf.kind == oracle.NEAR_TIE
+                rep.error_bound_ties += inf.kind == oracle.ERROR_BOUND
+                if inf.kind == oracle.REJECTED or o_ep[j] != evp_h[s][check_units[j]] \
+                        or o_es[j] != evs_h[s][check_units[j]]:
+                    rep.mismatches += 1
+                    if len(rep.notes) < 10:
+                        rep.notes.append(f"t={t} unit {check_units[j]}: gpu victim "
+                                         f"{evs_h[s][check_units[j]]}, oracle {o_es[j]} "
+                                         f"(kind {oracle.KIND_NAMES[inf.kind]}, gap {inf.gap_rel:.2e})")
+        if follow and state_every:
+            compare_state(rep, w, cache, st, check_units, s0 + ns)
+        if property_checks is not None:
+            property_checks(cache, P + s0 + ns - 1)
+        s0 += ns
+        del dq, dk, dv, outs, evs, evp
+    if follow:
+        compare_state(rep, w, cache, st, check_units, steps)
+    return rep
+
+
+def compare_state(rep: Report, w, cache, st: oracle.State, check_units, steps_done: int):
+    """Slot map and K/V rows must be identical; scores within the accumulation tolerance."""
+    sp = to_host(cache.slot_pos, "i32")[check_units]
+    if not np.array_equal(sp, st.slot_pos):
+        bad = np.argwhere(sp != st.slot_pos)
+        rep.notes.append(f"after {steps_done} steps: slot map differs at {bad[:5].tolist()}")
+        return
+    kc = to_host(cache.k_cache, w.dtype)[check_units]
+    vc = to_host(cache.v_cache, w.dtype)[check_units]
+    if not (np.array_equal(kc, st.k_cache) and np.array_equal(vc, st.v_cache)):
+        rep.notes.append(f"after {steps_done} steps: K/V cache rows differ")
+    sc = to_host(cache.scores, "f32")[check_units].astype(np.float64)
+    ref = st.scores.astype(np.float64)
+    rel = np.abs(sc - ref) / np.maximum(np.abs(ref), 1e-6)
+    rep.max_score_rel_err = max(rep.max_score_rel_err, float(rel.max(initial=0.0)))
+    if float(rel.max(initial=0.0)) > score_rtol(steps_done) + 1e-5:
+        rep.notes.append(f"after {steps_done} steps: score rel err {rel.max():.3e} > "
+                         f"{score_rtol(steps_done) + 1e-5:.3e}")

@@ -1,0 +1,110 @@
+"""Host-side checks of libh2o.so: it builds for sm_103a, loads, exports every symbol include/h2o.h
+declares, and rejects bad arguments before any CUDA call (so these run without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import kv_cache_eviction_step_gb300 as h2o
+from kv_cache_eviction_step_gb300 import build as h2o_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    h2o_build.build()
+    return h2o.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "h2o.h")).read()
+    return re.findall(r"H2O_API\s+[\w\s\*]+?\b(h2o_\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    assert set(names) == set(h2o.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)
+
+
+def test_only_the_abi_is_exported(lib):
+    out = os.popen(f"nm -D --defined-only {h2o_build.LIB}").read()
+    syms = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert {s for s in syms if s.startswith("h2o_")} == set(h2o.EXPORTS)
+
+
+def test_status_strings(lib):
+    assert h2o.status_string(h2o.OK) == "ok"
+    assert "invalid" in h2o.status_string(h2o.ERR_INVALID_ARG)
+    assert h2o.status_string(99) == "unknown status"
+
+
+def dims(**kw):
+    base = dict(units_b=2, heads=4, head_dim=128, budget=8, k_heavy=4, k_local=4, dtype=h2o.BF16)
+    base.update(kw)
+    return h2o.Dims(**base)
+
+
+def test_workspace_bytes(lib):
+    d = dims()
+    units, P = 8, 100
+    per = (units * P * 4 + 255) // 256 * 256
+    assert h2o.h2o_prefill_workspace_bytes(d, P) == 3 * per
+    assert h2o.h2o_prefill_workspace_bytes(dims(k_heavy=5), P) == 0
+    assert h2o.h2o_prefill_workspace_bytes(d, 0) == 0
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(k_heavy=5), h2o.ERR_INVALID_ARG),          # k_heavy + k_local != budget
+    (dict(budget=0, k_heavy=0, k_local=0), h2o.ERR_INVALID_ARG),
+    (dict(k_local=-1, k_heavy=9), h2o.ERR_INVALID_ARG),
+    (dict(heads=0), h2o.ERR_INVALID_ARG),
+    (dict(dtype=7), h2o.ERR_INVALID_ARG),
+    (dict(head_dim=96), h2o.ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_dims(lib, bad, status):
+    d = dims(**bad)
+    rc = lib.h2o_decode_step(ctypes.byref(d), 10, *([16] * 10), None)
+    assert rc == status
+
+
+def test_decode_rejects_null_misaligned_and_position(lib):
+    d = dims()
+    ptrs = [4096 * (i + 1) for i in range(10)]
+    assert lib.h2o_decode_step(ctypes.byref(d), 0, *ptrs, None) == h2o.ERR_INVALID_ARG
+    for i in range(10):
+        p = list(ptrs)
+        p[i] = None
+        assert lib.h2o_decode_step(ctypes.byref(d), 10, *p, None) == h2o.ERR_INVALID_ARG
+        p[i] = ptrs[i] + 8
+        assert lib.h2o_decode_step(ctypes.byref(d), 10, *p, None) == h2o.ERR_INVALID_ARG
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    d = dims()
+    ws = h2o.h2o_prefill_workspace_bytes(d, 64)
+    args = [4096 * (i + 1) for i in range(7)]
+    # prompt length out of range
+    assert lib.h2o_prefill_select(ctypes.byref(d), 0, *args, 4096, ws * 10, None) == h2o.ERR_INVALID_ARG
+    assert lib.h2o_prefill_select(ctypes.byref(d), 16385, *args, 4096, 1 << 40, None) == h2o.ERR_UNSUPPORTED
+    # workspace too small
+    assert lib.h2o_prefill_select(ctypes.byref(d), 64, *args, 4096, ws - 1, None) == h2o.ERR_INVALID_ARG
+    # misaligned cache pointer
+    bad = list(args)
+    bad[3] += 4
+    assert lib.h2o_prefill_select(ctypes.byref(d), 64, *bad, 4096, ws, None) == h2o.ERR_INVALID_ARG
+    assert lib.h2o_prefill_scores(ctypes.byref(d), 64, 4096, 8192, None, 4096, ws, None) == h2o.ERR_INVALID_ARG
+
+
+def test_zero_units_is_a_noop(lib):
+    d = dims(units_b=0)
+    assert lib.h2o_decode_step(ctypes.byref(d), 10, *([None] * 10), None) == h2o.OK
+    assert lib.h2o_prefill_select(ctypes.byref(d), 64, *([None] * 7), None, 0, None) == h2o.OK

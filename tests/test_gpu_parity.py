@@ -1,0 +1,225 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on the same seeded inputs (needs a GB300)."""
+
+import numpy as np
+import pytest
+
+import oracle
+import parity
+import synth
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+def _assert(rep: parity.Report):
+    msg = (f"{rep.workload}: {rep.mismatches} mismatches / {rep.decisions} decisions, "
+           f"near ties {rep.near_ties}, error-bound ties {rep.error_bound_ties}, prefill "
+           f"mismatches {rep.prefill_mismatches}, max out err {rep.max_out_err:.2e}, max score rel "
+           f"err {rep.max_score_rel_err:.2e}, notes {rep.notes}")
+    print(msg)
+    assert rep.ok(), msg
+    assert rep.error_bound_ties <= max(2, rep.decisions // 1000), msg
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    h2o.load()
+    torch.cuda.init()
+    yield
+    assert h2o.h2o_get_device_error() == 0
+
+
+def test_tiny_workload_every_unit_every_step():
+    """batch 1, 2 heads, d=64 fp32, 64+64, k=32 (16+16): the whole workload against the oracle."""
+    _assert(parity.run(W["tiny"], state_every=8))
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("opt-6.7b", dict(layers=1, batch=2, heads=3)),
+    ("llama-7b", dict(batch=1, heads=3)),
+    ("opt-30b", dict(batch=1, heads=3)),
+    ("streaming", dict(heads=2, decode_steps=4800)),
+])
+def test_workload_shapes_on_few_units(name, kw):
+    """Each workload's prompt length, budget split, head dim and dtype on a few units, so the oracle
+    runs every unit; few units also make the decode step split each unit over a CTA cluster."""
+    w = W[name].with_(**kw)
+    _assert(parity.run(w, state_every=128))
+
+
+def _sweep_cases():
+    rng = np.random.default_rng(7)
+    cases = []
+    for i in range(14):
+        D = int(rng.choice([64, 128]))
+        dtype = "f32" if i % 3 == 0 else "bf16"
+        budget = int(rng.choice([1, 2, 5, 17, 33, 63, 100, 129]))
+        regime = i % 4
+        P = {0: max(1, budget // 2), 1: budget, 2: budget + 1 + int(rng.integers(0, 60)),
+             3: int(rng.integers(1, 3 * budget + 2))}[regime]
+        kl = int(rng.choice([0, 1, budget, budget // 2]))
+        units_b = int(rng.choice([1, 3, 40, 200]))
+        heads = int(rng.choice([1, 2, 5]))
+        cases.append(synth.Workload(
+            f"sweep{i}", layers=1, batch=units_b, heads=heads, head_dim=D, dtype=dtype,
+            prompt_len=P, decode_steps=int(rng.integers(1, 70)), budget=budget,
+            k_heavy=budget - kl, k_local=kl, hh_kind="pareto",
+            hh_count=max(1, (P + 70) // 20), q_boost=1.0))
+    return cases
+
+
+@pytest.mark.parametrize("w", _sweep_cases(), ids=lambda w: f"{w.name}-D{w.head_dim}-{w.dtype}-k{w.budget}"
+                         f"-kl{w.k_local}-P{w.prompt_len}-u{w.units}")
+def test_sweep(w):
+    """Odd budgets, prompts shorter / equal / longer than the budget, k_local in {0, 1, k/2, k},
+    D in {64, 128}, fp32 and bf16, 1 to 1000 units (1 to 16 CTAs per unit)."""
+    check = None if w.units <= 64 else np.linspace(0, w.units - 1, 24).astype(int)
+    _assert(parity.run(w, check_units=check, state_every=16))
+
+
+def test_prefill_column_sums_elementwise():
+    """P1-P2 alone: h2o_prefill_scores against the oracle's float64 column sums, every element."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    for name, kw in [("opt-6.7b", dict(layers=1, batch=1, heads=4)), ("tiny", {}),
+                     ("llama-7b", dict(batch=1, heads=2)), ("opt-30b", dict(batch=1, heads=2, prompt_len=333))]:
+        w = W[name].with_(**kw)
+        inp = synth.generate(w, steps=0)
+        dims = parity.dims_of(w)
+        q, k = parity.to_device(inp.q_prompt, w.dtype), parity.to_device(inp.k_prompt, w.dtype)
+        colsum = torch.empty((w.units, w.prompt_len), dtype=torch.float32, device="cuda")
+        ws = torch.empty(h2o.h2o_prefill_workspace_bytes(dims, w.prompt_len), dtype=torch.uint8, device="cuda")
+        h2o.h2o_prefill_scores(dims, w.prompt_len, q, k, colsum, ws)
+        got = colsum.cpu().numpy().astype(np.float64)
+        orc = oracle.Oracle(w.budget, w.k_heavy, w.k_local)
+        st = orc.new_state(w.units, w.head_dim, synth.storage_dtype(w))
+        ref, _ = orc.prefill_select(inp.q_prompt, inp.k_prompt, inp.v_prompt, st, want_colsum=True)
+        rel = np.abs(got - ref) / np.maximum(ref, 1e-3)
+        assert rel.max() < 2e-5, (name, rel.max())
+        assert np.allclose(got.sum(axis=1), w.prompt_len, rtol=1e-5)
+
+
+def test_exact_ties_evict_lowest_position():
+    """Hand-built full caches whose updated scores tie exactly (all-zero keys and queries give
+    equal weights): the GPU must evict the lowest position, like the oracle."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    budget, D = 8, 64
+    for kl, pos, sc, want in [
+        (1, [7, 3, 9, 5, 12, 4, 11, 10], [0.5] * 8, 1),                         # lowest position 3
+        (3, [12, 3, 14, 5, 2, 9, 13, 10], [0.25] * 8, 4),                       # 2 (13, 14 protected)
+        (2, [5, 8, 2, 9, 10, 11, 12, 13], [0.25, 0.5, 0.25, 0.75, 1, 1, 1, 1], 2),  # tie 5 vs 2 -> 2
+        (8, [7, 6, 9, 8, 10, 11, 12, 13], [0.0, 9.0, 0, 0, 0, 0, 0, 0], 1),     # window: only 6
+    ]:
+        d = h2o.Dims(units_b=1, heads=1, head_dim=D, budget=budget, k_heavy=budget - kl, k_local=kl,
+                     dtype=h2o.BF16)
+        t = 14
+        z = torch.zeros((1, D), dtype=torch.bfloat16, device="cuda")
+        kc = torch.zeros((1, budget, D), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        scores = torch.tensor([sc], dtype=torch.float32, device="cuda")
+        sp = torch.tensor([pos], dtype=torch.int32, device="cuda")
+        out = torch.empty_like(z)
+        es = torch.empty(1, dtype=torch.int32, device="cuda")
+        ep = torch.empty_like(es)
+        h2o.h2o_decode_step(d, t, z, z, z + 1, kc, vc, scores, sp, out, es, ep)
+        torch.cuda.synchronize()
+        assert es.item() == want and ep.item() == pos[want], (kl, es.item(), ep.item())
+        assert sp[0, want].item() == t
+        assert torch.all(vc[0, want] == 1)
+        # oracle on the same state agrees
+        orc = oracle.Oracle(budget, budget - kl, kl)
+        st = orc.new_state(1, D, np.uint16)
+        st.slot_pos[0], st.scores[0] = pos, sc
+        zz = np.zeros((1, D), dtype=np.uint16)
+        _, oes, _, _, _ = orc.decode_step(t, zz, zz, zz, st)
+        assert oes[0] == want
+        assert np.array_equal(scores.cpu().numpy(), st.scores)
+
+
+def test_device_error_word_reports_a_timed_out_wait():
+    """The bounded wait gives up on a barrier nothing completes, sets the error word and returns;
+    the context stays usable."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    assert h2o.h2o_get_device_error() == 0
+    h2o.h2o_selftest_wait_timeout()
+    assert h2o.h2o_get_device_error() == h2o.DEVERR_WAIT_TIMEOUT
+    assert h2o.h2o_get_device_error() == 0  # cleared
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+def test_rejected_calls_leave_state_untouched():
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    d = h2o.Dims(units_b=1, heads=2, head_dim=64, budget=4, k_heavy=2, k_local=2, dtype=h2o.F32)
+    kc = torch.full((2, 4, 64), 3.0, device="cuda")
+    with pytest.raises(h2o.H2OError):
+        bad = h2o.Dims(units_b=1, heads=2, head_dim=64, budget=4, k_heavy=3, k_local=2, dtype=h2o.F32)
+        z = torch.zeros((2, 64), device="cuda")
+        s = torch.zeros((2, 4), device="cuda")
+        p = torch.zeros((2, 4), dtype=torch.int32, device="cuda")
+        e = torch.zeros(2, dtype=torch.int32, device="cuda")
+        h2o.h2o_decode_step(bad, 5, z, z, z, kc, kc, s, p, z, e, e)
+    assert torch.all(kc == 3.0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,check", [("opt-6.7b", 8), ("llama-7b", 4), ("opt-30b", 6)])
+def test_full_size_workload_sampled_units(name, check):
+    """The full workload in the launch shape the benchmark times; the oracle follows sampled units
+    (spread over layers, sequences and heads) through every step."""
+    w = W[name]
+    units = np.linspace(0, w.units - 1, check).astype(int)
+    _assert(parity.run(w, check_units=units, state_every=64))
+
+
+@pytest.mark.slow
+def test_streaming_full_length_properties_and_prefix_parity():
+    """512 + 262144 steps at budget 4096: invariants that hold at any length, checked every 4096
+    steps on every unit (slot map valid, recent window resident, K/V rows are the generated rows of
+    their positions, scores finite and bounded by the number of queries), plus oracle parity on
+    one unit over the first 6144 steps (growth to the full budget and 2048 evicting steps)."""
+    import torch
+
+    w = W["streaming"]
+    U, k, kl, P = w.units, w.budget, w.k_local, w.prompt_len
+    sample_units = [0, 13, 31]
+
+    def props(cache, t):
+        sp = parity.to_host(cache.slot_pos, "i32")
+        sc = parity.to_host(cache.scores, "f32")
+        n = min(t + 1, k)
+        for u in range(U):
+            pos = sp[u][sp[u] >= 0]
+            assert len(pos) == n and len(np.unique(pos)) == n, (t, u)
+            recent = np.arange(max(0, t - kl + 1), t + 1)
+            assert np.isin(recent, pos).all(), (t, u)
+        assert np.isfinite(sc).all() and (sc >= 0).all()
+        assert (sc.sum(axis=1, dtype=np.float64) <= t + 1 + 1e-2).all()
+        kc = parity.to_host(cache.k_cache, w.dtype)
+        vc = parity.to_host(cache.v_cache, w.dtype)
+        lo = max(0, t + 1 - 4096)  # regenerate the most recent 4096 positions only
+        for u in sample_units:
+            rows = sp[u]
+            gen = synth.unit_sequence(w, synth.DEFAULT_SEED, u, lo, t + 1)
+            sel = rows >= lo
+            assert np.array_equal(kc[u][sel], gen[1][rows[sel] - lo]), (t, u)
+            assert np.array_equal(vc[u][sel], gen[2][rows[sel] - lo]), (t, u)
+
+    rep = parity.run(w, check_units=[0], steps=6144, state_every=1024)
+    _assert(rep)
+    rep = parity.run(w, check_units=[], steps=w.decode_steps, chunk_steps=4096,
+                     property_checks=props, state_every=0)
+    assert not rep.notes, rep.notes
+    torch.cuda.synchronize()
