@@ -238,10 +238,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="opt-6.7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="h2o", choices=["h2o", "reference"])
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.layers is not None:
+        w = w.with_(layers=args.layers)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, w, world, rank)

@@ -28,8 +28,11 @@
  *     Softmax(QK^T/sqrt(D)) among the rest (equal sums keep the later position); kept tokens fill
  *     slots 0.. in ascending position, unused slots get position -1, score 0 and zero K/V rows.
  *
- * Memory. Every pointer argument is DEVICE memory owned by the caller, row-major and contiguous,
- * 16-byte aligned (cudaMalloc / torch allocations are). Element type of q/k/v/out/caches is
+ * Memory. Every pointer argument is DEVICE memory owned by the caller, row-major and contiguous.
+ * q, k, v, k_new, v_new, k_cache, v_cache and the workspace must be 16-byte aligned (they are read
+ * with 16-byte vector and bulk copies; every row of D = 64 or 128 elements keeps that alignment);
+ * scores, slot_pos, evicted_* and colsum 4-byte aligned; out aligned to its element. Element type
+ * of q/k/v/out/caches is
  * dims.dtype (H2O_F32: float, H2O_BF16: bfloat16); scores are float32; positions and indices are
  * int32. The library allocates nothing per call; it keeps one 4-byte device error word per device,
  * created on first use.
@@ -154,6 +157,10 @@ H2O_API h2o_status h2o_get_device_error(void* stream, int32_t* code);
  * reports it (and clears it). Nothing else is touched. Returns H2O_ERR_CUDA if the launch fails.
  */
 H2O_API h2o_status h2o_selftest_wait_timeout(void* stream);
+
+/* Name of the CUDA error (e.g. "cudaErrorInvalidValue") behind the most recent H2O_ERR_CUDA
+ * returned on the calling thread; "cudaSuccess" if there was none. Static string. */
+H2O_API const char* h2o_last_cuda_error(void);
 
 /* Static, human-readable name of a status. */
 H2O_API const char* h2o_status_string(h2o_status status);

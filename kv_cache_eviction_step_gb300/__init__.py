@@ -25,7 +25,7 @@ DEVERR_NONE, DEVERR_WAIT_TIMEOUT, DEVERR_NO_CANDIDATE = range(3)
 
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
            "h2o_decode_step", "h2o_get_device_error", "h2o_selftest_wait_timeout",
-           "h2o_status_string")
+           "h2o_last_cuda_error", "h2o_status_string")
 
 
 class Dims(ctypes.Structure):
@@ -47,7 +47,8 @@ class Dims(ctypes.Structure):
 class H2OError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+        detail = f", {last_cuda_error()}" if status == ERR_CUDA else ""
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status}{detail})")
 
 
 _lib: ctypes.CDLL | None = None
@@ -79,6 +80,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_get_device_error.restype = ctypes.c_int
     lib.h2o_selftest_wait_timeout.argtypes = [vp]
     lib.h2o_selftest_wait_timeout.restype = ctypes.c_int
+    lib.h2o_last_cuda_error.argtypes = []
+    lib.h2o_last_cuda_error.restype = ctypes.c_char_p
     lib.h2o_status_string.argtypes = [ctypes.c_int]
     lib.h2o_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -87,6 +90,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return load().h2o_status_string(status).decode()
+
+
+def last_cuda_error() -> str:
+    """Name of the CUDA error behind the last ERR_CUDA on this thread."""
+    return load().h2o_last_cuda_error().decode()
 
 
 def _ptr(x) -> int | None:

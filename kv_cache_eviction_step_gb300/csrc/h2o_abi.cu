@@ -15,6 +15,8 @@ namespace {
 
 __device__ int32_t g_error_word;
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 // Device address of the error word for the current device (resolved once per device).
 int32_t* error_word() {
   static std::mutex mu;
@@ -25,12 +27,20 @@ int32_t* error_word() {
   for (auto& c : cache)
     if (c.first == dev) return c.second;
   void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_error_word);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = e;
+    return nullptr;
+  }
   cache.emplace_back(dev, static_cast<int32_t*>(ptr));
   return static_cast<int32_t*>(ptr);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned_to(const void* p, int bytes) {
+  return (reinterpret_cast<uintptr_t>(p) & static_cast<uintptr_t>(bytes - 1)) == 0;
+}
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -47,7 +57,12 @@ h2o_status check_dims(const h2o_dims* d) {
 
 int elem_bytes(const h2o_dims* d) { return d->dtype == H2O_F32 ? 4 : 2; }
 
-h2o_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H2O_OK : H2O_ERR_CUDA; }
+h2o_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return H2O_OK;
+  t_last_cuda_error = e;
+  (void)cudaGetLastError();  // clear the sticky-free launch error so later calls start clean
+  return H2O_ERR_CUDA;
+}
 
 // Waits on an mbarrier that nothing ever arrives at, with a short limit: exercises the bounded-wait
 // path (error word set, clean return) without any copy in flight.
@@ -67,6 +82,10 @@ __global__ void wait_timeout_probe_kernel(int32_t* err, unsigned long long limit
 using namespace h2o;
 
 extern "C" {
+
+const char* h2o_last_cuda_error(void) {
+  return t_last_cuda_error == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(t_last_cuda_error);
+}
 
 const char* h2o_status_string(h2o_status status) {
   switch (status) {
@@ -97,7 +116,7 @@ static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, 
   p.row_sum = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + arr);
   p.colsum = colsum;
   p.err = error_word();
-  if (p.err == nullptr) return H2O_ERR_CUDA;
+  if (p.err == nullptr) return from_cuda(cudaGetLastError());
   p.units = units;
   p.P = prompt_len;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
@@ -124,7 +143,7 @@ h2o_status h2o_prefill_scores(const h2o_dims* dims, int32_t prompt_len, const vo
   h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
   if (st != H2O_OK) return st;
   if (dims->units_b == 0) return H2O_OK;
-  if (!colsum || !aligned16(colsum)) return H2O_ERR_INVALID_ARG;
+  if (!colsum || !aligned4(colsum)) return H2O_ERR_INVALID_ARG;
   return prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes,
                              static_cast<cudaStream_t>(stream));
 }
@@ -138,8 +157,8 @@ h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const vo
   if (dims->budget > select_max_budget()) return H2O_ERR_UNSUPPORTED;
   if (dims->units_b == 0) return H2O_OK;
   if (!v || !k_cache || !v_cache || !scores || !slot_pos) return H2O_ERR_INVALID_ARG;
-  if (!aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(scores) ||
-      !aligned16(slot_pos))
+  if (!aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(scores) ||
+      !aligned4(slot_pos))
     return H2O_ERR_INVALID_ARG;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int units = dims->units_b * dims->heads;
@@ -172,9 +191,13 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
   if (st != H2O_OK) return st;
   if (position < 1) return H2O_ERR_INVALID_ARG;
   if (dims->units_b == 0) return H2O_OK;
-  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, scores, slot_pos, out, evicted_slot, evicted_pos};
-  for (const void* ptr : ptrs)
+  const void* vec_ptrs[] = {q, k_new, v_new, k_cache, v_cache};  // 16-byte vector / bulk loads
+  for (const void* ptr : vec_ptrs)
     if (ptr == nullptr || !aligned16(ptr)) return H2O_ERR_INVALID_ARG;
+  const void* word_ptrs[] = {scores, slot_pos, evicted_slot, evicted_pos};
+  for (const void* ptr : word_ptrs)
+    if (ptr == nullptr || !aligned4(ptr)) return H2O_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned_to(out, elem_bytes(dims))) return H2O_ERR_INVALID_ARG;
   DecodeParams p = {};
   p.q = q;
   p.k_new = k_new;
@@ -187,7 +210,7 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
   p.evicted_slot = evicted_slot;
   p.evicted_pos = evicted_pos;
   p.err = error_word();
-  if (p.err == nullptr) return H2O_ERR_CUDA;
+  if (p.err == nullptr) return from_cuda(cudaGetLastError());
   p.units = dims->units_b * dims->heads;
   p.budget = dims->budget;
   p.k_local = dims->k_local;
@@ -202,7 +225,7 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
 
 h2o_status h2o_selftest_wait_timeout(void* stream) {
   int32_t* word = error_word();
-  if (word == nullptr) return H2O_ERR_CUDA;
+  if (word == nullptr) return from_cuda(cudaGetLastError());
   wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word, 50000000ull);
   return from_cuda(cudaGetLastError());
 }

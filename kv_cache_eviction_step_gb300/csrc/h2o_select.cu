@@ -153,7 +153,11 @@ cudaError_t prepare_select() {
   int optin = 0;
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_select_kernel);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           optin - static_cast<int>(fa.sharedSizeBytes));
   if (e != cudaSuccess) return e;
   done.push_back(dev);
   return cudaSuccess;

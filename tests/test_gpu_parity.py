@@ -112,15 +112,14 @@ def test_exact_ties_evict_lowest_position():
 
     import kv_cache_eviction_step_gb300 as h2o
     budget, D = 8, 64
-    for kl, pos, sc, want in [
-        (1, [7, 3, 9, 5, 12, 4, 11, 10], [0.5] * 8, 1),                         # lowest position 3
-        (3, [12, 3, 14, 5, 2, 9, 13, 10], [0.25] * 8, 4),                       # 2 (13, 14 protected)
-        (2, [5, 8, 2, 9, 10, 11, 12, 13], [0.25, 0.5, 0.25, 0.75, 1, 1, 1, 1], 2),  # tie 5 vs 2 -> 2
-        (8, [7, 6, 9, 8, 10, 11, 12, 13], [0.0, 9.0, 0, 0, 0, 0, 0, 0], 1),     # window: only 6
+    for t, kl, pos, sc, want in [
+        (14, 1, [7, 3, 9, 5, 12, 4, 11, 10], [0.5] * 8, 1),                     # lowest position 3
+        (15, 3, [12, 3, 14, 5, 2, 9, 13, 10], [0.25] * 8, 4),                   # 2 (13, 14 protected)
+        (15, 2, [5, 8, 2, 9, 10, 11, 12, 13], [0.25, 0.5, 0.25, 0.75, 1, 1, 1, 1], 2),  # 5 vs 2 -> 2
+        (14, 8, [7, 6, 9, 8, 10, 11, 12, 13], [0.0, 9.0, 0, 0, 0, 0, 0, 0], 1),  # window: only 6
     ]:
         d = h2o.Dims(units_b=1, heads=1, head_dim=D, budget=budget, k_heavy=budget - kl, k_local=kl,
                      dtype=h2o.BF16)
-        t = 14
         z = torch.zeros((1, D), dtype=torch.bfloat16, device="cuda")
         kc = torch.zeros((1, budget, D), dtype=torch.bfloat16, device="cuda")
         vc = torch.zeros_like(kc)
