@@ -120,6 +120,31 @@ H2O_API h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, 
                               float* scores, int32_t* slot_pos, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Size of the device array h2o_prefill_select_static uses as its scratch (16 MiB). */
+#define H2O_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * h2o_prefill_select without a workspace argument, for callers that cannot allocate device memory
+ * (for example a serving engine that reserved all device memory for its own pool at start-up, or a
+ * plugin running inside a host framework that owns the allocator and hands it only the tensors it
+ * declared). The H2O pages have no counterpart: this is a deployment convenience. The scratch lives
+ * in one device array of H2O_STATIC_SCRATCH_BYTES inside this library, which every GPU that loads the
+ * library holds until the process exits; nothing is allocated or freed by the call.
+ *   - Same arguments, results and errors as h2o_prefill_select, minus the workspace.
+ *   - Limit: h2o_prefill_workspace_bytes(dims, prompt_len) <= H2O_STATIC_SCRATCH_BYTES, i.e.
+ *     units * prompt_len <= 1,398,080 (e.g. 2048 units with 512-token prompts); larger calls return
+ *     H2O_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents (no array
+ *     has to start at zero: each is fully written before it is read). Calls that overlap on the
+ *     GPU, on different streams or from different threads, race on it: order them on one stream.
+ */
+H2O_API h2o_status h2o_prefill_select_static(const h2o_dims* dims, int32_t prompt_len,
+                                             const void* q, const void* k, const void* v,
+                                             void* k_cache, void* v_cache, float* scores,
+                                             int32_t* slot_pos, void* stream);
+
 /*
  * One budgeted decode step (rows D1-D7) at absolute position `position` (>= 1) for every unit,
  * fused into one kernel launch. With n = min(position, budget) valid cached slots 0..n-1:

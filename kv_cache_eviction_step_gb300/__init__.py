@@ -23,7 +23,10 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = range(5)
 DEVERR_NONE, DEVERR_WAIT_TIMEOUT, DEVERR_NO_CANDIDATE = range(3)
 
+STATIC_SCRATCH_BYTES = 16 << 20  # H2O_STATIC_SCRATCH_BYTES
+
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
+           "h2o_prefill_select_static",
            "h2o_decode_step", "h2o_get_device_error", "h2o_selftest_wait_timeout",
            "h2o_last_cuda_error", "h2o_status_string")
 
@@ -74,6 +77,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_prefill_scores.restype = ctypes.c_int
     lib.h2o_prefill_select.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.h2o_prefill_select.restype = ctypes.c_int
+    lib.h2o_prefill_select_static.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.h2o_prefill_select_static.restype = ctypes.c_int
     lib.h2o_decode_step.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.h2o_decode_step.restype = ctypes.c_int
     lib.h2o_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -142,6 +147,17 @@ def h2o_prefill_select(dims: Dims, prompt_len: int, q, k, v, k_cache, v_cache, s
     _check("h2o_prefill_select", load().h2o_prefill_select(
         ctypes.byref(dims), prompt_len, _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
         _ptr(scores), _ptr(slot_pos), _ptr(workspace), wb, _stream(stream)))
+
+
+def h2o_prefill_select_static(dims: Dims, prompt_len: int, q, k, v, k_cache, v_cache, scores,
+                              slot_pos, stream=None):
+    """h2o_prefill_select with its scratch in the library's fixed 16 MiB device array, for callers
+    that cannot allocate device memory (a memory pool that owns the whole device, a plugin inside a
+    framework that owns the allocator). Calls on one device share that array: order them on one
+    stream. units * prompt_len must not exceed 1,398,080."""
+    _check("h2o_prefill_select_static", load().h2o_prefill_select_static(
+        ctypes.byref(dims), prompt_len, _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+        _ptr(scores), _ptr(slot_pos), _stream(stream)))
 
 
 def h2o_decode_step(dims: Dims, position: int, q, k_new, v_new, k_cache, v_cache, scores,
