@@ -19,13 +19,22 @@ thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 
 // Device address of the error word for the current device (resolved once per device).
 int32_t* error_word() {
+  thread_local int last_dev = -1;
+  thread_local int32_t* last_ptr = nullptr;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return nullptr;
+  if (cur == last_dev && last_ptr != nullptr) return last_ptr;
   static std::mutex mu;
   static std::vector<std::pair<int, int32_t*>> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   for (auto& c : cache)
-    if (c.first == dev) return c.second;
+    if (c.first == dev) {
+      last_dev = dev;
+      last_ptr = c.second;
+      return c.second;
+    }
   void* ptr = nullptr;
   const cudaError_t e = cudaGetSymbolAddress(&ptr, g_error_word);
   if (e != cudaSuccess) {
@@ -33,7 +42,20 @@ int32_t* error_word() {
     return nullptr;
   }
   cache.emplace_back(dev, static_cast<int32_t*>(ptr));
-  return static_cast<int32_t*>(ptr);
+  last_dev = dev;
+  last_ptr = static_cast<int32_t*>(ptr);
+  return last_ptr;
+}
+
+int sm_count() {
+  thread_local int dev_cached = -1, sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1 << 30;
+  if (dev != dev_cached) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1 << 30;
+    dev_cached = dev;
+  }
+  return sms;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -121,6 +143,9 @@ static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, 
   p.P = prompt_len;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
   (void)workspace_bytes;
+  // bf16: tcgen05 tensor cores (bf16 x bf16 products are exact in the fp32 accumulator); fp32 stays
+  // on the CUDA cores, where the products are not rounded to tf32.
+  if (dims->dtype == H2O_BF16) return from_cuda(launch_prefill_scores_tc(p, dims->head_dim, stream));
   return from_cuda(launch_prefill_scores_simt(p, dims->head_dim, dims->dtype, stream));
 }
 
@@ -217,8 +242,13 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
   p.position = position;
   p.n = position < dims->budget ? position : dims->budget;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
+  // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
+  // over units. Otherwise the CUDA-core kernel, each unit split over a CTA cluster when units are few.
+  if (decode_tc_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= 4 * sm_count())
+    return from_cuda(launch_decode_tc(p, static_cast<cudaStream_t>(stream)));
   size_t smem = 0;
-  if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem))
+  if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem,
+                   &p.grid))
     return H2O_ERR_UNSUPPORTED;
   return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
 }

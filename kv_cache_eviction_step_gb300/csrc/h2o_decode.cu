@@ -31,8 +31,9 @@
 namespace h2o {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumers = 256;                 // 8 consumer warps compute
+constexpr int kWarps = kConsumers / 32;
+constexpr int kThreads = kConsumers + 32;       // + 1 producer warp issues the bulk copies
 constexpr int kTileBytes = 8192;
 constexpr int kMaxSplits = 16;
 constexpr int kDefaultStages = 6;
@@ -42,7 +43,7 @@ struct Shape {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kLanesPerRow = kRowBytes / 16;        // lanes sharing one K/V row
   static constexpr int kElems = 16 / static_cast<int>(sizeof(T));  // elements per lane
-  static constexpr int kGroups = kThreads / kLanesPerRow;    // rows processed side by side
+  static constexpr int kGroups = kConsumers / kLanesPerRow;  // rows processed side by side
   static constexpr int kTileRows = kTileBytes / kRowBytes;
   static_assert(kLanesPerRow >= 1 && kLanesPerRow <= 32, "row must span 1..32 lanes");
 };
@@ -74,8 +75,8 @@ __host__ __device__ inline Layout decode_layout(int stages, int chunk) {
   Layout L;
   auto up = [](int x, int a) { return (x + a - 1) / a * a; };
   L.ring = 0;
-  L.bars = stages * kTileBytes;
-  L.pub = up(L.bars + stages * 8, 16);
+  L.bars = stages * kTileBytes;               // full[stages], then empty[stages]
+  L.pub = up(L.bars + 2 * stages * 8, 16);
   L.red = up(L.pub + static_cast<int>(sizeof(Publish<D>)), 16);
   L.logit = up(L.red + kRedBytes, 16);
   L.wgt = L.logit + chunk * 4;
@@ -117,13 +118,18 @@ __device__ __forceinline__ float row_sum(float v) {
   return v;
 }
 
+// Barrier over the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
   const int warp = threadIdx.x >> 5;
-  __syncthreads();
+  consumer_sync();
   if ((threadIdx.x & 31) == 0) red[warp] = v;
-  __syncthreads();
+  consumer_sync();
   float r = red[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) r = fmaxf(r, red[w]);
@@ -134,9 +140,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   const int warp = threadIdx.x >> 5;
-  __syncthreads();
+  consumer_sync();
   if ((threadIdx.x & 31) == 0) red[warp] = v;
-  __syncthreads();
+  consumer_sync();
   float r = 0.f;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) r += red[w];
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
   const Layout L = decode_layout<D>(stages, p.chunk);
   unsigned char* ring = smem + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + stages;
   Publish<D>* pub = reinterpret_cast<Publish<D>*>(smem + L.pub);
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* s_new_sh = red + kWarps;          // one float after the reduction slots
@@ -178,29 +185,44 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
   float* wgt = reinterpret_cast<float*>(smem + L.wgt);
   float* sc = reinterpret_cast<float*>(smem + L.sc);
   int32_t* sp = reinterpret_cast<int32_t*>(smem + L.sp);
+  const bool cache_full = p.n == p.budget;
 
   if (tid == 0) {
-    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
     fence_mbar_init();
   }
-  __syncthreads();
+  __syncthreads();  // the last block-wide barrier: from here on producer and consumers split
 
   const size_t row0 = static_cast<size_t>(unit) * p.budget + c0;
-  const unsigned char* kbase = static_cast<const unsigned char*>(p.k_cache) + row0 * S::kRowBytes;
-  const unsigned char* vbase = static_cast<const unsigned char*>(p.v_cache) + row0 * S::kRowBytes;
-  auto issue = [&](int i) {
-    const int s = i % stages;
-    const int tt = i < tiles ? i : i - tiles;
-    const int r0 = tt * S::kTileRows;
-    const int nr = min(S::kTileRows, rows - r0);
-    const uint32_t bytes = static_cast<uint32_t>(nr) * S::kRowBytes;
-    mbar_expect_tx(&full[s], bytes);
-    bulk_g2s(ring + s * kTileBytes, (i < tiles ? kbase : vbase) + static_cast<size_t>(r0) * S::kRowBytes,
-             bytes, &full[s]);
-  };
-  if (tid == 0) {
-    const int first = min(stages, total);
-    for (int i = 0; i < first; ++i) issue(i);
+  if (warp == kWarps) {
+    // Producer warp: K tiles then V tiles, each into the next ring stage once every consumer warp
+    // has released it.
+    if (lane == 0) {
+      const unsigned char* kbase = static_cast<const unsigned char*>(p.k_cache) + row0 * S::kRowBytes;
+      const unsigned char* vbase = static_cast<const unsigned char*>(p.v_cache) + row0 * S::kRowBytes;
+      for (int i = 0; i < total; ++i) {
+        const int s = i % stages;
+        if (i >= stages && !mbar_wait(&empty[s], static_cast<uint32_t>(i / stages - 1) & 1u, p.err)) break;
+        const int tt = i < tiles ? i : i - tiles;
+        const int r0 = tt * S::kTileRows;
+        const int nr = min(S::kTileRows, rows - r0);
+        const uint32_t bytes = static_cast<uint32_t>(nr) * S::kRowBytes;
+        mbar_expect_tx(&full[s], bytes);
+        bulk_g2s(ring + s * kTileBytes, (i < tiles ? kbase : vbase) + static_cast<size_t>(r0) * S::kRowBytes,
+                 bytes, &full[s]);
+      }
+    }
+    __syncwarp();
+    // Join the cluster barriers the consumers pass through, then leave.
+    if (splits > 1) {
+      cluster_sync_all();
+      if (cache_full) cluster_sync_all();
+      cluster_sync_all();
+    }
+    return;
   }
 
   // D1: the new token. Each lane keeps its 16-byte slice of q in registers.
@@ -224,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
     if (lane == 0) *s_new_sh = acc * p.scale;
   }
   // Scores and positions of this CTA's slots, read while the first tiles are in flight.
-  for (int r = tid; r < rows; r += kThreads) {
+  for (int r = tid; r < rows; r += kConsumers) {
     sc[r] = p.scores[row0 + r];
     sp[r] = p.slot_pos[row0 + r];
   }
@@ -251,26 +273,26 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
       acc = row_sum<S::kLanesPerRow>(acc);
       if (r < nr && lig == 0) logit[r0 + r] = acc * p.scale;
     }
-    __syncthreads();
-    if (tid == 0 && ok && i + stages < total) issue(i + stages);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 
   // D3 (local part): max and weights; rank 0 also carries the new token.
-  __syncthreads();  // s_new and the score/position prefetch are visible (also when tiles == 0)
+  consumer_sync();  // logits, s_new and the score/position prefetch are visible (also if tiles == 0)
   const float s_new = *s_new_sh;
   float mloc = -INFINITY;
-  for (int r = tid; r < rows; r += kThreads) mloc = fmaxf(mloc, logit[r]);
+  for (int r = tid; r < rows; r += kConsumers) mloc = fmaxf(mloc, logit[r]);
   if (rank == 0 && tid == 0) mloc = fmaxf(mloc, s_new);
   mloc = block_max(mloc, red);
   float lsum = 0.f;
-  for (int r = tid; r < rows; r += kThreads) {
+  for (int r = tid; r < rows; r += kConsumers) {
     const float w = expf(logit[r] - mloc);
     wgt[r] = w;
     lsum += w;
   }
   const float w_new = (rank == 0) ? expf(s_new - mloc) : 0.f;
   if (rank == 0 && tid == 0) lsum += w_new;
-  lsum = block_sum(lsum, red);  // its __syncthreads also publishes wgt[]
+  lsum = block_sum(lsum, red);  // its barrier also publishes wgt[]
 
   // D4 (local part): sum_j w_j V_j over the V tiles.
   float acc[S::kElems];
@@ -292,15 +314,16 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
         for (int e = 0; e < S::kElems; ++e) acc[e] = fmaf(w, vf[e], acc[e]);
       }
     }
-    __syncthreads();
-    if (tid == 0 && ok && i + stages < total) issue(i + stages);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
   // All tiles are consumed, so the ring is free: reduce the row groups' partial outputs there.
   float* part = reinterpret_cast<float*>(ring);
+  consumer_sync();  // every warp is done with its last tile before the ring is reused
 #pragma unroll
   for (int e = 0; e < S::kElems; ++e) part[grp * D + lig * S::kElems + e] = acc[e];
-  __syncthreads();
-  for (int d = tid; d < D; d += kThreads) {
+  consumer_sync();
+  for (int d = tid; d < D; d += kConsumers) {
     float o = 0.f;
     for (int g = 0; g < S::kGroups; ++g) o += part[g * D + d];
     if (rank == 0) {
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
 
   // D3 (global part): combine (m, l, o) across the cluster.
   if (splits > 1) cluster_sync_all();
-  __syncthreads();
+  consumer_sync();
   if (tid == 0) {
     float m = -INFINITY;
     for (int c = 0; c < splits; ++c) m = fmaxf(m, (splits > 1 ? peer_ptr(pub, c) : pub)->m);
@@ -335,11 +358,11 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
     red[0] = m;
     red[1] = l;
   }
-  __syncthreads();
+  consumer_sync();
   const float mg = red[0];
   const float lg = red[1];
   if (rank == 0) {
-    for (int d = tid; d < D; d += kThreads) {
+    for (int d = tid; d < D; d += kConsumers) {
       float o = 0.f;
       for (int c = 0; c < splits; ++c) o = fmaf((splits > 1 ? peer_ptr(pub, c) : pub)->o[d], pub->f[c], o);
       store_out<T>(p.out, static_cast<size_t>(unit) * D + d, o / lg);
@@ -347,11 +370,10 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
   }
 
   // D5 + D6 (local part): p_j, updated scores, argmin key over the unprotected slots.
-  const bool cache_full = p.n == p.budget;
   const int32_t last_candidate = p.position - p.k_local;
   unsigned long long best = ~0ull;
   int32_t best_slot = -1;
-  for (int r = tid; r < rows; r += kThreads) {
+  for (int r = tid; r < rows; r += kConsumers) {
     const float pr = expf(logit[r] - mg) / lg;
     const float ns = sc[r] + pr;
     sc[r] = ns;
@@ -379,12 +401,12 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
     }
     unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + L.red + kRedKeys);
     int32_t* sred = reinterpret_cast<int32_t*>(smem + L.red + kRedSlots);
-    __syncthreads();
+    consumer_sync();
     if (lane == 0) {
       kred[warp] = best;
       sred[warp] = best_slot;
     }
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
       for (int w = 1; w < kWarps; ++w) {
         if (kred[w] < best) {
@@ -397,7 +419,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
     }
     // D6 (global part): cluster-wide minimum key; its owner holds the victim slot.
     if (splits > 1) cluster_sync_all();
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
       unsigned long long k = ~0ull;
       int32_t slot = -1;
@@ -412,13 +434,13 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
       kred[0] = k;
       sred[0] = slot;
     }
-    __syncthreads();
+    consumer_sync();
     vkey = kred[0];
     victim = sred[0];
   }
 
   // D7: write back the score table and put the new token into its slot.
-  for (int r = tid; r < rows; r += kThreads) p.scores[row0 + r] = (c0 + r == victim) ? p_new : sc[r];
+  for (int r = tid; r < rows; r += kConsumers) p.scores[row0 + r] = (c0 + r == victim) ? p_new : sc[r];
   const int32_t target = cache_full ? victim : p.n;
   const bool owner = cache_full ? (victim >= c0 && victim < c0 + rows) : (rank == 0);
   if (owner && target >= 0 && ok) {
@@ -457,6 +479,10 @@ int device_sm_count() {
 // Opt one kernel into the device's full dynamic shared memory and into 16-CTA clusters, once per
 // (kernel, device).
 cudaError_t prepare_kernel(const void* fn) {
+  thread_local const void* last_fn = nullptr;
+  thread_local int last_dev = -1;
+  int cur = 0;
+  if (cudaGetDevice(&cur) == cudaSuccess && fn == last_fn && cur == last_dev) return cudaSuccess;
   static std::mutex mu;
   static std::vector<std::pair<const void*, int>> done;
   int dev = 0;
@@ -464,7 +490,11 @@ cudaError_t prepare_kernel(const void* fn) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   for (auto& d : done)
-    if (d.first == fn && d.second == dev) return cudaSuccess;
+    if (d.first == fn && d.second == dev) {
+      last_fn = fn;
+      last_dev = dev;
+      return cudaSuccess;
+    }
   int optin = 0;
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
@@ -477,6 +507,8 @@ cudaError_t prepare_kernel(const void* fn) {
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   done.emplace_back(fn, dev);
+  last_fn = fn;
+  last_dev = dev;
   return cudaSuccess;
 }
 
@@ -519,11 +551,50 @@ bool cluster_fits(const void* fn, int splits, size_t smem) {
 
 }  // namespace
 
+namespace {
+
+bool plan_decode_uncached(int units, int n, int head_dim, int elem_bytes, int* splits_out,
+                          int* chunk_out, int* stages_out, size_t* smem_out, int* grid_out);
+
+struct PlanMemo {
+  int dev = -1, units = -1, n = -1, head_dim = -1, elem_bytes = -1;
+  int splits = 0, chunk = 0, stages = 0, grid = 0;
+  size_t smem = 0;
+  bool ok = false;
+};
+
+}  // namespace
+
+// Decode steps of one workload repeat the same shape (n stops changing once the cache is full), so
+// the plan of the previous call on this thread is reused when nothing changed.
 bool plan_decode(int units, int n, int head_dim, int elem_bytes, int* splits_out, int* chunk_out,
-                 int* stages_out, size_t* smem_out) {
+                 int* stages_out, size_t* smem_out, int* grid_out) {
+  thread_local PlanMemo memo;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (!(memo.dev == dev && memo.units == units && memo.n == n && memo.head_dim == head_dim &&
+        memo.elem_bytes == elem_bytes)) {
+    memo.ok = plan_decode_uncached(units, n, head_dim, elem_bytes, &memo.splits, &memo.chunk,
+                                   &memo.stages, &memo.smem, &memo.grid);
+    memo.dev = dev;
+    memo.units = units;
+    memo.n = n;
+    memo.head_dim = head_dim;
+    memo.elem_bytes = elem_bytes;
+  }
+  *splits_out = memo.splits;
+  *chunk_out = memo.chunk;
+  *stages_out = memo.stages;
+  *smem_out = memo.smem;
+  *grid_out = memo.grid;
+  return memo.ok;
+}
+
+namespace {
+
+bool plan_decode_uncached(int units, int n, int head_dim, int elem_bytes, int* splits_out,
+                          int* chunk_out, int* stages_out, size_t* smem_out, int* grid_out) {
   const int dtype = elem_bytes == 2 ? H2O_BF16 : H2O_F32;
-  const void* fn = kernel_of(head_dim, dtype);
-  if (prepare_kernel(fn) != cudaSuccess) return false;
   const int row_bytes = head_dim * elem_bytes;
   const int tile_rows = kTileBytes / row_bytes;
   const int target_ctas = 4 * device_sm_count();
@@ -531,8 +602,12 @@ bool plan_decode(int units, int n, int head_dim, int elem_bytes, int* splits_out
   if (units < target_ctas) want = (target_ctas + units - 1) / units;
   const int max_by_rows = (n + tile_rows - 1) / tile_rows;  // at least one tile per CTA
   want = max(1, min(want, min(kMaxSplits, max_by_rows)));
-  // Fewest splits whose shared memory fits, starting from the wanted parallelism; wider clusters
-  // are taken only if the device can schedule them.
+
+  // Each unit over `splits` CTAs of one cluster (one CTA when there are enough units). Fewest splits
+  // whose shared memory fits, starting from the wanted parallelism; wider clusters are taken only if
+  // the device can schedule them.
+  const void* fn = kernel_of(head_dim, dtype);
+  if (prepare_kernel(fn) != cudaSuccess) return false;
   for (int splits = want; splits <= kMaxSplits; ++splits) {
     const int chunk = (n + splits - 1) / splits;
     const int tiles = (chunk + tile_rows - 1) / tile_rows;
@@ -546,10 +621,13 @@ bool plan_decode(int units, int n, int head_dim, int elem_bytes, int* splits_out
     *chunk_out = chunk;
     *stages_out = stages;
     *smem_out = static_cast<size_t>(L.total);
+    *grid_out = units * splits;
     return true;
   }
   return false;
 }
+
+}  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int dtype, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(

@@ -1,0 +1,601 @@
+// h2o_decode_tc.cu -- the fused H2O decode step (hot-path rows D1-D7) with both contractions on the
+// 5th-generation tensor cores, for bf16 caches with D = 128 and budgets up to 512 slots.
+//
+// Per unit (layer, sequence, head) with n = min(t, budget) cached slots:
+//   D2  logits: S = K q, K the unit's [n x 128] key rows (tiles of 128 rows) and q the new query,
+//       as tcgen05.mma M = 128 (slots) x N = 16 (q in row 0, zeros after) x K = 128; the logit of
+//       slot j lands in TMEM lane j % 128, column 16 (j / 128)          (H2O post §2.1.1)
+//   D3  softmax over the n logits and the new token on the epilogue warps (one slot per thread per
+//       tile)
+//   D4  output: o = V^T w as tcgen05.mma M = 128 (d) x N = 16 x K = slots, V^T read straight from
+//       the TMA-written V tile as an MN-major operand, w written by the epilogue as two bf16 rows
+//       (w = hi + lo, so the weights keep ~16 significant bits); o lands in TMEM lane d
+//   D5  scores[j] += p_j in fp32, p_j = exp(s_j - m) / l from the fp32 logits (not from hi/lo)
+//                                                            (H2O post §2.2; 分析 §3.2)
+//   D6  victim = argmin over slots with position <= t - k_local of (score, position)
+//   D7  the new token's K/V row, score p_new and position go into the victim slot (H2O post §2.3)
+//
+// The kernel is persistent: each CTA walks units blockIdx.x, +gridDim.x, ... Warp roles: warps 0-3
+// epilogue (one TMEM lane quarter each), warp 4 TMA producer (q rows, K tiles, V tiles of the
+// successive units through one 4-stage ring of 32 KB tiles), warp 5 TMEM allocator + MMA issuer.
+// Tensor memory holds two unit slots (logits + output accumulator each), so the producer and the
+// tensor core run into the next unit while the epilogue finishes the current one. All waits are
+// bounded (mbar_wait); every role stops at its first timeout and tensor memory is always freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "h2o_internal.cuh"
+
+namespace h2o {
+namespace {
+
+constexpr int kD = 128;                    // head dim of this path
+constexpr int kTileRows = 128;             // cache rows per tile (MMA M for the logits)
+constexpr int kBox = 128 * 128;            // one [128 rows x 64 cols] bf16 box: 16 KB
+constexpr int kTileBytes = 2 * kBox;       // a 128-row tile, both 64-column halves
+constexpr int kStages = 4;
+constexpr int kMaxTiles = 4;               // budgets up to 512 slots
+constexpr int kNRows = 16;                 // rows of the small operand (q, or w hi/lo): MMA N
+constexpr int kSmallBox = kNRows * 128;    // [16 rows x 64 cols] bf16: 2 KB
+constexpr int kQBytes = 2 * kSmallBox;     // q operand: both 64-column halves
+constexpr int kWBytes = 2 * kMaxTiles * kSmallBox;  // w operand: 64 slots per 2 KB box
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kTmaWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr uint32_t kTmemCols = 256;        // two unit slots of 128 columns
+constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
+constexpr int kAlign = 1024;
+
+// Shared-memory layout (offsets from a 1024-aligned base).
+constexpr int kRingOff = 0;
+constexpr int kQOff = kRingOff + kStages * kTileBytes;
+constexpr int kWOff = kQOff + 2 * kQBytes;
+constexpr int kCtrlOff = kWOff + 2 * kWBytes;
+constexpr int kCtrlBytes = 1024;
+constexpr int kSmem = kCtrlOff + kCtrlBytes + kAlign;
+
+struct TcDecodeParams {
+  CUtensorMap tm_k;        // K cache [units][budget][128] bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap tm_v;        // V cache, same
+  CUtensorMap tm_q;        // queries [units][128] bf16, box 64 x 1, 128-byte swizzle
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  float* scores;
+  int32_t* slot_pos;
+  __nv_bfloat16* out;
+  int32_t* evicted_slot;
+  int32_t* evicted_pos;
+  int32_t* err;
+  int32_t units, budget, k_local, position, n, tiles;
+  float scale;
+};
+
+// ---- PTX wrappers (same encodings as the prefill's tcgen05 path) -------------------------------
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 128-byte-swizzled operand descriptor. K-major: rows of 128 bytes, 8-row groups `sbo` apart.
+// MN-major: 64-element MN groups `lbo` apart, 8-row K groups `sbo` apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// kind::f16 instruction descriptors, fp32 accumulate, bf16 A and B, M = 128, N = 16.
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((kNRows >> 3) << 17) | ((128 >> 4) << 24);
+constexpr uint32_t kIdescQK = kIdescBase;              // A = K tile (K-major), B = q (K-major)
+constexpr uint32_t kIdescPV = kIdescBase | (1u << 15); // A = V^T (MN-major), B = w (K-major)
+
+__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, float& a, float& b) {
+  uint32_t r0, r1;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1)
+      : "r"(taddr)
+      : "memory");
+  a = __uint_as_float(r0);
+  b = __uint_as_float(r1);
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
+__device__ __forceinline__ unsigned long long evict_key_tc(float score, int32_t pos) {
+  uint32_t b = __float_as_uint(score);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(pos);
+}
+
+// Byte offset of element j (0..n) of row `row` (0 = hi, 1 = lo) of the w operand: 64 slots per
+// 2 KB box, 128-byte rows, 16-byte chunks swizzled by the row index.
+__device__ __forceinline__ int w_offset(int j, int row) {
+  const int box = j >> 6, jj = j & 63;
+  return box * kSmallBox + row * 128 + ((((jj >> 3) ^ row) & 7) << 4) + ((jj & 7) << 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid_constant__ TcDecodeParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
+  unsigned char* ring = smem + kRingOff;
+  unsigned char* qbuf = smem + kQOff;
+  unsigned char* wbuf = smem + kWOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCtrlOff);
+  uint64_t* full = bars;                     // [kStages]
+  uint64_t* empty = full + kStages;          // [kStages]
+  uint64_t* q_full = empty + kStages;        // [2]
+  uint64_t* q_empty = q_full + 2;            // [2]
+  uint64_t* s_full = q_empty + 2;            // [2] logits ready
+  uint64_t* w_ready = s_full + 2;            // [2] weights written
+  uint64_t* o_full = w_ready + 2;            // [2] output ready
+  uint64_t* tm_free = o_full + 2;            // [2] unit slot of tensor memory free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_free + 2);
+  float* red = reinterpret_cast<float*>(smem + kCtrlOff + 512);          // [kEpiWarps] + 4
+  unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + kCtrlOff + 640);  // [kEpiWarps]
+  int32_t* sred = reinterpret_cast<int32_t*>(smem + kCtrlOff + 704);     // [kEpiWarps]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.tiles;
+  const int n = p.n;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&q_full[r], 1);
+      mbar_init(&q_empty[r], 1);
+      mbar_init(&s_full[r], 1);
+      mbar_init(&w_ready[r], 1);
+      mbar_init(&o_full[r], 1);
+      mbar_init(&tm_free[r], kEpiWarps);
+    }
+    fence_mbar_init();
+  }
+  // Rows 1..15 of the q operand stay zero (TMA writes row 0 only); the w operand is fully
+  // rewritten per unit.
+  for (int i = tid; i < 2 * kQBytes / 16; i += kThreads) reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      uint32_t g = 0;
+      int k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
+        const int r = k & 1;
+        if (k >= 2 && !mbar_wait(&q_empty[r], static_cast<uint32_t>((k >> 1) - 1) & 1u, p.err)) break;
+        mbar_expect_tx(&q_full[r], 2 * 128);
+        tma_load_2d(qbuf + r * kQBytes, &p.tm_q, 0, u, &q_full[r]);
+        tma_load_2d(qbuf + r * kQBytes + kSmallBox, &p.tm_q, 64, u, &q_full[r]);
+        for (int i = 0; i < 2 * T; ++i, ++g) {
+          const int s = static_cast<int>(g % kStages);
+          if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
+          const int row0 = (i < T ? i : i - T) * kTileRows;
+          mbar_expect_tx(&full[s], kTileBytes);
+          tma_load_3d(ring + s * kTileBytes, map, 0, row0, u, &full[s]);
+          tma_load_3d(ring + s * kTileBytes + kBox, map, 64, row0, u, &full[s]);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      uint32_t g = 0;
+      int k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
+        const int r = k & 1;
+        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        const uint32_t slot = tmem + static_cast<uint32_t>(r) * 128;
+        if (k >= 2 && !mbar_wait(&tm_free[r], ph ^ 1u, p.err)) break;
+        if (!mbar_wait(&q_full[r], ph, p.err)) break;
+        const uint32_t q_base = smem_u32(qbuf + r * kQBytes);
+        // D2: logits of each 128-row K tile into columns 16 t of this unit's slot.
+        for (int t = 0; t < T; ++t, ++g) {
+          const int s = static_cast<int>(g % kStages);
+          if (!mbar_wait(&full[s], (g / kStages) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(ring + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off_a = (kk >> 2) * kBox + (kk & 3) * 32;
+            const uint32_t off_b = (kk >> 2) * kSmallBox + (kk & 3) * 32;
+            mma(slot + 16 * t, sw128_desc(a_base + off_a, 16, 1024), sw128_desc(q_base + off_b, 16, 1024),
+                kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&q_empty[r]);
+        mma_commit(&s_full[r]);
+        // D4: o = V^T w over the V tiles, once the epilogue has written w.
+        if (!mbar_wait(&w_ready[r], ph, p.err)) break;
+        tc_fence_after();
+        const uint32_t w_base = smem_u32(wbuf + r * kWBytes);
+        for (int t = 0; t < T; ++t, ++g) {
+          const int s = static_cast<int>(g % kStages);
+          if (!mbar_wait(&full[s], (g / kStages) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(ring + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk) {
+            // V^T as MN-major A: 64-d groups one box apart, 8-slot groups 1024 bytes apart; 16 slots
+            // (two groups) per instruction. w as K-major B: 64 slots per 2 KB box.
+            const uint32_t off_a = kk * 2048;
+            const int j0 = t * kTileRows + kk * 16;
+            const uint32_t off_b = (j0 >> 6) * kSmallBox + ((j0 & 63) >> 3) * 16;
+            mma(slot + kPvCol, sw128_desc(v_base + off_a, kBox, 1024), sw128_desc(w_base + off_b, 16, 1024),
+                kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&o_full[r]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // Epilogue: thread (warp, lane) owns slot 128 t + 32 warp + lane of every tile t, and output
+    // element d = tid.
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int32_t last_candidate = p.position - p.k_local;
+    const bool cache_full = n == p.budget;
+    int k = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
+      const int r = k & 1;
+      const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+      const size_t row0 = static_cast<size_t>(u) * p.budget;
+      const size_t ud = static_cast<size_t>(u) * kD + tid;
+      // This unit's new token and state, loaded now and used after the logits arrive.
+      const float qd = __bfloat162float(p.q[ud]);
+      const __nv_bfloat16 kn = p.k_new[ud];
+      const __nv_bfloat16 vn = p.v_new[ud];
+      float sc[kMaxTiles];
+      int32_t sp[kMaxTiles];
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int j = t * kTileRows + tid;
+        const bool valid = t < T && j < n;
+        sc[t] = valid ? p.scores[row0 + j] : 0.f;
+        sp[t] = valid ? p.slot_pos[row0 + j] : 0;
+      }
+      // s_new = q . k_new / sqrt(D) across the 128 epilogue threads.
+      float part = qd * __bfloat162float(kn);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == 0) red[warp] = part;
+
+      if (!mbar_wait(&s_full[r], ph, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kMaxTiles];
+      float m = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        s[t] = -INFINITY;
+        if (t < T) {
+          const float raw = tmem_ld1(lane_base + r * 128 + 16 * t);
+          if (t * kTileRows + tid < n) s[t] = raw * p.scale;
+        }
+        m = fmaxf(m, s[t]);
+      }
+      epi_sync();  // red[] holds the s_new partials
+      const float s_new = (red[0] + red[1] + red[2] + red[3]) * p.scale;
+      m = fmaxf(m, s_new);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      epi_sync();
+      if (lane == 0) red[warp] = m;
+      epi_sync();
+      m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+      // D3: weights, and the bf16 hi/lo split of each weight into the w operand.
+      float e[kMaxTiles];
+      float lsum = 0.f;
+      unsigned char* wb = wbuf + r * kWBytes;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        if (t < T) {
+          const int j = t * kTileRows + tid;
+          e[t] = (s[t] == -INFINITY) ? 0.f : expf(s[t] - m);
+          lsum += e[t];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(e[t]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(e[t] - __bfloat162float(hi));
+          *reinterpret_cast<__nv_bfloat16*>(wb + w_offset(j, 0)) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(wb + w_offset(j, 1)) = lo;
+        } else {
+          e[t] = 0.f;
+        }
+      }
+      fence_async_smem();
+      const float w_new = expf(s_new - m);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      epi_sync();  // every thread's w entries are written (and fenced); red[] free again
+      if (tid == 0) mbar_arrive(&w_ready[r]);
+      if (lane == 0) red[warp] = lsum;
+      epi_sync();
+      const float l = red[0] + red[1] + red[2] + red[3] + w_new;
+
+      // D5 + D6 while the tensor core computes the output.
+      unsigned long long best = ~0ull;
+      int32_t best_slot = -1;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        if (t < T && t * kTileRows + tid < n) {
+          const float pr = e[t] / l;
+          sc[t] = sc[t] + pr;
+          if (cache_full && sp[t] <= last_candidate) {
+            const unsigned long long key = evict_key_tc(sc[t], sp[t]);
+            if (key < best) {
+              best = key;
+              best_slot = t * kTileRows + tid;
+            }
+          }
+        }
+      }
+      const float p_new = w_new / l;
+      int32_t victim = -1;
+      unsigned long long vkey = ~0ull;
+      if (cache_full) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int32_t os = __shfl_xor_sync(0xffffffffu, best_slot, off);
+          if (ob < best) {
+            best = ob;
+            best_slot = os;
+          }
+        }
+        if (lane == 0) {
+          kred[warp] = best;
+          sred[warp] = best_slot;
+        }
+        epi_sync();
+        vkey = kred[0];
+        victim = sred[0];
+#pragma unroll
+        for (int w = 1; w < kEpiWarps; ++w)
+          if (kred[w] < vkey) {
+            vkey = kred[w];
+            victim = sred[w];
+          }
+        if (tid == 0 && victim < 0) atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
+      }
+
+      // D4 result: o[d] = (V^T w_hi + V^T w_lo + w_new v_new) / l.
+      if (!mbar_wait(&o_full[r], ph, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float c0, c1;
+      tmem_ld2(lane_base + r * 128 + kPvCol, c0, c1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tm_free[r]);
+      p.out[ud] = __float2bfloat16_rn((c0 + c1 + w_new * __bfloat162float(vn)) / l);
+
+      // D7: scores back, the new token into its slot, eviction indices.
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int j = t * kTileRows + tid;
+        if (t < T && j < n) p.scores[row0 + j] = (j == victim) ? p_new : sc[t];
+      }
+      const int32_t target = cache_full ? victim : n;
+      if (target >= 0) {
+        p.k_cache[(row0 + target) * kD + tid] = kn;
+        p.v_cache[(row0 + target) * kD + tid] = vn;
+        if (tid == 0) {
+          p.slot_pos[row0 + target] = p.position;
+          if (!cache_full) p.scores[row0 + target] = p_new;
+        }
+      }
+      if (tid == 0) {
+        p.evicted_slot[u] = cache_full ? victim : -1;
+        p.evicted_pos[u] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
+      }
+      epi_sync();  // red / kred reuse by the next unit
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps depend only on the buffers and the shape; a decode loop reuses them every step.
+struct MapCache {
+  const void *k = nullptr, *v = nullptr, *q = nullptr;
+  int units = -1, budget = -1;
+  CUtensorMap tm_k, tm_v, tm_q;
+};
+
+}  // namespace
+
+bool decode_tc_supported(int head_dim, int dtype, int budget) {
+  return head_dim == kD && dtype == H2O_BF16 && budget <= kMaxTiles * kTileRows && encode_fn() != nullptr;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
+  thread_local MapCache mc;
+  TcDecodeParams p;
+  const cuuint32_t tile_box[3] = {64, kTileRows, 1};
+  if (mc.k != dp.k_cache || mc.units != dp.units || mc.budget != dp.budget) {
+    const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(dp.budget), static_cast<cuuint64_t>(dp.units)};
+    const cuuint64_t strides[2] = {kD * 2, static_cast<cuuint64_t>(dp.budget) * kD * 2};
+    if (!encode(&mc.tm_k, dp.k_cache, 3, dims, strides, tile_box)) return cudaErrorInvalidValue;
+    mc.k = dp.k_cache;
+  }
+  if (mc.v != dp.v_cache || mc.units != dp.units || mc.budget != dp.budget) {
+    const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(dp.budget), static_cast<cuuint64_t>(dp.units)};
+    const cuuint64_t strides[2] = {kD * 2, static_cast<cuuint64_t>(dp.budget) * kD * 2};
+    if (!encode(&mc.tm_v, dp.v_cache, 3, dims, strides, tile_box)) return cudaErrorInvalidValue;
+    mc.v = dp.v_cache;
+  }
+  if (mc.q != dp.q || mc.units != dp.units) {
+    const cuuint64_t dims[2] = {kD, static_cast<cuuint64_t>(dp.units)};
+    const cuuint64_t strides[1] = {kD * 2};
+    const cuuint32_t box[2] = {64, 1};
+    if (!encode(&mc.tm_q, dp.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    mc.q = dp.q;
+  }
+  mc.units = dp.units;
+  mc.budget = dp.budget;
+  p.tm_k = mc.tm_k;
+  p.tm_v = mc.tm_v;
+  p.tm_q = mc.tm_q;
+  p.q = static_cast<const __nv_bfloat16*>(dp.q);
+  p.k_new = static_cast<const __nv_bfloat16*>(dp.k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(dp.v_new);
+  p.k_cache = static_cast<__nv_bfloat16*>(dp.k_cache);
+  p.v_cache = static_cast<__nv_bfloat16*>(dp.v_cache);
+  p.scores = dp.scores;
+  p.slot_pos = dp.slot_pos;
+  p.out = static_cast<__nv_bfloat16*>(dp.out);
+  p.evicted_slot = dp.evicted_slot;
+  p.evicted_pos = dp.evicted_pos;
+  p.err = dp.err;
+  p.units = dp.units;
+  p.budget = dp.budget;
+  p.k_local = dp.k_local;
+  p.position = dp.position;
+  p.n = dp.n;
+  p.tiles = (dp.n + kTileRows - 1) / kTileRows;
+  p.scale = dp.scale;
+
+  static std::mutex mu;
+  static std::vector<std::pair<int, int>> ready;  // (device, SM count)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& d : ready)
+      if (d.first == dev) sms = d.second;
+    if (sms == 0) {
+      e = cudaFuncSetAttribute(h2o_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      ready.emplace_back(dev, sms);
+    }
+  }
+  const int grid = dp.units < sms ? dp.units : sms;
+  h2o_decode_tc_kernel<<<grid, kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace h2o

@@ -32,6 +32,7 @@ struct DecodeParams {
   int32_t splits;       // CTAs (one cluster) per unit
   int32_t chunk;        // cached slots per CTA
   int32_t stages;       // ring depth in tiles
+  int32_t grid;         // CTAs launched
   float scale;          // 1/sqrt(D)
 };
 
@@ -67,14 +68,18 @@ struct SelectParams {
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int dtype, cudaStream_t s);
 cudaError_t launch_prefill_scores_simt(const PrefillParams& p, int head_dim, int dtype, cudaStream_t s);
+cudaError_t launch_prefill_scores_tc(const PrefillParams& p, int head_dim, cudaStream_t s);  // bf16
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
+// Tensor-core decode step (bf16, D = 128, budget <= 512), persistent over units.
+bool decode_tc_supported(int head_dim, int dtype, int budget);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
 int select_max_prompt();
 int select_max_budget();
 
 // Chooses how many CTAs (one thread-block cluster) share one unit's decode step and how many slots
-// each CTA owns; also the ring depth. Returns false if no launchable shape exists.
+// each CTA owns; also the ring depth, shared memory and grid. Returns false if no shape fits.
 bool plan_decode(int units, int n, int head_dim, int elem_bytes, int* splits, int* chunk,
-                 int* stages, size_t* smem_bytes);
+                 int* stages, size_t* smem_bytes, int* grid);
 
 // ---- device helpers -----------------------------------------------------------------------
 
@@ -118,7 +123,8 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns` of wall time (2 s by
 // default): then the device error word is set and false is returned, so no wait in this library
-// can hang the GPU.
+// can hang the GPU. Each try_wait may suspend the thread (up to the hint, ~10 ms) until the phase
+// completes, so waiting warps do not spin on the issue slots.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
                                           uint64_t limit_ns = 2000000000ull) {
   const uint32_t addr = smem_u32(bar);
@@ -126,13 +132,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(addr), "r"(parity)
+        : "r"(addr), "r"(parity), "r"(10000000u)
         : "memory");
     if (done) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 3u) == 0) {
       const uint64_t now = global_timer_ns();
       if (it == 0) start = now;
       else if (now - start > limit_ns) {
@@ -141,6 +147,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
       }
     }
   }
+}
+
+// One arrival on `bar` (release semantics: this thread's prior shared-memory reads are ordered
+// before the phase it helps complete).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

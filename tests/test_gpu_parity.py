@@ -82,6 +82,24 @@ def test_sweep(w):
     _assert(parity.run(w, check_units=check, state_every=16))
 
 
+@pytest.mark.parametrize("name,kw", [
+    ("opt-6.7b", dict(layers=1, batch=20, heads=32, decode_steps=96)),
+    ("llama-7b", dict(batch=20, heads=32, decode_steps=48)),
+    ("opt-30b", dict(batch=12, heads=56, decode_steps=64, prompt_len=100, budget=300, k_heavy=150,
+                     k_local=150)),
+    ("opt-6.7b", dict(layers=1, batch=20, heads=32, decode_steps=40, prompt_len=600, budget=512,
+                      k_heavy=511, k_local=1)),
+])
+def test_tensor_core_decode_path(name, kw):
+    """At least 4 units per SM with bf16, D = 128 and budgets up to 512 take the tcgen05 decode
+    kernel: 2 and 4 tiles of 128 slots, a cache that grows from 100 to 300 slots before evicting,
+    and the largest budget with k_local = 1. The oracle follows sampled units through every step."""
+    w = W[name].with_(**kw)
+    assert w.units >= 608 and w.head_dim == 128 and w.dtype == "bf16" and w.budget <= 512
+    units = np.linspace(0, w.units - 1, 10).astype(int)
+    _assert(parity.run(w, check_units=units, state_every=16))
+
+
 def test_prefill_column_sums_elementwise():
     """P1-P2 alone: h2o_prefill_scores against the oracle's float64 column sums, every element."""
     import torch
