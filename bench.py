@@ -36,8 +36,9 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "H2O decode tokens/s (batch x steps, 1 GB300) and KV-read GB/s vs HBM"
-DECODE_SRC = os.path.join(ROOT, "kv_cache_eviction_step_gb300", "csrc", "h2o_decode.cu")
+CSRC = os.path.join(ROOT, "kv_cache_eviction_step_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+GRAPH_STEPS = 1024  # decode launches per captured CUDA graph
 
 
 def decode_bytes_per_unit(n: int, head_dim: int, elem_bytes: int) -> int:
@@ -60,14 +61,23 @@ def source_sha(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def decode_kernel(w: synth.Workload, sms: int) -> tuple[str, str]:
+    """Which decode kernel the library launches for this workload (the same rule as the C ABI's
+    dispatch: tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512), and its source."""
+    if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 512 and w.units >= 4 * sms:
+        return "h2o_decode_tc_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
+    return "h2o_decode_step_kernel", os.path.join(CSRC, "h2o_decode.cu")
+
+
+def recorded_traffic(workload: str, kernel: str, src: str):
     """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the current
-    kernel source and this workload; otherwise None."""
+    source of this kernel and on this workload; otherwise None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         rec = json.load(f)
-    if rec.get("kernel_sha") != source_sha(DECODE_SRC) or rec.get("workload") != workload:
+    if (rec.get("kernel") != kernel or rec.get("kernel_sha") != source_sha(src)
+            or rec.get("workload") != workload):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -291,8 +301,8 @@ def main():
         h2o.h2o_prefill_select(dims, P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], cache.k_cache,
                                cache.v_cache, cache.scores, cache.slot_pos, cache.workspace, sp_ptr)
 
-    def decode_all():
-        for s in range(S):
+    def decode_range(s0, s1):
+        for s in range(s0, s1):
             h2o.h2o_decode_step(dims, P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s],
                                 cache.k_cache, cache.v_cache, cache.scores, cache.slot_pos, out[s],
                                 evs[s], evp[s], sp_ptr)
@@ -302,13 +312,17 @@ def main():
     # launches and the S decode launches) so host-side call overhead is out of the timed region.
     with torch.cuda.stream(stream):
         prefill()
-        decode_all()
+        decode_range(0, S)
     torch.cuda.synchronize(dev)
-    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_pre = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_pre, stream=stream):
         prefill()
-    with torch.cuda.graph(g_dec, stream=stream):
-        decode_all()
+    g_dec = []  # decode launches in graphs of at most GRAPH_STEPS launches
+    for s0 in range(0, S, GRAPH_STEPS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            decode_range(s0, min(S, s0 + GRAPH_STEPS))
+        g_dec.append(g)
 
     def job(marks=None):
         with torch.cuda.stream(stream):
@@ -317,7 +331,8 @@ def main():
             g_pre.replay()
             if marks is not None:
                 marks[1].record(stream)
-            g_dec.replay()
+            for g in g_dec:
+                g.replay()
             if marks is not None:
                 marks[2].record(stream)
 
@@ -355,9 +370,10 @@ def main():
     avg_bytes = float(np.mean(bytes_per_launch))
     avg_decode_s = float(np.mean(decode_ms)) / 1000.0
     achieved = avg_bytes / avg_decode_s / 1e9
+    kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
-                "kernel": "h2o_decode_step_kernel", "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc),
+                "kernel": kname, "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_decode_s * 1e6}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,

@@ -17,7 +17,7 @@
 //
 // The kernel is persistent: each CTA walks units blockIdx.x, +gridDim.x, ... Warp roles: warps 0-3
 // epilogue (one TMEM lane quarter each), warp 4 TMA producer (q rows, K tiles, V tiles of the
-// successive units through one 4-stage ring of 32 KB tiles), warp 5 TMEM allocator + MMA issuer.
+// successive units through one 5-stage ring of 32 KB tiles), warp 5 TMEM allocator + MMA issuer.
 // Tensor memory holds two unit slots (logits + output accumulator each), so the producer and the
 // tensor core run into the next unit while the epilogue finishes the current one. All waits are
 // bounded (mbar_wait); every role stops at its first timeout and tensor memory is always freed.
@@ -38,7 +38,7 @@ constexpr int kD = 128;                    // head dim of this path
 constexpr int kTileRows = 128;             // cache rows per tile (MMA M for the logits)
 constexpr int kBox = 128 * 128;            // one [128 rows x 64 cols] bf16 box: 16 KB
 constexpr int kTileBytes = 2 * kBox;       // a 128-row tile, both 64-column halves
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kMaxTiles = 4;               // budgets up to 512 slots
 constexpr int kNRows = 16;                 // rows of the small operand (q, or w hi/lo): MMA N
 constexpr int kSmallBox = kNRows * 128;    // [16 rows x 64 cols] bf16: 2 KB
