@@ -62,10 +62,13 @@ def source_sha(path: str) -> str:
 
 
 def decode_kernel(w: synth.Workload, sms: int) -> tuple[str, str]:
-    """Which decode kernel the library launches for this workload (the same rule as the C ABI's
-    dispatch: tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512), and its source."""
+    """Which decode kernel the library launches for this workload (the C ABI's dispatch rule:
+    persistent tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512, the cluster-split
+    tcgen05 kernel for other bf16 D = 128 caches up to 8192 slots, the CUDA-core kernel otherwise)."""
     if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 512 and w.units >= 4 * sms:
         return "h2o_decode_tc_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
+    if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 8192:
+        return "h2o_decode_tc_split_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
     return "h2o_decode_step_kernel", os.path.join(CSRC, "h2o_decode.cu")
 
 
@@ -252,12 +255,16 @@ def main():
     ap.add_argument("--impl", default="h2o", choices=["h2o", "reference"])
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (smaller cases for profiling)")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="override the workload's decode steps (shorter jobs for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.layers is not None:
         w = w.with_(layers=args.layers)
+    if args.decode_steps is not None:
+        w = w.with_(decode_steps=args.decode_steps)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, w, world, rank)

@@ -243,9 +243,13 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
   p.n = position < dims->budget ? position : dims->budget;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
   // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
-  // over units. Otherwise the CUDA-core kernel, each unit split over a CTA cluster when units are few.
+  // over units. Other shapes (fp32, D = 64, caches beyond 8192 slots) use the CUDA-core kernel, each
+  // unit split over a CTA cluster when units are few.
   if (decode_tc_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= 4 * sm_count())
     return from_cuda(launch_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  // Fewer bf16 units of D = 128 (or longer caches): the tensor-core step split over a CTA cluster.
+  if (decode_tc_split_supported(dims->head_dim, dims->dtype, p.units, p.n))
+    return from_cuda(launch_decode_tc_split(p, static_cast<cudaStream_t>(stream)));
   size_t smem = 0;
   if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem,
                    &p.grid))

@@ -489,6 +489,396 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
   }
 }
 
+// ---- cluster-split variant: few units, long caches ---------------------------------------------
+//
+// When there are too few units to fill the GPU (e.g. 32 heads of one sequence with a 4096-slot
+// budget), a unit is split over a cluster of `splits` CTAs, CTA r owning slots [r chunk, (r+1) chunk)
+// with chunk <= 512. Each CTA computes its logits and V^T w on the tensor core as above, with the
+// weights taken relative to its own logit max so the tensor core never waits for the cluster; the
+// CTAs then exchange (1) their (max, normaliser) pairs, from which every CTA forms the common max m
+// and normaliser l, and (2) their eviction key plus a 1/splits slice of their output partial,
+// rescaled by exp(m_c - m), by writing into the peers' shared memory (st.shared::cluster) and
+// arriving on the peers' exchange mbarriers with cluster-scope release. Only the epilogue warps take
+// part, so the TMA and MMA warps never wait on the cluster.
+// CTA r finishes output elements [r 128/splits, (r+1) 128/splits); the CTA holding the victim writes
+// the new token; rank 0 writes the eviction indices.
+
+constexpr int kSplitStages = 3;
+constexpr int kMaxSplitsTc = 16;
+constexpr int kSplitMaxChunk = kMaxTiles * kTileRows;  // 512 slots per CTA
+// The small operands keep only the rows that are read back (q: row 0; w: rows 0-1) in 1 KB boxes
+// (one 8-row group) placed 1 KB apart. An operand's second 8-row group (rows 8-15) is then the next
+// box, and those rows only feed accumulator columns 8-15, which are never read.
+constexpr int kNarrowBox = 8 * 128;
+constexpr int kSQOff = kSplitStages * kTileBytes;
+constexpr int kSQBytes = 3 * kNarrowBox;
+constexpr int kSWOff = kSQOff + kSQBytes;
+constexpr int kSWBytes = (kSplitMaxChunk / 64 + 1) * kNarrowBox;
+constexpr int kSXOff = kSWOff + kSWBytes;
+
+struct SplitXchg {
+  float m_in[kMaxSplitsTc];
+  float l_in[kMaxSplitsTc];
+  unsigned long long key_in[kMaxSplitsTc];
+  int32_t slot_in[kMaxSplitsTc];
+  float o_in[kD];  // [rank][128 / splits]: the senders' partials of this CTA's output slice
+};
+constexpr int kSCtrlOff = kSXOff + 1024;
+constexpr int kSplitSmem = kSCtrlOff + 512 + kAlign;
+static_assert(sizeof(SplitXchg) <= 1024, "exchange area");
+
+struct TcSplitParams {
+  TcDecodeParams d;
+  int32_t splits, chunk;
+};
+
+__device__ __forceinline__ uint32_t peer_smem(const void* local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_s32(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+}
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Bounded wait with cluster-scope acquire: data that peers stored before their release-arrive on
+// this barrier is visible afterwards.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err) {
+  const uint32_t addr = smem_u32(bar);
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 3u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (it == 0) start = now;
+      else if (now - start > 2000000000ull) {
+        atomicCAS(err, H2O_DEVERR_NONE, H2O_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int w_offset_narrow(int j, int row) {
+  const int box = j >> 6, jj = j & 63;
+  return box * kNarrowBox + row * 128 + ((((jj >> 3) ^ row) & 7) << 4) + ((jj & 7) << 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const __grid_constant__ TcSplitParams sp_) {
+  const TcDecodeParams& p = sp_.d;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
+  unsigned char* ring = smem;
+  unsigned char* qbuf = smem + kSQOff;
+  unsigned char* wbuf = smem + kSWOff;
+  SplitXchg* xg = reinterpret_cast<SplitXchg*>(smem + kSXOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSCtrlOff);  // [kSplitStages]
+  uint64_t* empty = full + kSplitStages;                             // [kSplitStages]
+  uint64_t* q_full = empty + kSplitStages;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* w_ready = s_full + 1;
+  uint64_t* o_full = w_ready + 1;
+  uint64_t* xbar = o_full + 1;                                        // [3] exchanges
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 3);
+  float* red = reinterpret_cast<float*>(smem + kSCtrlOff + 256);
+  unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + kSCtrlOff + 320);
+  int32_t* sred = reinterpret_cast<int32_t*>(smem + kSCtrlOff + 384);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int splits = sp_.splits;
+  const uint32_t rank = cluster_ctarank();
+  const int unit = static_cast<int>(blockIdx.x) / splits;
+  const int c0 = static_cast<int>(rank) * sp_.chunk;
+  const int rows = max(0, min(p.n - c0, sp_.chunk));
+  const int T = (rows + kTileRows - 1) / kTileRows;
+  constexpr uint32_t kCols = 128;
+
+  if (tid == 0) {
+    for (int s = 0; s < kSplitStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(w_ready, 1);
+    mbar_init(o_full, 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&xbar[x], static_cast<uint32_t>(splits));
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // every CTA's exchange barriers exist before any peer arrives on them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const size_t row0 = static_cast<size_t>(unit) * p.budget;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      mbar_expect_tx(q_full, 2 * 128);
+      tma_load_2d(qbuf, &p.tm_q, 0, unit, q_full);
+      tma_load_2d(qbuf + kNarrowBox, &p.tm_q, 64, unit, q_full);
+      for (int i = 0; i < 2 * T; ++i) {
+        const int s = i % kSplitStages;
+        if (i >= kSplitStages && !mbar_wait(&empty[s], static_cast<uint32_t>(i / kSplitStages - 1) & 1u, p.err)) break;
+        const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
+        const int r0 = c0 + (i < T ? i : i - T) * kTileRows;
+        mbar_expect_tx(&full[s], kTileBytes);
+        tma_load_3d(ring + s * kTileBytes, map, 0, r0, unit, &full[s]);
+        tma_load_3d(ring + s * kTileBytes + kBox, map, 64, r0, unit, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && mbar_wait(q_full, 0, p.err)) {
+      const uint32_t q_base = smem_u32(qbuf);
+      bool ok = true;
+      int i = 0;
+      for (int t = 0; t < T && ok; ++t, ++i) {
+        const int s = i % kSplitStages;
+        if (!(ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kSplitStages) & 1u, p.err))) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(ring + s * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off_a = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * kNarrowBox + (kk & 3) * 32;
+          mma(tmem + 16 * t, sw128_desc(a_base + off_a, 16, 1024), sw128_desc(q_base + off_b, 16, 1024),
+              kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(s_full);
+      if (ok && mbar_wait(w_ready, 0, p.err)) {
+        tc_fence_after();
+        const uint32_t w_base = smem_u32(wbuf);
+        for (int t = 0; t < T; ++t, ++i) {
+          const int s = i % kSplitStages;
+          if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kSplitStages) & 1u, p.err)) break;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(ring + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk) {
+            const int j0 = t * kTileRows + kk * 16;
+            const uint32_t off_b = (j0 >> 6) * kNarrowBox + ((j0 & 63) >> 3) * 16;
+            mma(tmem + kPvCol, sw128_desc(v_base + kk * 2048, kBox, 1024), sw128_desc(w_base + off_b, 16, 1024),
+                kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+      }
+      mma_commit(o_full);
+    }
+    __syncwarp();
+  } else {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool cache_full = p.n == p.budget;
+    const int32_t last_candidate = p.position - p.k_local;
+    const size_t ud = static_cast<size_t>(unit) * kD + tid;
+    const float qd = __bfloat162float(p.q[ud]);
+    const __nv_bfloat16 kn = p.k_new[ud];
+    const __nv_bfloat16 vn = p.v_new[ud];
+    const int slice = kD / splits;
+    float vn_slice = 0.f;
+    if (tid < slice) vn_slice = __bfloat162float(p.v_new[static_cast<size_t>(unit) * kD + rank * slice + tid]);
+    float sc[kMaxTiles];
+    int32_t sp[kMaxTiles];
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      const int jl = t * kTileRows + tid;
+      const bool valid = t < T && jl < rows;
+      sc[t] = valid ? p.scores[row0 + c0 + jl] : 0.f;
+      sp[t] = valid ? p.slot_pos[row0 + c0 + jl] : 0;
+    }
+    float part = qd * __bfloat162float(kn);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) red[warp] = part;
+
+    bool ok = mbar_wait(s_full, 0, p.err);
+    tc_fence_after();
+    float s[kMaxTiles];
+    float m = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      s[t] = -INFINITY;
+      if (t < T) {
+        const float raw = tmem_ld1(lane_base + 16 * t);
+        if (ok && t * kTileRows + tid < rows) s[t] = raw * p.scale;
+      }
+      m = fmaxf(m, s[t]);
+    }
+    epi_sync();
+    const float s_new = (red[0] + red[1] + red[2] + red[3]) * p.scale;
+    if (rank == 0) m = fmaxf(m, s_new);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    epi_sync();
+    if (lane == 0) red[warp] = m;
+    epi_sync();
+    const float mc = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));  // this CTA's max
+    // Weights with respect to the local max, so the tensor core can start on V^T w at once; the
+    // partial output is rescaled by exp(mc - m) once the cluster-wide max m is known.
+    float lsum = 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      if (t < T) {
+        const int jl = t * kTileRows + tid;
+        const float e = (s[t] == -INFINITY) ? 0.f : expf(s[t] - mc);
+        lsum += e;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16*>(wbuf + w_offset_narrow(jl, 0)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(wbuf + w_offset_narrow(jl, 1)) = lo;
+      }
+    }
+    fence_async_smem();
+    if (rank == 0 && tid == 0) lsum += expf(s_new - mc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    epi_sync();  // w written and fenced by every thread; red[] read by every thread
+    if (tid == 0) mbar_arrive(w_ready);
+    if (lane == 0) red[warp] = lsum;
+    epi_sync();
+    const float lc = red[0] + red[1] + red[2] + red[3];
+    // Exchange 1: (local max, local normaliser) -> cluster-wide max and normaliser.
+    if (tid == 0) {
+      for (int r = 0; r < splits; ++r) {
+        st_peer_f32(peer_smem(&xg->m_in[rank], r), mc);
+        st_peer_f32(peer_smem(&xg->l_in[rank], r), lc);
+        arrive_peer(peer_smem(&xbar[0], r));
+      }
+    }
+    ok = mbar_wait_cluster(&xbar[0], 0, p.err) && ok;
+    float mg = -INFINITY;
+    for (int r = 0; r < splits; ++r) mg = fmaxf(mg, xg->m_in[r]);
+    float l = 0.f;
+    for (int r = 0; r < splits; ++r) l = fmaf(xg->l_in[r], expf(xg->m_in[r] - mg), l);
+    const float w_new = expf(s_new - mg);
+
+    unsigned long long best = ~0ull;
+    int32_t best_slot = -1;
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      const int jl = t * kTileRows + tid;
+      if (t < T && jl < rows) {
+        sc[t] = sc[t] + expf(s[t] - mg) / l;
+        if (cache_full && sp[t] <= last_candidate) {
+          const unsigned long long key = evict_key_tc(sc[t], sp[t]);
+          if (key < best) {
+            best = key;
+            best_slot = c0 + jl;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int32_t os = __shfl_xor_sync(0xffffffffu, best_slot, off);
+      if (ob < best) {
+        best = ob;
+        best_slot = os;
+      }
+    }
+    if (lane == 0) {
+      kred[warp] = best;
+      sred[warp] = best_slot;
+    }
+    const float p_new = w_new / l;
+
+    // This CTA's output partial, rescaled to the common max, one slice to each rank.
+    ok = mbar_wait(o_full, 0, p.err) && ok;
+    tc_fence_after();
+    float oc0 = 0.f, oc1 = 0.f;
+    tmem_ld2(lane_base + kPvCol, oc0, oc1);
+    const float opart = T > 0 ? (oc0 + oc1) * expf(mc - mg) : 0.f;
+    st_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart);
+    fence_cluster();
+    epi_sync();
+    // Exchange 2: eviction keys and output slices.
+    if (tid == 0) {
+      unsigned long long kb = kred[0];
+      int32_t sb = sred[0];
+      for (int w = 1; w < kEpiWarps; ++w)
+        if (kred[w] < kb) {
+          kb = kred[w];
+          sb = sred[w];
+        }
+      for (int r = 0; r < splits; ++r) {
+        st_peer_u64(peer_smem(&xg->key_in[rank], r), kb);
+        st_peer_s32(peer_smem(&xg->slot_in[rank], r), sb);
+        arrive_peer(peer_smem(&xbar[1], r));
+      }
+    }
+    ok = mbar_wait_cluster(&xbar[1], 0, p.err) && ok;
+    int32_t victim = -1;
+    unsigned long long vkey = ~0ull;
+    if (cache_full) {
+      for (int r = 0; r < splits; ++r)
+        if (xg->key_in[r] < vkey) {
+          vkey = xg->key_in[r];
+          victim = xg->slot_in[r];
+        }
+      if (tid == 0 && rank == 0 && victim < 0) atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
+    }
+    if (tid < slice) {
+      float o = 0.f;
+      for (int r = 0; r < splits; ++r) o += xg->o_in[r * slice + tid];
+      o = fmaf(w_new, vn_slice, o);
+      p.out[static_cast<size_t>(unit) * kD + rank * slice + tid] = __float2bfloat16_rn(o / l);
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      const int jl = t * kTileRows + tid;
+      if (t < T && jl < rows) p.scores[row0 + c0 + jl] = (c0 + jl == victim) ? p_new : sc[t];
+    }
+    const int32_t target = cache_full ? victim : p.n;
+    const bool owner = cache_full ? (victim >= c0 && victim < c0 + rows) : (rank == 0);
+    if (owner && target >= 0 && ok) {
+      p.k_cache[(row0 + target) * kD + tid] = kn;
+      p.v_cache[(row0 + target) * kD + tid] = vn;
+      if (tid == 0) {
+        p.slot_pos[row0 + target] = p.position;
+        if (!cache_full) p.scores[row0 + target] = p_new;
+      }
+    }
+    if (rank == 0 && tid == 0) {
+      p.evicted_slot[unit] = cache_full ? victim : -1;
+      p.evicted_pos[unit] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+  }
+}
+
 // ---- host side ---------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -524,13 +914,11 @@ struct MapCache {
 
 }  // namespace
 
-bool decode_tc_supported(int head_dim, int dtype, int budget) {
-  return head_dim == kD && dtype == H2O_BF16 && budget <= kMaxTiles * kTileRows && encode_fn() != nullptr;
-}
+namespace {
 
-cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
+// Fills the tensor-core parameters shared by both variants (tensor maps cached per thread).
+cudaError_t fill_params(const DecodeParams& dp, TcDecodeParams& p) {
   thread_local MapCache mc;
-  TcDecodeParams p;
   const cuuint32_t tile_box[3] = {64, kTileRows, 1};
   if (mc.k != dp.k_cache || mc.units != dp.units || mc.budget != dp.budget) {
     const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(dp.budget), static_cast<cuuint64_t>(dp.units)};
@@ -574,6 +962,121 @@ cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
   p.n = dp.n;
   p.tiles = (dp.n + kTileRows - 1) / kTileRows;
   p.scale = dp.scale;
+  return cudaSuccess;
+}
+
+struct SplitPlan {
+  int dev = -1, units = -1, n = -1;
+  int splits = 0, chunk = 0;
+  bool ok = false;
+};
+
+cudaLaunchConfig_t split_config(int units, int splits, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units) * static_cast<unsigned>(splits));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSplitSmem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Power-of-two cluster size (so the 128 output elements split evenly) and a chunk of whole 128-slot
+// tiles, at most 512 slots; more CTAs per unit (up to 8) while there are fewer than ~2 per SM and each
+// would still get at least one full tile.
+bool plan_split(int units, int n, int* splits_out, int* chunk_out) {
+  thread_local SplitPlan memo;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (memo.dev == dev && memo.units == units && memo.n == n) {
+    *splits_out = memo.splits;
+    *chunk_out = memo.chunk;
+    return memo.ok;
+  }
+  memo.dev = dev;
+  memo.units = units;
+  memo.n = n;
+  memo.ok = false;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  // Splitting for parallelism stops at 8 CTAs per cluster: a 16-CTA cluster has to fit inside one
+  // GPC, which leaves too few of them resident at once; only caches over 4096 slots take 16.
+  int splits = 1;
+  while (splits < kMaxSplitsTc &&
+         ((n + splits - 1) / splits > kSplitMaxChunk ||
+          (splits < 8 && units * splits < 2 * sms && (n + 2 * splits - 1) / (2 * splits) >= kTileRows)))
+    splits *= 2;
+  int chunk = (n + splits - 1) / splits;
+  chunk = (chunk + kTileRows - 1) / kTileRows * kTileRows;
+  if (chunk > kSplitMaxChunk) return false;
+  static std::mutex mu;
+  static std::vector<int> ready;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    bool found = false;
+    for (int d : ready) found |= d == dev;
+    if (!found) {
+      if (cudaFuncSetAttribute(h2o_decode_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSplitSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(h2o_decode_tc_split_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+              cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      ready.push_back(dev);
+    }
+  }
+  if (splits > 1) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = split_config(splits, splits, nullptr, attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(h2o_decode_tc_split_kernel), &cfg) !=
+            cudaSuccess ||
+        clusters == 0) {
+      (void)cudaGetLastError();
+      return false;
+    }
+  }
+  memo.splits = splits;
+  memo.chunk = chunk;
+  memo.ok = true;
+  *splits_out = splits;
+  *chunk_out = chunk;
+  return true;
+}
+
+}  // namespace
+
+bool decode_tc_split_supported(int head_dim, int dtype, int units, int n) {
+  int splits = 0, chunk = 0;
+  return head_dim == kD && dtype == H2O_BF16 && n <= kMaxSplitsTc * kSplitMaxChunk && encode_fn() != nullptr &&
+         plan_split(units, n, &splits, &chunk);
+}
+
+cudaError_t launch_decode_tc_split(const DecodeParams& dp, cudaStream_t stream) {
+  TcSplitParams sp;
+  cudaError_t e = fill_params(dp, sp.d);
+  if (e != cudaSuccess) return e;
+  if (!plan_split(dp.units, dp.n, &sp.splits, &sp.chunk)) return cudaErrorInvalidConfiguration;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = split_config(dp.units, sp.splits, stream, attr);
+  void* args[] = {&sp};
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(h2o_decode_tc_split_kernel), args);
+}
+
+bool decode_tc_supported(int head_dim, int dtype, int budget) {
+  return head_dim == kD && dtype == H2O_BF16 && budget <= kMaxTiles * kTileRows && encode_fn() != nullptr;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
+  TcDecodeParams p;
+  cudaError_t fe = fill_params(dp, p);
+  if (fe != cudaSuccess) return fe;
 
   static std::mutex mu;
   static std::vector<std::pair<int, int>> ready;  // (device, SM count)

@@ -73,6 +73,9 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
 // Tensor-core decode step (bf16, D = 128, budget <= 512), persistent over units.
 bool decode_tc_supported(int head_dim, int dtype, int budget);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
+// Tensor-core decode step with each unit split over a CTA cluster (bf16, D = 128, few units).
+bool decode_tc_split_supported(int head_dim, int dtype, int units, int n);
+cudaError_t launch_decode_tc_split(const DecodeParams& p, cudaStream_t s);
 int select_max_prompt();
 int select_max_budget();
 
