@@ -30,6 +30,14 @@ KIND_NAMES = ["no_eviction", "rule", "near_tie", "error_bound", "rejected"]
 TIE_REL = 1e-6
 
 
+POLICY_H2O, POLICY_LOCAL, POLICY_SINK_WINDOW, POLICY_TOPK, POLICY_STRIDED = range(5)
+
+
+class Policy(ctypes.Structure):
+    """Eviction policy: H2O (default) or one of the baselines; see h2o_oracle.c."""
+    _fields_ = [("kind", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("stride", ctypes.c_int32)]
+
+
 class StepInfo(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("rule_victim", ctypes.c_int32),
                 ("victim", ctypes.c_int32), ("evicted_pos", ctypes.c_int32),
@@ -64,6 +72,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.h2o_oracle_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                            vp, vp, vp, vp, vp, vp, f64, f64, vp]
     lib.h2o_oracle_decode_step.restype = ctypes.c_int
+    lib.h2o_oracle_prefill_select_policy.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
+                                                     vp, vp, vp, vp, vp, vp, vp, f64, f64, vp]
+    lib.h2o_oracle_prefill_select_policy.restype = ctypes.c_int
+    lib.h2o_oracle_decode_step_policy.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                                  vp, vp, vp, vp, vp, vp, vp, vp, vp, f64, f64, vp]
+    lib.h2o_oracle_decode_step_policy.restype = ctypes.c_int
     lib.h2o_oracle_run_unit.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                         ctypes.c_int64, vp, vp, vp, vp, vp]
     lib.h2o_oracle_run_unit.restype = ctypes.c_int
@@ -113,9 +127,14 @@ class State:
 class Oracle:
     """The oracle's two operations on numpy arrays (host memory)."""
 
-    def __init__(self, budget: int, k_heavy: int, k_local: int, lib_path: str = LIB):
+    def __init__(self, budget: int, k_heavy: int, k_local: int, lib_path: str = LIB,
+                 policy: Policy | None = None):
         self.lib = load(lib_path)
         self.budget, self.k_heavy, self.k_local = budget, k_heavy, k_local
+        self.policy = policy
+
+    def _pol(self):
+        return None if self.policy is None else ctypes.cast(ctypes.pointer(self.policy), ctypes.c_void_p)
 
     def new_state(self, units: int, head_dim: int, dtype) -> State:
         return State(units, self.budget, head_dim, dtype)
@@ -128,10 +147,10 @@ class Oracle:
         colsum = np.empty((units, P), dtype=np.float64) if want_colsum else None
         infos = (PrefillInfo * max(units, 1))()
         pref = None if prefer_pos is None else np.ascontiguousarray(prefer_pos, dtype=np.int32)
-        rc = self.lib.h2o_oracle_prefill_select(
+        rc = self.lib.h2o_oracle_prefill_select_policy(
             units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), P,
             _ptr(q), _ptr(k), _ptr(v), _ptr(state.k_cache), _ptr(state.v_cache),
-            _ptr(state.scores), _ptr(state.slot_pos), _ptr(colsum), _ptr(pref),
+            _ptr(state.scores), _ptr(state.slot_pos), _ptr(colsum), self._pol(), _ptr(pref),
             tie_rel, err_rel, ctypes.cast(infos, ctypes.c_void_p))
         if rc != 0:
             raise ValueError(f"h2o_oracle_prefill_select rejected its arguments (code {rc})")
@@ -149,11 +168,12 @@ class Oracle:
         probs = np.full((units, self.budget + 1), np.nan) if want_probs else None
         infos = (StepInfo * max(units, 1))()
         pref = None if prefer_victim is None else np.ascontiguousarray(prefer_victim, dtype=np.int32)
-        rc = self.lib.h2o_oracle_decode_step(
+        rc = self.lib.h2o_oracle_decode_step_policy(
             units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), t,
             _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(state.k_cache), _ptr(state.v_cache),
             _ptr(state.scores), _ptr(state.slot_pos), _ptr(out), _ptr(probs), _ptr(ev_slot),
-            _ptr(ev_pos), _ptr(pref), tie_rel, err_rel, ctypes.cast(infos, ctypes.c_void_p))
+            _ptr(ev_pos), self._pol(), _ptr(pref), tie_rel, err_rel,
+            ctypes.cast(infos, ctypes.c_void_p))
         if rc != 0:
             raise ValueError(f"h2o_oracle_decode_step rejected its arguments (code {rc})")
         return out, ev_slot, ev_pos, probs, infos[:units]

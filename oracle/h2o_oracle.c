@@ -97,9 +97,10 @@ static int keep_order(const void* a, const void* b) {
   return (x->pos > y->pos) ? -1 : (x->pos < y->pos) ? 1 : 0;
 }
 
-/* c_j = sum over rows i >= j of softmax_i(j), softmax over the causal row i: j' = 0..i. */
+/* c_j = sum over rows i >= j of softmax_i(j), softmax over the causal row i: j' = 0..i. If
+ * last_row is given it receives softmax_{P-1}(j), the last prompt query's attention. */
 static void causal_column_sums(int32_t D, int32_t dtype, int32_t P, const void* q, const void* k,
-                               double scale, double* c, double* qrow, double* s) {
+                               double scale, double* c, double* qrow, double* s, double* last_row) {
   for (int32_t j = 0; j < P; ++j) c[j] = 0.0;
   for (int32_t i = 0; i < P; ++i) {
     for (int32_t d = 0; d < D; ++d) qrow[d] = elem(q, dtype, (size_t)i * D + d);
@@ -111,6 +112,47 @@ static void causal_column_sums(int32_t D, int32_t dtype, int32_t P, const void* 
     double l = 0.0;
     for (int32_t j = 0; j <= i; ++j) l += exp(s[j] - m);
     for (int32_t j = 0; j <= i; ++j) c[j] += exp(s[j] - m) / l;
+    if (last_row && i == P - 1)
+      for (int32_t j = 0; j <= i; ++j) last_row[j] = exp(s[j] - m) / l;
+  }
+}
+
+/* ---- policies ------------------------------------------------------------------------------ */
+
+static int check_policy(const h2o_oracle_policy* pol, int32_t budget) {
+  switch (pol->kind) {
+    case H2O_ORACLE_POLICY_H2O:
+    case H2O_ORACLE_POLICY_LOCAL:
+    case H2O_ORACLE_POLICY_TOPK:
+      return 0;
+    case H2O_ORACLE_POLICY_SINK_WINDOW:
+      return (pol->n_sink >= 0 && pol->n_sink < budget) ? 0 : -7;
+    case H2O_ORACLE_POLICY_STRIDED:
+      return pol->stride >= 1 ? 0 : -7;
+  }
+  return -7;
+}
+
+/* Policies that decide by position alone (no near ties to adopt). */
+static int by_position(const h2o_oracle_policy* pol) {
+  return pol->kind == H2O_ORACLE_POLICY_LOCAL || pol->kind == H2O_ORACLE_POLICY_SINK_WINDOW ||
+         pol->kind == H2O_ORACLE_POLICY_STRIDED;
+}
+
+/* Eviction order of the position rules: smaller goes first. Local and sink + window evict the
+ * oldest position; strided evicts positions off its grid (pos mod stride != 0) oldest first, and
+ * grid positions only when no other candidate is left. */
+static int64_t position_rank(const h2o_oracle_policy* pol, int32_t pos) {
+  if (pol->kind == H2O_ORACLE_POLICY_STRIDED && pos % pol->stride == 0) return (int64_t)1 << 40 | pos;
+  return pos;
+}
+
+/* Whether a cached position may be evicted at step t. */
+static int eviction_candidate(const h2o_oracle_policy* pol, int32_t pos, int32_t t, int32_t k_local) {
+  switch (pol->kind) {
+    case H2O_ORACLE_POLICY_LOCAL: return 1;
+    case H2O_ORACLE_POLICY_SINK_WINDOW: return pos >= pol->n_sink;
+    default: return (int64_t)pos <= (int64_t)t - k_local;
   }
 }
 
@@ -147,21 +189,37 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
                               float* scores, int32_t* slot_pos, double* colsum,
                               const int32_t* prefer_pos, double tie_rel, double err_rel,
                               h2o_oracle_prefill_info* infos) {
+  return h2o_oracle_prefill_select_policy(units, D, budget, k_heavy, k_local, dtype, P, q, k, v,
+                                          k_cache, v_cache, scores, slot_pos, colsum, NULL,
+                                          prefer_pos, tie_rel, err_rel, infos);
+}
+
+int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                     int32_t k_local, int32_t dtype, int32_t P, const void* q,
+                                     const void* k, const void* v, void* k_cache, void* v_cache,
+                                     float* scores, int32_t* slot_pos, double* colsum,
+                                     const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                                     double tie_rel, double err_rel, h2o_oracle_prefill_info* infos) {
+  const h2o_oracle_policy h2o_rule = {H2O_ORACLE_POLICY_H2O, 0, 0};
+  const h2o_oracle_policy* pol = policy ? policy : &h2o_rule;
   int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
   if (rc) return rc;
   if (P < 1) return -4;
+  rc = check_policy(pol, budget);
+  if (rc) return rc;
   const size_t eb = elem_bytes(dtype);
   const size_t row = (size_t)D * eb;
   const double scale = 1.0 / sqrt((double)D);
 
   double* c = (double*)malloc(sizeof(double) * (size_t)P);
+  double* a = (double*)malloc(sizeof(double) * (size_t)P);  /* last prompt row's attention */
   double* s = (double*)malloc(sizeof(double) * (size_t)P);
   double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
   ranked* cand = (ranked*)malloc(sizeof(ranked) * (size_t)P);
   unsigned char* keep = (unsigned char*)malloc((size_t)P);
   unsigned char* keep_pref = (unsigned char*)malloc((size_t)P);
-  if (!c || !s || !qrow || !cand || !keep || !keep_pref) {
-    free(c); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
+  if (!c || !a || !s || !qrow || !cand || !keep || !keep_pref) {
+    free(c); free(a); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
     return -9;
   }
 
@@ -175,17 +233,36 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
     int32_t* sp = slot_pos + (size_t)u * budget;
     h2o_oracle_prefill_info info = {H2O_ORACLE_NO_EVICTION, 0, INFINITY};
 
-    causal_column_sums(D, dtype, P, qu, ku, scale, c, qrow, s);
+    causal_column_sums(D, dtype, P, qu, ku, scale, c, qrow, s, a);
     if (colsum) memcpy(colsum + (size_t)u * P, c, sizeof(double) * (size_t)P);
+    /* The value a kept token starts from: its accumulated attention over the prompt, or for
+     * Top-K the attention the current (last) prompt token gives it. */
+    const double* start = pol->kind == H2O_ORACLE_POLICY_TOPK ? a : c;
 
     /* Which prompt positions stay. */
     if (P <= budget) {
       memset(keep, 1, (size_t)P);
+    } else if (pol->kind == H2O_ORACLE_POLICY_LOCAL || pol->kind == H2O_ORACLE_POLICY_SINK_WINDOW) {
+      /* The most recent positions, plus the first n_sink ones for sink + window. */
+      const int32_t sinks = pol->kind == H2O_ORACLE_POLICY_SINK_WINDOW ? pol->n_sink : 0;
+      memset(keep, 0, (size_t)P);
+      for (int32_t p = 0; p < sinks; ++p) keep[p] = 1;
+      for (int32_t p = P - (budget - sinks); p < P; ++p) keep[p] = 1;
+      info.kind = H2O_ORACLE_RULE;
+      if (prefer_pos) {
+        const int32_t* pp = prefer_pos + (size_t)u * budget;
+        for (int32_t sl = 0; sl < budget; ++sl)
+          if (pp[sl] < 0 || pp[sl] >= P || !keep[pp[sl]]) info.kind = H2O_ORACLE_REJECTED;
+      }
     } else {
       memset(keep, 0, (size_t)P);
       for (int32_t p = P - k_local; p < P; ++p) keep[p] = 1;     /* the k_local most recent */
       int32_t nc = P - k_local;                                 /* older positions compete */
-      for (int32_t p = 0; p < nc; ++p) { cand[p].c = c[p]; cand[p].pos = p; }
+      /* Ranked by the start value (H2O, Top-K) or, for strided, grid membership. */
+      for (int32_t p = 0; p < nc; ++p) {
+        cand[p].c = pol->kind == H2O_ORACLE_POLICY_STRIDED ? (double)(p % pol->stride == 0) : start[p];
+        cand[p].pos = p;
+      }
       qsort(cand, (size_t)nc, sizeof(ranked), keep_order);
       for (int32_t r = 0; r < k_heavy; ++r) keep[cand[r].pos] = 1;
       info.kind = H2O_ORACLE_RULE;
@@ -194,6 +271,15 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
         int32_t kind = judge_prefill_preference(budget, k_local, P, c, keep,
                                                 prefer_pos + (size_t)u * budget, tie_rel, err_rel,
                                                 keep_pref);
+        if (pol->kind != H2O_ORACLE_POLICY_H2O) {
+          /* Same judgement on the values this policy ranks by. */
+          double* vals = s;  /* row scratch is free here */
+          for (int32_t p = 0; p < P; ++p)
+            vals[p] = pol->kind == H2O_ORACLE_POLICY_STRIDED ? (double)(p % pol->stride == 0) : a[p];
+          kind = judge_prefill_preference(budget, k_local, P, vals, keep,
+                                          prefer_pos + (size_t)u * budget, tie_rel, err_rel, keep_pref);
+          if (by_position(pol) && kind != H2O_ORACLE_RULE) kind = H2O_ORACLE_REJECTED;
+        }
         info.kind = kind;
         if (kind == H2O_ORACLE_NEAR_TIE || kind == H2O_ORACLE_ERROR_BOUND)
           memcpy(keep, keep_pref, (size_t)P);
@@ -206,7 +292,7 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
       if (!keep[p]) continue;
       memcpy(kc + (size_t)slot * row, ku + (size_t)p * row, row);
       memcpy(vc + (size_t)slot * row, vu + (size_t)p * row, row);
-      sc[slot] = (float)c[p];
+      sc[slot] = (float)start[p];
       sp[slot] = p;
       ++slot;
     }
@@ -219,7 +305,7 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
     }
     if (infos) infos[u] = info;
   }
-  free(c); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
+  free(c); free(a); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
   return 0;
 }
 
@@ -232,9 +318,25 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
                            int32_t* evicted_slot, int32_t* evicted_pos,
                            const int32_t* prefer_victim, double tie_rel, double err_rel,
                            h2o_oracle_step_info* infos) {
+  return h2o_oracle_decode_step_policy(units, D, budget, k_heavy, k_local, dtype, t, q, k_new, v_new,
+                                       k_cache, v_cache, scores, slot_pos, out, probs, evicted_slot,
+                                       evicted_pos, NULL, prefer_victim, tie_rel, err_rel, infos);
+}
+
+int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                  int32_t k_local, int32_t dtype, int32_t t, const void* q,
+                                  const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, float* scores, int32_t* slot_pos, double* out,
+                                  double* probs, int32_t* evicted_slot, int32_t* evicted_pos,
+                                  const h2o_oracle_policy* policy, const int32_t* prefer_victim,
+                                  double tie_rel, double err_rel, h2o_oracle_step_info* infos) {
+  const h2o_oracle_policy h2o_rule = {H2O_ORACLE_POLICY_H2O, 0, 0};
+  const h2o_oracle_policy* pol = policy ? policy : &h2o_rule;
   int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
   if (rc) return rc;
   if (t < 1) return -4;
+  rc = check_policy(pol, budget);
+  if (rc) return rc;
   const int32_t n = t < budget ? t : budget;   /* valid cached slots before this step */
   const size_t eb = elem_bytes(dtype);
   const size_t row = (size_t)D * eb;
@@ -286,6 +388,10 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
      * ([post] §2.2, [note] §3.2), as one float32 addition of the float32 weight. */
     for (int32_t j = 0; j < n; ++j) {
       float add = (float)p[j];
+      if (pol->kind == H2O_ORACLE_POLICY_TOPK) {
+        sc[j] = add;  /* Top-K ranks by the current step's attention only */
+        continue;
+      }
       sc[j] = sc[j] + add;
     }
 
@@ -297,14 +403,24 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
        * score goes, equal scores evict the lowest position ([post] §2.2, [note] §3.2). */
       const int64_t last_candidate = (int64_t)t - k_local;
       int32_t best = -1, second = -1;
-      for (int32_t j = 0; j < n; ++j) {
-        if ((int64_t)sp[j] > last_candidate) continue;
-        ++info.n_candidates;
-        if (best < 0 || sc[j] < sc[best] || (sc[j] == sc[best] && sp[j] < sp[best])) {
-          second = best;
-          best = j;
-        } else if (second < 0 || sc[j] < sc[second] || (sc[j] == sc[second] && sp[j] < sp[second])) {
-          second = j;
+      if (!by_position(pol)) {
+        for (int32_t j = 0; j < n; ++j) {
+          if ((int64_t)sp[j] > last_candidate) continue;
+          ++info.n_candidates;
+          if (best < 0 || sc[j] < sc[best] || (sc[j] == sc[best] && sp[j] < sp[best])) {
+            second = best;
+            best = j;
+          } else if (second < 0 || sc[j] < sc[second] || (sc[j] == sc[second] && sp[j] < sp[second])) {
+            second = j;
+          }
+        }
+      } else {
+        /* Position rules (Local, sink + window, strided): the first eligible slot in their
+         * eviction order goes; positions are distinct, so there are no ties. */
+        for (int32_t j = 0; j < n; ++j) {
+          if (!eviction_candidate(pol, sp[j], t, k_local)) continue;
+          ++info.n_candidates;
+          if (best < 0 || position_rank(pol, sp[j]) < position_rank(pol, sp[best])) best = j;
         }
       }
       if (best < 0) { free(qv); free(s); free(p); return -6; }  /* impossible when kl <= budget */
@@ -312,7 +428,9 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
       if (second >= 0) info.gap_rel = rel_gap((double)sc[best], (double)sc[second]);
       info.kind = H2O_ORACLE_RULE;
       target = best;
-      if (prefer_victim && prefer_victim[u] != best) {
+      if (prefer_victim && prefer_victim[u] != best && by_position(pol)) {
+        info.kind = H2O_ORACLE_REJECTED;  /* decided by position: nothing to adopt */
+      } else if (prefer_victim && prefer_victim[u] != best) {
         int32_t w = prefer_victim[u];
         info.kind = H2O_ORACLE_REJECTED;
         if (w >= 0 && w < n && (int64_t)sp[w] <= last_candidate && sc[w] != sc[best]) {

@@ -29,6 +29,22 @@ enum {
   H2O_ORACLE_REJECTED = 4       /* preference not adopted: rule's choice kept                  */
 };
 
+/* Eviction policies. H2O is the method; the others are the baselines the pages compare it with,
+ * run through the same state: see h2o_oracle.c for the exact rules. */
+enum {
+  H2O_ORACLE_POLICY_H2O = 0,          /* accumulated attention, k_local recent tokens protected   */
+  H2O_ORACLE_POLICY_LOCAL = 1,        /* sliding window: the oldest cached position goes          */
+  H2O_ORACLE_POLICY_SINK_WINDOW = 2,  /* the first n_sink positions never go, else the oldest     */
+  H2O_ORACLE_POLICY_TOPK = 3,         /* like H2O but ranked by the current step's attention only */
+  H2O_ORACLE_POLICY_STRIDED = 4       /* off-grid positions (pos % stride != 0) go first, oldest  */
+};
+
+typedef struct {
+  int32_t kind;
+  int32_t n_sink;   /* sink + window: 0 <= n_sink < budget */
+  int32_t stride;   /* strided: >= 1 */
+} h2o_oracle_policy;
+
 typedef struct {
   int32_t kind;          /* one of the enum above                                              */
   int32_t rule_victim;   /* slot the rule picks (-1 if the cache was not full)                 */
@@ -83,6 +99,26 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
                            int32_t* evicted_slot, int32_t* evicted_pos,
                            const int32_t* prefer_victim, double tie_rel, double err_rel,
                            h2o_oracle_step_info* infos);
+
+/* The same two operations under another eviction policy (NULL = H2O). Prefill: Local keeps the last
+ * `budget` prompt positions; sink + window the first n_sink and the last budget - n_sink; Top-K the
+ * last k_local plus the k_heavy older positions the last prompt token attends to most, its scores
+ * starting from that attention; strided the last k_local plus the k_heavy newest older positions
+ * on its grid (then off-grid ones). Decode: Top-K replaces each score by the step's weight instead
+ * of adding it; Local, sink + window and strided evict by position (see h2o_oracle.c). */
+int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                     int32_t k_local, int32_t dtype, int32_t P, const void* q,
+                                     const void* k, const void* v, void* k_cache, void* v_cache,
+                                     float* scores, int32_t* slot_pos, double* colsum,
+                                     const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                                     double tie_rel, double err_rel, h2o_oracle_prefill_info* infos);
+int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                  int32_t k_local, int32_t dtype, int32_t t, const void* q,
+                                  const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, float* scores, int32_t* slot_pos, double* out,
+                                  double* probs, int32_t* evicted_slot, int32_t* evicted_pos,
+                                  const h2o_oracle_policy* policy, const int32_t* prefer_victim,
+                                  double tie_rel, double err_rel, h2o_oracle_step_info* infos);
 
 /*
  * Convenience driver for timing: one unit's whole job, i.e. h2o_oracle_prefill_select on its prompt

@@ -315,8 +315,121 @@ def pin_near_tie_adoption(lib):
         assert infos[0].kind == kind and es[0] == victim, (scores, prefer, infos[0].kind, es[0])
 
 
+def _policy(kind, n_sink=0, stride=1):
+    return oracle.Policy(kind, n_sink, stride)
+
+
+def _resident(rec):
+    return sorted(int(p) for p in rec.slot_pos_after if p >= 0)
+
+
+def pin_local_policy_is_the_window(lib):
+    """Local (the post's sliding-window baseline): whatever the k_heavy/k_local split, the cache is
+    the last k positions and each output is the window attention over t-k .. t."""
+    rng = np.random.default_rng(21)
+    for _ in range(10):
+        D, budget = int(rng.choice([1, 4, 8])), int(rng.integers(1, 7))
+        P, S = int(rng.integers(1, 13)), int(rng.integers(1, 13))
+        kl = int(rng.integers(0, budget + 1))
+        q, k, v = tj.random_sequence(rng, P + S, D, "f32", hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, budget - kl, kl, policy=_policy(oracle.POLICY_LOCAL))
+        Q, K, V = bf.widen(q), bf.widen(k), bf.widen(v)
+        assert sorted(p for p in tr.prefill_state.slot_pos[0] if p >= 0) == list(range(max(0, P - budget), P))
+        for rec in tr.steps:
+            _close(rec.out, bf.window_attention(Q, K, V, rec.t, budget), 1e-12, 1e-13, "local output")
+            assert _resident(rec) == list(range(max(0, rec.t - budget + 1), rec.t + 1)), "local set"
+
+
+def pin_sink_window_keeps_sinks_and_recent(lib):
+    """Sink + window (StreamingLLM's attention sinks, mentioned alongside H2O on the pages): the first
+    n_sink positions stay, the rest is the most recent window; outputs attend exactly that set."""
+    rng = np.random.default_rng(22)
+    for _ in range(12):
+        D, budget = int(rng.choice([1, 4, 8])), int(rng.integers(2, 8))
+        n_sink = int(rng.integers(0, budget))
+        P, S = int(rng.integers(1, 13)), int(rng.integers(1, 13))
+        q, k, v = tj.random_sequence(rng, P + S, D, "f32", hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, budget // 2, budget - budget // 2,
+                    policy=_policy(oracle.POLICY_SINK_WINDOW, n_sink=n_sink))
+        Q, K, V = bf.widen(q), bf.widen(k), bf.widen(v)
+
+        def want(last):  # resident positions once `last` is the newest token
+            n = last + 1
+            if n <= budget:
+                return list(range(n))
+            return sorted(set(range(n_sink)) | set(range(n - (budget - n_sink), n)))
+        assert sorted(p for p in tr.prefill_state.slot_pos[0] if p >= 0) == want(P - 1)
+        for rec in tr.steps:
+            attended = want(rec.t - 1) + [rec.t]
+            _close(rec.out, bf.attention(Q[rec.t], K[attended], V[attended])[0], 1e-12, 1e-13,
+                   "sink+window output")
+            assert _resident(rec) == want(rec.t), f"t={rec.t}: {_resident(rec)} != {want(rec.t)}"
+
+
+def pin_strided_keeps_its_grid(lib):
+    """Strided: beside the k_local recent positions (at least the new token), the older positions kept
+    are the newest ones on the stride grid, then the newest off it -- the closed form of repeatedly
+    evicting off-grid positions oldest first."""
+    rng = np.random.default_rng(23)
+    for _ in range(12):
+        D, budget = int(rng.choice([1, 4])), int(rng.integers(2, 8))
+        kl = int(rng.integers(0, budget + 1))
+        kh = budget - kl
+        stride = int(rng.integers(1, 5))
+        P, S = int(rng.integers(1, 15)), int(rng.integers(1, 15))
+        q, k, v = tj.random_sequence(rng, P + S, D, "f32")
+        tr = tj.run(lib, q, k, v, P, S, budget, kh, kl, policy=_policy(oracle.POLICY_STRIDED, stride=stride))
+
+        def want(last, recent):
+            n = last + 1
+            if n <= budget:
+                return list(range(n))
+            older = sorted(range(n - recent), key=lambda p: (p % stride == 0, p), reverse=True)
+            return sorted(older[: budget - recent] + list(range(n - recent, n)))
+        assert sorted(p for p in tr.prefill_state.slot_pos[0] if p >= 0) == want(P - 1, kl)
+        for rec in tr.steps:
+            # a decode step always admits the new token, even with k_local = 0
+            w = want(rec.t, max(kl, 1))
+            assert _resident(rec) == w, f"stride {stride}, kl {kl}, t={rec.t}: {_resident(rec)} != {w}"
+
+
+def pin_topk_ranks_by_current_attention(lib):
+    """Top-K (the post's baseline that keeps the K highest current scores): each step's scores are
+    exactly that step's weights recomputed from raw Q/K, the victim is their argmin outside the
+    recent tokens, and the prefill keeps the older positions the last prompt token attends to most."""
+    checked = 0
+    for rng, D, P, S, budget, kh, kl, dtype in _cases(24, 30, max_p=12, max_s=12):
+        q, k, v = tj.random_sequence(rng, P + S, D, dtype, hh=2)
+        tr = tj.run(lib, q, k, v, P, S, budget, kh, kl, policy=_policy(oracle.POLICY_TOPK))
+        Q, K = bf.widen(q), bf.widen(k)
+        last = bf.attention_weights(Q[P - 1], K[:P])
+        kept = bf.heavy_selection(last, budget, kh, kl)
+        got = [int(p) for p in tr.prefill_state.slot_pos[0] if p >= 0]
+        older = sorted(last[: max(0, P - kl)], reverse=True)
+        near = P > budget and 0 < kh < P - kl and abs(older[kh - 1] - older[kh]) <= 1e-9
+        if not near:
+            assert got == kept, f"Top-K prefill kept {got}, expected {kept}"
+            _close(tr.prefill_state.scores[0][: len(got)], last[got], 1e-6, 1e-7, "Top-K prefill scores")
+        for rec in tr.steps:
+            resident = [int(p) for p in rec.slot_pos_before if p >= 0]
+            w = bf.attention_weights(Q[rec.t], K[resident + [rec.t]])
+            cur = dict(zip(resident, w[:-1]))
+            if rec.evicted_pos >= 0:
+                cands = sorted((p for p in resident if p <= rec.t - kl), key=lambda p: (cur[p], p))
+                if len(cands) > 1 and abs(cur[cands[1]] - cur[cands[0]]) <= 1e-6 * cur[cands[1]]:
+                    continue
+                assert rec.evicted_pos == cands[0], f"t={rec.t}: Top-K evicted {rec.evicted_pos}, want {cands[0]}"
+                checked += 1
+            for j, p in enumerate(rec.slot_pos_after):
+                if p >= 0:
+                    _close(rec.scores_after[j], w[-1] if p == rec.t else cur[int(p)], 1e-6, 1e-8,
+                           "Top-K score = current weight")
+    assert checked > 30
+
+
 PINS = [pin_full_budget_is_dense, pin_no_heavy_is_sliding_window,
         pin_victim_is_argmin_of_recomputed_scores, pin_uniform_attention_closed_form,
         pin_mass_and_slot_invariants, pin_small_local_is_unprotected_argmin,
         pin_hand_built_ties_and_protection, pin_prefill_equal_sums_keep_later, pin_prompt_fits_budget, pin_bf16_is_exact_widening,
-        pin_near_tie_adoption]
+        pin_near_tie_adoption, pin_local_policy_is_the_window, pin_sink_window_keeps_sinks_and_recent,
+        pin_strided_keeps_its_grid, pin_topk_ranks_by_current_attention]

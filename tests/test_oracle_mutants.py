@@ -42,6 +42,16 @@ MUTANTS = {
     "new_score_zero": ("    sc[target] = (float)p[n];", "    sc[target] = 0.0f;"),
     "wrong_position_written": ("    sp[target] = t;", "    sp[target] = t - 1;"),
     "evict_before_accumulate": ("      float add = (float)p[j];", "      float add = 0.0f;"),
+    "topk_accumulates": ("        sc[j] = add;  /* Top-K ranks by the current step's attention only */",
+                         "        sc[j] = sc[j] + add;"),
+    "topk_prefill_ranks_by_colsum": ("const double* start = pol->kind == H2O_ORACLE_POLICY_TOPK ? a : c;",
+                                     "const double* start = c;"),
+    "sink_off_by_one": ("case H2O_ORACLE_POLICY_SINK_WINDOW: return pos >= pol->n_sink;",
+                        "case H2O_ORACLE_POLICY_SINK_WINDOW: return pos > pol->n_sink;"),
+    "strided_grid_inverted": ("if (pol->kind == H2O_ORACLE_POLICY_STRIDED && pos % pol->stride == 0) return",
+                              "if (pol->kind == H2O_ORACLE_POLICY_STRIDED && pos % pol->stride != 0) return"),
+    "local_evicts_newest": ("if (best < 0 || position_rank(pol, sp[j]) < position_rank(pol, sp[best])) best = j;",
+                            "if (best < 0 || position_rank(pol, sp[j]) > position_rank(pol, sp[best])) best = j;"),
     "new_value_row_from_key": ("memcpy(vc + (size_t)target * row, (const char*)v_new",
                                "memcpy(vc + (size_t)target * row, (const char*)k_new"),
 }

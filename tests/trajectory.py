@@ -55,10 +55,10 @@ def random_sequence(rng: np.random.Generator, length: int, D: int, dtype: str,
 
 
 def run(lib_path: str, q_seq, k_seq, v_seq, P: int, S: int, budget: int, k_heavy: int,
-        k_local: int, prefer=None) -> Trajectory:
+        k_local: int, prefer=None, policy=None) -> Trajectory:
     """One unit: prefill on positions 0..P-1, then decode positions P..P+S-1."""
     D = q_seq.shape[1]
-    orc = oracle.Oracle(budget, k_heavy, k_local, lib_path=lib_path)
+    orc = oracle.Oracle(budget, k_heavy, k_local, lib_path=lib_path, policy=policy)
     st = orc.new_state(1, D, q_seq.dtype)
     colsum, pinfo = orc.prefill_select(q_seq[None, :P], k_seq[None, :P], v_seq[None, :P], st,
                                        want_colsum=True)
