@@ -80,6 +80,28 @@ typedef struct {
   int32_t dtype;     /* h2o_dtype of q/k/v/out and the K/V caches                             */
 } h2o_dims;
 
+/* Eviction policies. H2O is the method; the others are the baselines the pages compare it with
+ * (the ttsmallhot.github.io post's §3.1.1 "Local" and "Top-K", StreamingLLM's attention sinks named
+ * in its §4, and a fixed-stride rule after its "Strided" sparse-attention baseline), run through the
+ * same cache state so they can be compared under the same budget. */
+typedef enum {
+  H2O_POLICY_H2O = 0,          /* lowest accumulated score among positions <= t - k_local           */
+  H2O_POLICY_LOCAL = 1,        /* the oldest cached position (sliding window of `budget` tokens)     */
+  H2O_POLICY_SINK_WINDOW = 2,  /* the oldest position >= n_sink: the first n_sink positions stay     */
+  H2O_POLICY_TOPK = 3,         /* like H2O, but each score is replaced by the step's weight instead
+                                  of accumulated; the prefill ranks by the last prompt token's
+                                  attention and seeds the scores with it                            */
+  H2O_POLICY_STRIDED = 4       /* among positions <= t - k_local, the oldest with pos % stride != 0,
+                                  else the oldest on the grid; the prefill keeps the newest grid
+                                  positions among the older ones                                     */
+} h2o_policy_kind;
+
+typedef struct {
+  int32_t kind;    /* h2o_policy_kind                                          */
+  int32_t n_sink;  /* H2O_POLICY_SINK_WINDOW: 0 <= n_sink < budget; else 0     */
+  int32_t stride;  /* H2O_POLICY_STRIDED: >= 1; else ignored                   */
+} h2o_policy;
+
 /* Device error word values. */
 #define H2O_DEVERR_NONE 0
 #define H2O_DEVERR_WAIT_TIMEOUT 1   /* a bounded wait on a copy or a peer block gave up       */
@@ -167,6 +189,28 @@ H2O_API h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const
                            const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                            float* scores, int32_t* slot_pos, void* out, int32_t* evicted_slot,
                            int32_t* evicted_pos, void* stream);
+
+/*
+ * h2o_prefill_select and h2o_decode_step under another eviction policy (policy == NULL means
+ * H2O_POLICY_H2O, i.e. the plain entry points). Same buffers, layouts and errors; an invalid policy
+ * (unknown kind, n_sink outside [0, budget), stride < 1) returns H2O_ERR_INVALID_ARG. Prefill
+ * selection per policy (prompt longer than the budget): Local keeps the last `budget` positions;
+ * sink + window the first n_sink and the last budget - n_sink; Top-K the last k_local plus the
+ * k_heavy older positions the last prompt token attends to most, with scores starting from that
+ * attention (the workspace's column-sum array then holds it); strided the last k_local plus the
+ * k_heavy newest older positions on its grid (then off it). A cache must be decoded under the policy
+ * it was prefilled with.
+ */
+H2O_API h2o_status h2o_prefill_select_policy(const h2o_dims* dims, const h2o_policy* policy,
+                                             int32_t prompt_len, const void* q, const void* k,
+                                             const void* v, void* k_cache, void* v_cache,
+                                             float* scores, int32_t* slot_pos, void* workspace,
+                                             size_t workspace_bytes, void* stream);
+H2O_API h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy* policy,
+                                          int32_t position, const void* q, const void* k_new,
+                                          const void* v_new, void* k_cache, void* v_cache,
+                                          float* scores, int32_t* slot_pos, void* out,
+                                          int32_t* evicted_slot, int32_t* evicted_pos, void* stream);
 
 /*
  * Synchronises `stream`, reads the current device's error word into *code (if code != NULL) and

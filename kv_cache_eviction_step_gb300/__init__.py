@@ -22,13 +22,14 @@ from . import build as _build
 F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = range(5)
 DEVERR_NONE, DEVERR_WAIT_TIMEOUT, DEVERR_NO_CANDIDATE = range(3)
+POLICY_H2O, POLICY_LOCAL, POLICY_SINK_WINDOW, POLICY_TOPK, POLICY_STRIDED = range(5)
 
 STATIC_SCRATCH_BYTES = 16 << 20  # H2O_STATIC_SCRATCH_BYTES
 
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
-           "h2o_prefill_select_static",
-           "h2o_decode_step", "h2o_get_device_error", "h2o_selftest_wait_timeout",
-           "h2o_last_cuda_error", "h2o_status_string")
+           "h2o_prefill_select_static", "h2o_prefill_select_policy",
+           "h2o_decode_step", "h2o_decode_step_policy", "h2o_get_device_error",
+           "h2o_selftest_wait_timeout", "h2o_last_cuda_error", "h2o_status_string")
 
 
 class Dims(ctypes.Structure):
@@ -45,6 +46,18 @@ class Dims(ctypes.Structure):
 
     def __repr__(self):
         return ("Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
+
+
+class Policy(ctypes.Structure):
+    """``h2o_policy``: which slot a decode step evicts (and which prompt positions prefill keeps)."""
+
+    _fields_ = [("kind", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("stride", ctypes.c_int32)]
+
+    def __init__(self, kind: int = POLICY_H2O, n_sink: int = 0, stride: int = 1):
+        super().__init__(kind, n_sink, stride)
+
+    def __repr__(self):
+        return f"Policy(kind={self.kind}, n_sink={self.n_sink}, stride={self.stride})"
 
 
 class H2OError(RuntimeError):
@@ -81,6 +94,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_prefill_select_static.restype = ctypes.c_int
     lib.h2o_decode_step.argtypes = [dp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.h2o_decode_step.restype = ctypes.c_int
+    pp = ctypes.POINTER(Policy)
+    lib.h2o_prefill_select_policy.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.h2o_prefill_select_policy.restype = ctypes.c_int
+    lib.h2o_decode_step_policy.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.h2o_decode_step_policy.restype = ctypes.c_int
     lib.h2o_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.h2o_get_device_error.restype = ctypes.c_int
     lib.h2o_selftest_wait_timeout.argtypes = [vp]
@@ -169,6 +187,31 @@ def h2o_decode_step(dims: Dims, position: int, q, k_new, v_new, k_cache, v_cache
         _ptr(evicted_pos), _stream(stream)))
 
 
+def _policy_ref(policy: Policy | None):
+    return None if policy is None else ctypes.byref(policy)
+
+
+def h2o_prefill_select_policy(dims: Dims, policy: Policy | None, prompt_len: int, q, k, v, k_cache,
+                              v_cache, scores, slot_pos, workspace, stream=None,
+                              workspace_bytes: int | None = None):
+    """h2o_prefill_select under ``policy`` (None = H2O)."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check("h2o_prefill_select_policy", load().h2o_prefill_select_policy(
+        ctypes.byref(dims), _policy_ref(policy), prompt_len, _ptr(q), _ptr(k), _ptr(v),
+        _ptr(k_cache), _ptr(v_cache), _ptr(scores), _ptr(slot_pos), _ptr(workspace), wb,
+        _stream(stream)))
+
+
+def h2o_decode_step_policy(dims: Dims, policy: Policy | None, position: int, q, k_new, v_new,
+                           k_cache, v_cache, scores, slot_pos, out, evicted_slot, evicted_pos,
+                           stream=None):
+    """h2o_decode_step under ``policy`` (None = H2O)."""
+    _check("h2o_decode_step_policy", load().h2o_decode_step_policy(
+        ctypes.byref(dims), _policy_ref(policy), position, _ptr(q), _ptr(k_new), _ptr(v_new),
+        _ptr(k_cache), _ptr(v_cache), _ptr(scores), _ptr(slot_pos), _ptr(out), _ptr(evicted_slot),
+        _ptr(evicted_pos), _stream(stream)))
+
+
 def h2o_get_device_error(stream=None) -> int:
     """Synchronise ``stream``, return and clear the device error word (0 = none)."""
     code = ctypes.c_int32(0)
@@ -187,9 +230,10 @@ class H2OCache:
     """Device buffers of one budgeted cache (caller-owned memory, allocated here with torch) and the
     running position. A convenience wrapper over the ABI calls; it computes nothing itself."""
 
-    def __init__(self, dims: Dims, prompt_len: int, device="cuda"):
+    def __init__(self, dims: Dims, prompt_len: int, device="cuda", policy: Policy | None = None):
         import torch
         self.dims = dims
+        self.policy = policy
         self.prompt_len = prompt_len
         self.position = prompt_len
         dt = torch.float32 if dims.dtype == F32 else torch.bfloat16
@@ -206,15 +250,15 @@ class H2OCache:
         self.evicted_pos = torch.empty(u, dtype=torch.int32, device=device)
 
     def prefill(self, q, k, v, stream=None):
-        h2o_prefill_select(self.dims, self.prompt_len, q, k, v, self.k_cache, self.v_cache,
-                           self.scores, self.slot_pos, self.workspace, stream)
+        h2o_prefill_select_policy(self.dims, self.policy, self.prompt_len, q, k, v, self.k_cache,
+                                  self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
         self.position = self.prompt_len
 
     def step(self, q, k_new, v_new, out=None, evicted_slot=None, evicted_pos=None, stream=None):
         out = self.out if out is None else out
         es = self.evicted_slot if evicted_slot is None else evicted_slot
         ep = self.evicted_pos if evicted_pos is None else evicted_pos
-        h2o_decode_step(self.dims, self.position, q, k_new, v_new, self.k_cache, self.v_cache,
-                        self.scores, self.slot_pos, out, es, ep, stream)
+        h2o_decode_step_policy(self.dims, self.policy, self.position, q, k_new, v_new, self.k_cache,
+                               self.v_cache, self.scores, self.slot_pos, out, es, ep, stream)
         self.position += 1
         return out, es, ep

@@ -79,6 +79,20 @@ h2o_status check_dims(const h2o_dims* d) {
 
 int elem_bytes(const h2o_dims* d) { return d->dtype == H2O_F32 ? 4 : 2; }
 
+h2o_status check_policy(const h2o_policy* pol, int32_t budget) {
+  switch (pol->kind) {
+    case H2O_POLICY_H2O:
+    case H2O_POLICY_LOCAL:
+    case H2O_POLICY_TOPK:
+      return H2O_OK;
+    case H2O_POLICY_SINK_WINDOW:
+      return (pol->n_sink >= 0 && pol->n_sink < budget) ? H2O_OK : H2O_ERR_INVALID_ARG;
+    case H2O_POLICY_STRIDED:
+      return pol->stride >= 1 ? H2O_OK : H2O_ERR_INVALID_ARG;
+  }
+  return H2O_ERR_INVALID_ARG;
+}
+
 h2o_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return H2O_OK;
   t_last_cuda_error = e;
@@ -128,7 +142,8 @@ size_t h2o_prefill_workspace_bytes(const h2o_dims* dims, int32_t prompt_len) {
 
 static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, const void* q,
                                       const void* k, float* colsum, void* workspace,
-                                      size_t workspace_bytes, cudaStream_t stream) {
+                                      size_t workspace_bytes, cudaStream_t stream,
+                                      bool last_row_only = false) {
   const int units = dims->units_b * dims->heads;
   const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
   PrefillParams p = {};
@@ -142,6 +157,7 @@ static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, 
   p.units = units;
   p.P = prompt_len;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
+  p.last_row_only = last_row_only ? 1 : 0;
   (void)workspace_bytes;
   // bf16: tcgen05 tensor cores (bf16 x bf16 products are exact in the fp32 accumulator); fp32 stays
   // on the CUDA cores, where the products are not rounded to tf32.
@@ -173,11 +189,15 @@ h2o_status h2o_prefill_scores(const h2o_dims* dims, int32_t prompt_len, const vo
                              static_cast<cudaStream_t>(stream));
 }
 
-h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const void* q,
-                              const void* k, const void* v, void* k_cache, void* v_cache,
-                              float* scores, int32_t* slot_pos, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+static h2o_status prefill_select_impl(const h2o_dims* dims, const h2o_policy* policy,
+                                      int32_t prompt_len, const void* q, const void* k,
+                                      const void* v, void* k_cache, void* v_cache, float* scores,
+                                      int32_t* slot_pos, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
   h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
+  if (st != H2O_OK) return st;
+  const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
+  st = check_policy(&pol, dims->budget);
   if (st != H2O_OK) return st;
   if (dims->budget > select_max_budget()) return H2O_ERR_UNSUPPORTED;
   if (dims->units_b == 0) return H2O_OK;
@@ -189,7 +209,8 @@ h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const vo
   const int units = dims->units_b * dims->heads;
   const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
   float* colsum = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + 2 * arr);
-  st = prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes, s);
+  st = prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes, s,
+                           pol.kind == H2O_POLICY_TOPK);
   if (st != H2O_OK) return st;
   SelectParams p = {};
   p.colsum = colsum;
@@ -205,14 +226,54 @@ h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const vo
   p.k_heavy = dims->k_heavy;
   p.k_local = dims->k_local;
   p.row_bytes = dims->head_dim * elem_bytes(dims);
+  p.key_mode = 0;
+  p.stride = 1;
+  switch (pol.kind) {
+    case H2O_POLICY_LOCAL:  // the last `budget` positions
+      p.k_heavy = 0;
+      p.k_local = dims->budget;
+      break;
+    case H2O_POLICY_SINK_WINDOW:  // the first n_sink positions and the last budget - n_sink
+      p.k_heavy = pol.n_sink;
+      p.k_local = dims->budget - pol.n_sink;
+      p.key_mode = 2;
+      break;
+    case H2O_POLICY_STRIDED:
+      p.key_mode = 1;
+      p.stride = pol.stride;
+      break;
+    default:  // H2O ranks by column sums, Top-K by the last row's attention (same array)
+      break;
+  }
   return from_cuda(launch_select(p, s));
 }
 
-h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q,
-                           const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                           float* scores, int32_t* slot_pos, void* out, int32_t* evicted_slot,
-                           int32_t* evicted_pos, void* stream) {
+h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, const void* q,
+                              const void* k, const void* v, void* k_cache, void* v_cache,
+                              float* scores, int32_t* slot_pos, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return prefill_select_impl(dims, nullptr, prompt_len, q, k, v, k_cache, v_cache, scores, slot_pos,
+                             workspace, workspace_bytes, stream);
+}
+
+h2o_status h2o_prefill_select_policy(const h2o_dims* dims, const h2o_policy* policy,
+                                     int32_t prompt_len, const void* q, const void* k,
+                                     const void* v, void* k_cache, void* v_cache, float* scores,
+                                     int32_t* slot_pos, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return prefill_select_impl(dims, policy, prompt_len, q, k, v, k_cache, v_cache, scores, slot_pos,
+                             workspace, workspace_bytes, stream);
+}
+
+static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* policy,
+                                   int32_t position, const void* q, const void* k_new,
+                                   const void* v_new, void* k_cache, void* v_cache, float* scores,
+                                   int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                                   int32_t* evicted_pos, void* stream) {
   h2o_status st = check_dims(dims);
+  if (st != H2O_OK) return st;
+  const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
+  st = check_policy(&pol, dims->budget);
   if (st != H2O_OK) return st;
   if (position < 1) return H2O_ERR_INVALID_ARG;
   if (dims->units_b == 0) return H2O_OK;
@@ -242,6 +303,9 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
   p.position = position;
   p.n = position < dims->budget ? position : dims->budget;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
+  p.policy = pol.kind;
+  p.n_sink = pol.n_sink;
+  p.stride = pol.kind == H2O_POLICY_STRIDED ? pol.stride : 1;
   // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
   // over units. Other shapes (fp32, D = 64, caches beyond 8192 slots) use the CUDA-core kernel, each
   // unit split over a CTA cluster when units are few.
@@ -255,6 +319,23 @@ h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q
                    &p.grid))
     return H2O_ERR_UNSUPPORTED;
   return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q,
+                           const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           float* scores, int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                           int32_t* evicted_pos, void* stream) {
+  return decode_step_impl(dims, nullptr, position, q, k_new, v_new, k_cache, v_cache, scores,
+                          slot_pos, out, evicted_slot, evicted_pos, stream);
+}
+
+h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy* policy, int32_t position,
+                                  const void* q, const void* k_new, const void* v_new,
+                                  void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
+                                  void* out, int32_t* evicted_slot, int32_t* evicted_pos,
+                                  void* stream) {
+  return decode_step_impl(dims, policy, position, q, k_new, v_new, k_cache, v_cache, scores,
+                          slot_pos, out, evicted_slot, evicted_pos, stream);
 }
 
 h2o_status h2o_selftest_wait_timeout(void* stream) {

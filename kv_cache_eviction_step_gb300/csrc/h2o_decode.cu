@@ -86,14 +86,6 @@ __host__ __device__ inline Layout decode_layout(int stages, int chunk) {
   return L;
 }
 
-// Sort key of an eviction candidate: smaller key = evicted first. Orders by score (IEEE order made
-// unsigned-monotonic), then by position.
-__device__ __forceinline__ unsigned long long evict_key(float score, int32_t pos) {
-  uint32_t b = __float_as_uint(score);
-  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(pos);
-}
-
 template <typename T>
 __device__ __forceinline__ void unpack16(const uint4& r, float* f) {
   if constexpr (sizeof(T) == 2) {
@@ -375,14 +367,13 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_step_kernel(const DecodeP
   int32_t best_slot = -1;
   for (int r = tid; r < rows; r += kConsumers) {
     const float pr = expf(logit[r] - mg) / lg;
-    const float ns = sc[r] + pr;
+    const float ns = p.policy == H2O_POLICY_TOPK ? pr : sc[r] + pr;  // Top-K: this step's weight
     sc[r] = ns;
-    if (cache_full && sp[r] <= last_candidate) {
-      const unsigned long long key = evict_key(ns, sp[r]);
-      if (key < best) {
-        best = key;
-        best_slot = c0 + r;
-      }
+    bool cand = false;
+    const unsigned long long key = policy_key(p.policy, ns, sp[r], last_candidate, p.n_sink, p.stride, &cand);
+    if (cache_full && cand && key < best) {
+      best = key;
+      best_slot = c0 + r;
     }
   }
   const float p_new = expf(s_new - mg) / lg;

@@ -77,6 +77,7 @@ struct TcDecodeParams {
   int32_t* err;
   int32_t units, budget, k_local, position, n, tiles;
   float scale;
+  int32_t policy, n_sink, stride;  // eviction policy (h2o_policy_kind)
 };
 
 // ---- PTX wrappers (same encodings as the prefill's tcgen05 path) -------------------------------
@@ -159,12 +160,6 @@ __device__ __forceinline__ void tmem_ld2(uint32_t taddr, float& a, float& b) {
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
 
-__device__ __forceinline__ unsigned long long evict_key_tc(float score, int32_t pos) {
-  uint32_t b = __float_as_uint(score);
-  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(pos);
-}
-
 // Byte offset of element j (0..n) of row `row` (0 = hi, 1 = lo) of the w operand: 64 slots per
 // 2 KB box, 128-byte rows, 16-byte chunks swizzled by the row index.
 __device__ __forceinline__ int w_offset(int j, int row) {
@@ -172,7 +167,10 @@ __device__ __forceinline__ int w_offset(int j, int row) {
   return box * kSmallBox + row * 128 + ((((jj >> 3) ^ row) & 7) << 4) + ((jj & 7) << 1);
 }
 
+// kAnyPolicy = false compiles the H2O rule alone (the policy switch folds away); true reads it from p.
+template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid_constant__ TcDecodeParams p) {
+  const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
@@ -406,13 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
       for (int t = 0; t < kMaxTiles; ++t) {
         if (t < T && t * kTileRows + tid < n) {
           const float pr = e[t] / l;
-          sc[t] = sc[t] + pr;
-          if (cache_full && sp[t] <= last_candidate) {
-            const unsigned long long key = evict_key_tc(sc[t], sp[t]);
-            if (key < best) {
-              best = key;
-              best_slot = t * kTileRows + tid;
-            }
+          sc[t] = policy == H2O_POLICY_TOPK ? pr : sc[t] + pr;  // Top-K: this step's weight
+          bool cand = false;
+          const unsigned long long key =
+              policy_key(policy, sc[t], sp[t], last_candidate, p.n_sink, p.stride, &cand);
+          if (cache_full && cand && key < best) {
+            best = key;
+            best_slot = t * kTileRows + tid;
           }
         }
       }
@@ -581,8 +579,10 @@ __device__ __forceinline__ int w_offset_narrow(int j, int row) {
   return box * kNarrowBox + row * 128 + ((((jj >> 3) ^ row) & 7) << 4) + ((jj & 7) << 1);
 }
 
+template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const __grid_constant__ TcSplitParams sp_) {
   const TcDecodeParams& p = sp_.d;
+  const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem;
@@ -784,13 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     for (int t = 0; t < kMaxTiles; ++t) {
       const int jl = t * kTileRows + tid;
       if (t < T && jl < rows) {
-        sc[t] = sc[t] + expf(s[t] - mg) / l;
-        if (cache_full && sp[t] <= last_candidate) {
-          const unsigned long long key = evict_key_tc(sc[t], sp[t]);
-          if (key < best) {
-            best = key;
-            best_slot = c0 + jl;
-          }
+        const float pr = expf(s[t] - mg) / l;
+        sc[t] = policy == H2O_POLICY_TOPK ? pr : sc[t] + pr;  // Top-K: this step's weight
+        bool cand = false;
+        const unsigned long long key =
+            policy_key(policy, sc[t], sp[t], last_candidate, p.n_sink, p.stride, &cand);
+        if (cache_full && cand && key < best) {
+          best = key;
+          best_slot = c0 + jl;
         }
       }
     }
@@ -962,8 +963,17 @@ cudaError_t fill_params(const DecodeParams& dp, TcDecodeParams& p) {
   p.n = dp.n;
   p.tiles = (dp.n + kTileRows - 1) / kTileRows;
   p.scale = dp.scale;
+  p.policy = dp.policy;
+  p.n_sink = dp.n_sink;
+  p.stride = dp.stride;
   return cudaSuccess;
 }
+
+// The H2O-only and the any-policy instantiations of each kernel.
+const void* const kSplitKernels[2] = {reinterpret_cast<const void*>(h2o_decode_tc_split_kernel<false>),
+                                      reinterpret_cast<const void*>(h2o_decode_tc_split_kernel<true>)};
+const void* const kTcKernels[2] = {reinterpret_cast<const void*>(h2o_decode_tc_kernel<false>),
+                                   reinterpret_cast<const void*>(h2o_decode_tc_kernel<true>)};
 
 struct SplitPlan {
   int dev = -1, units = -1, n = -1;
@@ -1021,12 +1031,12 @@ bool plan_split(int units, int n, int* splits_out, int* chunk_out) {
     bool found = false;
     for (int d : ready) found |= d == dev;
     if (!found) {
-      if (cudaFuncSetAttribute(h2o_decode_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSplitSmem) != cudaSuccess ||
-          cudaFuncSetAttribute(h2o_decode_tc_split_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-              cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
+      for (const void* fn : kSplitKernels) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+          (void)cudaGetLastError();
+          return false;
+        }
       }
       ready.push_back(dev);
     }
@@ -1034,12 +1044,12 @@ bool plan_split(int units, int n, int* splits_out, int* chunk_out) {
   if (splits > 1) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = split_config(splits, splits, nullptr, attr);
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(h2o_decode_tc_split_kernel), &cfg) !=
-            cudaSuccess ||
-        clusters == 0) {
-      (void)cudaGetLastError();
-      return false;
+    for (const void* fn : kSplitKernels) {
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters == 0) {
+        (void)cudaGetLastError();
+        return false;
+      }
     }
   }
   memo.splits = splits;
@@ -1066,7 +1076,7 @@ cudaError_t launch_decode_tc_split(const DecodeParams& dp, cudaStream_t stream) 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = split_config(dp.units, sp.splits, stream, attr);
   void* args[] = {&sp};
-  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(h2o_decode_tc_split_kernel), args);
+  return cudaLaunchKernelExC(&cfg, kSplitKernels[dp.policy != H2O_POLICY_H2O], args);
 }
 
 bool decode_tc_supported(int head_dim, int dtype, int budget) {
@@ -1089,15 +1099,20 @@ cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
     for (auto& d : ready)
       if (d.first == dev) sms = d.second;
     if (sms == 0) {
-      e = cudaFuncSetAttribute(h2o_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
+      for (const void* fn : kTcKernels) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+      }
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
       ready.emplace_back(dev, sms);
     }
   }
   const int grid = dp.units < sms ? dp.units : sms;
-  h2o_decode_tc_kernel<<<grid, kThreads, kSmem, stream>>>(p);
+  if (dp.policy == H2O_POLICY_H2O)
+    h2o_decode_tc_kernel<false><<<grid, kThreads, kSmem, stream>>>(p);
+  else
+    h2o_decode_tc_kernel<true><<<grid, kThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -34,6 +34,9 @@ struct DecodeParams {
   int32_t stages;       // ring depth in tiles
   int32_t grid;         // CTAs launched
   float scale;          // 1/sqrt(D)
+  int32_t policy;       // h2o_policy_kind
+  int32_t n_sink;       // sink + window
+  int32_t stride;       // strided
 };
 
 struct PrefillParams {
@@ -46,6 +49,7 @@ struct PrefillParams {
   int32_t units;
   int32_t P;
   float scale;
+  int32_t last_row_only;  // column-sum pass: write the last prompt row's attention instead
 };
 
 struct SelectParams {
@@ -59,9 +63,11 @@ struct SelectParams {
   int32_t units;
   int32_t P;
   int32_t budget;
-  int32_t k_heavy;
-  int32_t k_local;
+  int32_t k_heavy;      // older positions kept by key (policy-adjusted)
+  int32_t k_local;      // most recent positions kept (policy-adjusted)
   int32_t row_bytes;    // D * element size
+  int32_t key_mode;     // 0: by colsum value, 1: stride grid, 2: lowest positions
+  int32_t stride;
 };
 
 // ---- launchers (host) ---------------------------------------------------------------------
@@ -156,6 +162,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
 // before the phase it helps complete).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Eviction order of one cached slot under a policy: `key` smaller = evicted first; `cand` = the
+// slot may be evicted at all. score is the updated score (H2O: accumulated, Top-K: this step's).
+__device__ __forceinline__ unsigned long long policy_key(int32_t policy, float score, int32_t pos,
+                                                         int32_t last_candidate, int32_t n_sink,
+                                                         int32_t stride, bool* cand) {
+  switch (policy) {
+    case H2O_POLICY_LOCAL:
+      *cand = true;
+      return static_cast<uint32_t>(pos);
+    case H2O_POLICY_SINK_WINDOW:
+      *cand = pos >= n_sink;
+      return static_cast<uint32_t>(pos);
+    case H2O_POLICY_STRIDED:
+      *cand = pos <= last_candidate;
+      return (static_cast<unsigned long long>(pos % stride == 0) << 32) | static_cast<uint32_t>(pos);
+    default: {  // H2O, Top-K: (score, position), the score made order-preserving as unsigned bits
+      *cand = pos <= last_candidate;
+      uint32_t b = __float_as_uint(score);
+      b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+      return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(pos);
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

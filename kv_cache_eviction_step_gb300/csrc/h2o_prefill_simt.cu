@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(kThreads) prefill_colsum_kernel(const PrefillP
   stage<T, D>(ks, k + static_cast<size_t>(j0) * D, p.P - j0);
   const int j = j0 + r;
   float acc = 0.f;
-  for (int i0 = j0; i0 < p.P; i0 += kTile) {
+  // The last-row variant (Top-K prefill) only needs the tile holding query P-1.
+  const int i_first = p.last_row_only ? max(j0, (p.P - 1) / kTile * kTile) : j0;
+  for (int i0 = i_first; i0 < p.P; i0 += kTile) {
     __syncthreads();
     stage<T, D>(qs, q + static_cast<size_t>(i0) * D, p.P - i0);
     if (threadIdx.x < kTile) {
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) prefill_colsum_kernel(const PrefillP
     __syncthreads();
     for (int cc = c; cc < kTile; cc += kLanesX) {
       const int i = i0 + cc;
-      if (i < j || i >= p.P || j >= p.P) continue;
+      if (i < j || i >= p.P || j >= p.P || (p.last_row_only && i != p.P - 1)) continue;
       const float s = dot_rows<D>(ks, r, qs, cc) * p.scale;
       acc += expf(s - mi[cc]) / li[cc];
     }

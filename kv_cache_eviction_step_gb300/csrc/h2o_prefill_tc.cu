@@ -54,6 +54,7 @@ struct TcParams {
   int32_t P;
   int32_t tiles;           // ceil(P / 128)
   float scale;
+  int32_t last_row_only;   // column sums: only the last query's weight (Top-K prefill)
 };
 
 template <int D>
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.x;
   const int at = blockIdx.y;                           // resident tile index
-  const int t_begin = kColsum ? at : 0;                // streamed tiles [t_begin, t_end)
+  // streamed tiles [t_begin, t_end); the last-row variant only needs the tile holding query P-1
+  const int t_begin = kColsum ? (p.last_row_only ? p.tiles - 1 : at) : 0;
   const int t_end = kColsum ? p.tiles : at + 1;
   const int nt = t_end - t_begin;
   const int P = p.P;
@@ -241,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int a = t & 1;
       const int col0 = (t_begin + t) * kTile;  // first key (row stats) or query (column sums)
       // Tiles strictly off the diagonal and inside the prompt need no causal or tail mask.
-      const bool interior = (kColsum ? (t_begin + t > at) : (t_begin + t < at)) && col0 + kTile <= P;
+      const bool interior = (kColsum ? (t_begin + t > at) : (t_begin + t < at)) && col0 + kTile <= P &&
+                            !p.last_row_only;
       const float* tm = sm_m + (t & 1) * kTile;
       const float* til = sm_il + (t & 1) * kTile;
       if constexpr (kColsum) {
@@ -296,6 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (interior) {
 #pragma unroll
             for (int x = 0; x < 32; ++x) c += expf(v[x] * p.scale - tm[ch * 32 + x]) * til[ch * 32 + x];
+          } else if (p.last_row_only) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              if (x0 + x == P - 1 && row <= P - 1) c += expf(v[x] * p.scale - tm[ch * 32 + x]) * til[ch * 32 + x];
           } else {
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
@@ -395,6 +402,7 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
   p.P = pp.P;
   p.tiles = (pp.P + kTile - 1) / kTile;
   p.scale = pp.scale;
+  p.last_row_only = 0;
   cudaError_t e = launch_pass<D, false>(p, pp.units, s);  // resident Q, streamed K
   if (e != cudaSuccess) return e;
   const CUtensorMap q_map = p.tm_a;
@@ -402,6 +410,7 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
   p.tm_b = q_map;
   p.row_max_in = pp.row_max;
   p.row_sum_in = pp.row_sum;
+  p.last_row_only = pp.last_row_only;
   return launch_pass<D, true>(p, pp.units, s);
 }
 

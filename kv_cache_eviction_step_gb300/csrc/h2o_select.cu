@@ -32,6 +32,15 @@ __device__ __forceinline__ unsigned long long keep_key(float c, int32_t pos) {
   return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(pos);
 }
 
+// Ranking key of an older prompt position (larger = kept first): by column-sum value (H2O, and Top-K
+// whose array holds the last row's attention), by stride-grid membership then position (strided), or
+// lowest position first (the sinks of sink + window).
+__device__ __forceinline__ unsigned long long select_key(int mode, float c, int32_t pos, int32_t stride) {
+  if (mode == 1) return (static_cast<unsigned long long>(pos % stride == 0) << 32) | static_cast<uint32_t>(pos);
+  if (mode == 2) return 0xFFFFFFFFull - static_cast<uint32_t>(pos);
+  return keep_key(c, pos);
+}
+
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -75,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) prefill_select_kernel(const SelectPa
 
   if (tid == 0) threshold = ~0ull;
   if (!keep_all && p.k_heavy > 0) {
-    for (int i = tid; i < npad; i += kThreads) keys[i] = i < ncand ? keep_key(c[i], i) : 0ull;
+    for (int i = tid; i < npad; i += kThreads) keys[i] = i < ncand ? select_key(p.key_mode, c[i], i, p.stride) : 0ull;
     __syncthreads();
     for (int k = 2; k <= npad; k <<= 1) {
       for (int j = k >> 1; j > 0; j >>= 1) {
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) prefill_select_kernel(const SelectPa
   const int lo = min(P, tid * seg), hi = min(P, lo + seg);
   auto kept = [&](int j) {
     if (keep_all || j >= ncand) return true;
-    return p.k_heavy > 0 && keep_key(c[j], j) >= thr;
+    return p.k_heavy > 0 && select_key(p.key_mode, c[j], j, p.stride) >= thr;
   };
   int cnt = 0;
   for (int j = lo; j < hi; ++j) cnt += kept(j) ? 1 : 0;

@@ -110,3 +110,37 @@ def test_zero_units_is_a_noop(lib):
     d = dims(units_b=0)
     assert lib.h2o_decode_step(ctypes.byref(d), 10, *([None] * 10), None) == h2o.OK
     assert lib.h2o_prefill_select(ctypes.byref(d), 64, *([None] * 7), None, 0, None) == h2o.OK
+
+
+@pytest.mark.parametrize("pol", [
+    h2o.Policy(7),                                       # unknown kind
+    h2o.Policy(-1),
+    h2o.Policy(h2o.POLICY_SINK_WINDOW, n_sink=8),        # n_sink must stay below the budget
+    h2o.Policy(h2o.POLICY_SINK_WINDOW, n_sink=-1),
+    h2o.Policy(h2o.POLICY_STRIDED, stride=0),
+])
+def test_policy_entry_points_reject_bad_policies(lib, pol):
+    d = dims()
+    ptrs = [4096 * (i + 1) for i in range(10)]
+    assert lib.h2o_decode_step_policy(ctypes.byref(d), ctypes.byref(pol), 10, *ptrs, None) \
+        == h2o.ERR_INVALID_ARG
+    ws = h2o.h2o_prefill_workspace_bytes(d, 64)
+    assert lib.h2o_prefill_select_policy(ctypes.byref(d), ctypes.byref(pol), 64, *ptrs[:7], 4096, ws,
+                                         None) == h2o.ERR_INVALID_ARG
+    # rejected even when there is no unit to process
+    d0 = dims(units_b=0)
+    assert lib.h2o_decode_step_policy(ctypes.byref(d0), ctypes.byref(pol), 10, *([None] * 10), None) \
+        == h2o.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("pol", [None, h2o.Policy(), h2o.Policy(h2o.POLICY_LOCAL),
+                                 h2o.Policy(h2o.POLICY_SINK_WINDOW, n_sink=7),
+                                 h2o.Policy(h2o.POLICY_TOPK), h2o.Policy(h2o.POLICY_STRIDED, stride=3)])
+def test_policy_entry_points_accept_valid_policies(lib, pol):
+    d0 = dims(units_b=0)
+    ref = None if pol is None else ctypes.byref(pol)
+    assert lib.h2o_decode_step_policy(ctypes.byref(d0), ref, 10, *([None] * 10), None) == h2o.OK
+    assert lib.h2o_prefill_select_policy(ctypes.byref(d0), ref, 64, *([None] * 7), None, 0, None) == h2o.OK
+    # the same argument checks as the plain entry points
+    d = dims()
+    assert lib.h2o_decode_step_policy(ctypes.byref(d), ref, 0, *([4096] * 10), None) == h2o.ERR_INVALID_ARG
