@@ -81,6 +81,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.h2o_oracle_run_unit.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                         ctypes.c_int64, vp, vp, vp, vp, vp]
     lib.h2o_oracle_run_unit.restype = ctypes.c_int
+    lib.h2o_oracle_prefill_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.h2o_oracle_prefill_attention.restype = ctypes.c_int
     return lib
 
 
@@ -94,6 +96,19 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib = _declare(ctypes.CDLL(path))
         _libs[path] = lib
         return lib
+
+
+def prefill_attention(q, k, v, lib_path: str = LIB) -> np.ndarray:
+    """Causal attention output of every prompt row, float64 [units, P, D]; q/k/v: [units, P, D]
+    float32 or bf16 bits (uint16)."""
+    q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+    units, P, D = q.shape
+    out = np.empty((units, P, D), dtype=np.float64)
+    rc = load(lib_path).h2o_oracle_prefill_attention(units, D, _dtype_code(q), P, _ptr(q), _ptr(k),
+                                                     _ptr(v), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"h2o_oracle_prefill_attention failed (code {rc})")
+    return out
 
 
 def _ptr(a):

@@ -460,6 +460,52 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
   return 0;
 }
 
+/* Causal attention output of the prompt ([post] §2.1.1: the weights are Softmax(QK^T / sqrt(d)) over
+ * the keys a row may see, here j <= i). Each row: float64 logits, their maximum, the exponentials and
+ * their sum, then the weighted sum of the value rows in position order. */
+int h2o_oracle_prefill_attention(int32_t units, int32_t D, int32_t dtype, int32_t P, const void* q,
+                                 const void* k, const void* v, double* out) {
+  if (units < 0 || D < 1 || P < 1) return -1;
+  if (dtype != H2O_ORACLE_F32 && dtype != H2O_ORACLE_BF16) return -3;
+  const double scale = 1.0 / sqrt((double)D);
+  const size_t eb = elem_bytes(dtype);
+  double* qrow = malloc(sizeof(double) * (size_t)D);
+  double* w = malloc(sizeof(double) * (size_t)P);
+  if (!qrow || !w) {
+    free(qrow);
+    free(w);
+    return -4;
+  }
+  for (int32_t u = 0; u < units; ++u) {
+    const size_t base = (size_t)u * P * D;
+    const void* qu = (const char*)q + base * eb;
+    const void* ku = (const char*)k + base * eb;
+    const void* vu = (const char*)v + base * eb;
+    for (int32_t i = 0; i < P; ++i) {
+      for (int32_t d = 0; d < D; ++d) qrow[d] = elem(qu, dtype, (size_t)i * D + d);
+      double m = -INFINITY;
+      for (int32_t j = 0; j <= i; ++j) {
+        w[j] = dot(qrow, ku, dtype, (size_t)j, D) * scale;
+        if (w[j] > m) m = w[j];
+      }
+      double l = 0.0;
+      for (int32_t j = 0; j <= i; ++j) {
+        w[j] = exp(w[j] - m);
+        l += w[j];
+      }
+      double* o = out + base + (size_t)i * D;
+      for (int32_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int32_t j = 0; j <= i; ++j) acc += w[j] / l * elem(vu, dtype, (size_t)j * D + d);
+        o[d] = acc;
+      }
+    }
+  }
+  free(qrow);
+  free(w);
+  return 0;
+}
+
 /* ---- timing driver: one unit's prefill and decode steps back to back ----------------------- */
 
 int h2o_oracle_run_unit(int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local, int32_t dtype,

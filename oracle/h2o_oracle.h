@@ -121,6 +121,14 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
                                   double tie_rel, double err_rel, h2o_oracle_step_info* infos);
 
 /*
+ * Prompt pass of the attention layer: out[u][i] = sum over j <= i of softmax_j(q_i . k_j / sqrt(D))
+ * v_j, the causal attention output of every prompt row, whose weights the prefill's column sums add
+ * up. Inputs [units, P, D] in `dtype`; out [units, P, D] float64. Returns 0, or < 0 on bad sizes.
+ */
+int h2o_oracle_prefill_attention(int32_t units, int32_t D, int32_t dtype, int32_t P, const void* q,
+                                 const void* k, const void* v, double* out);
+
+/*
  * Convenience driver for timing: one unit's whole job, i.e. h2o_oracle_prefill_select on its prompt
  * followed by `steps` calls of h2o_oracle_decode_step at positions P, P+1, ... It adds no arithmetic.
  *   q, k, v                [P, D]         the unit's prompt

@@ -22,6 +22,7 @@ import numpy as np
 
 import bruteforce as bf
 import oracle
+import synth
 import trajectory as tj
 
 
@@ -427,9 +428,69 @@ def pin_topk_ranks_by_current_attention(lib):
     assert checked > 30
 
 
+def _as_storage(a, dtype):
+    a = np.asarray(a, dtype=np.float32)
+    return a if dtype == "f32" else synth.to_bf16_bits(a)
+
+
+def pin_prefill_attention_closed_forms(lib):
+    """Prompt-pass attention output (the step the column sums are taken from, post §2.1.1):
+    all-zero queries give prefix means of the value rows; a key aligned with every query and
+    thousands of logit units above the rest takes all the weight from its position on."""
+    rng = np.random.default_rng(41)
+    for dtype in ("f32", "bf16"):
+        for P, D in [(1, 4), (7, 4), (19, 8), (33, 1)]:
+            v = _as_storage(rng.standard_normal((P, D)), dtype)
+            V = bf.widen(v)
+            q = _as_storage(np.zeros((P, D)), dtype)
+            k = _as_storage(rng.standard_normal((P, D)), dtype)
+            out = oracle.prefill_attention(q[None], k[None], v[None], lib)[0]
+            want = np.cumsum(V, axis=0) / np.arange(1, P + 1)[:, None]
+            _close(out, want, 1e-13, 1e-14, f"zero-query prefix means P={P}")
+            # one dominant key at position js: logits 64 * 64 / sqrt(D) against 0 for the others
+            js = int(rng.integers(0, P))
+            e0 = np.zeros(D)
+            e0[0] = 64.0
+            q = _as_storage(np.tile(e0, (P, 1)), dtype)
+            kk = np.zeros((P, D))
+            kk[js] = e0
+            out = oracle.prefill_attention(q[None], _as_storage(kk, dtype)[None], v[None], lib)[0]
+            want[js:] = V[js]
+            _close(out, want, 1e-13, 1e-14, f"dominant key at {js}, P={P}")
+
+
+def pin_prefill_attention_weights_are_the_column_sum_weights(lib):
+    """With one-hot value rows (v_j = e_j, D = P) the output rows are the attention weight rows:
+    each sums to 1 and, added over the rows, they give the prefill column sums computed by the
+    selection path. The last row equals the decode step's output at t = P - 1 under a full budget."""
+    rng = np.random.default_rng(42)
+    for P in (1, 5, 12):
+        for dtype in ("f32", "bf16"):
+            D = P
+            q, k, _ = tj.random_sequence(rng, P, D, dtype, hh=2)
+            v = _as_storage(np.eye(P), dtype)
+            out = oracle.prefill_attention(q[None], k[None], v[None], lib)[0]
+            _close(out.sum(axis=1), np.ones(P), 1e-13, 1e-14, "one-hot output rows sum to 1")
+            assert np.all(np.triu(out, 1) == 0.0), "weight on a later position"
+            orc = oracle.Oracle(P + 1, 1, P, lib_path=lib)
+            st = orc.new_state(1, D, q.dtype)
+            c, _ = orc.prefill_select(q[None], k[None], v[None], st, want_colsum=True)
+            _close(out.sum(axis=0), c[0], 1e-12, 1e-13, "column sums of the output rows")
+    for dtype in ("f32", "bf16"):
+        P, D = 9, 8
+        q, k, v = tj.random_sequence(rng, P, D, dtype, hh=2)
+        out = oracle.prefill_attention(q[None], k[None], v[None], lib)[0]
+        orc = oracle.Oracle(P, 0, P, lib_path=lib)
+        st = orc.new_state(1, D, q.dtype)
+        orc.prefill_select(q[None, : P - 1], k[None, : P - 1], v[None, : P - 1], st)
+        o, _, _, _, _ = orc.decode_step(P - 1, q[None, P - 1], k[None, P - 1], v[None, P - 1], st)
+        _close(out[P - 1], o[0], 1e-12, 1e-13, "last prompt row vs decode step")
+
+
 PINS = [pin_full_budget_is_dense, pin_no_heavy_is_sliding_window,
         pin_victim_is_argmin_of_recomputed_scores, pin_uniform_attention_closed_form,
         pin_mass_and_slot_invariants, pin_small_local_is_unprotected_argmin,
         pin_hand_built_ties_and_protection, pin_prefill_equal_sums_keep_later, pin_prompt_fits_budget, pin_bf16_is_exact_widening,
         pin_near_tie_adoption, pin_local_policy_is_the_window, pin_sink_window_keeps_sinks_and_recent,
-        pin_strided_keeps_its_grid, pin_topk_ranks_by_current_attention]
+        pin_strided_keeps_its_grid, pin_topk_ranks_by_current_attention,
+        pin_prefill_attention_closed_forms, pin_prefill_attention_weights_are_the_column_sum_weights]

@@ -52,6 +52,12 @@ MUTANTS = {
                               "if (pol->kind == H2O_ORACLE_POLICY_STRIDED && pos % pol->stride != 0) return"),
     "local_evicts_newest": ("if (best < 0 || position_rank(pol, sp[j]) < position_rank(pol, sp[best])) best = j;",
                             "if (best < 0 || position_rank(pol, sp[j]) > position_rank(pol, sp[best])) best = j;"),
+    "attention_drops_sqrt_d": ("  const double scale = 1.0 / sqrt((double)D);\n  const size_t eb",
+                               "  const double scale = 1.0;\n  const size_t eb"),
+    "attention_unnormalised": ("acc += w[j] / l * elem(vu, dtype", "acc += w[j] * elem(vu, dtype"),
+    "attention_skips_diagonal": ("for (int32_t j = 0; j <= i; ++j) acc += w[j] / l",
+                                 "for (int32_t j = 0; j < i; ++j) acc += w[j] / l"),
+    "attention_values_from_keys": ("acc += w[j] / l * elem(vu, dtype", "acc += w[j] / l * elem(ku, dtype"),
     "new_value_row_from_key": ("memcpy(vc + (size_t)target * row, (const char*)v_new",
                                "memcpy(vc + (size_t)target * row, (const char*)k_new"),
 }
