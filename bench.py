@@ -259,6 +259,7 @@ def main():
                     help="override the workload's decode steps (shorter jobs for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill-forward", action="store_true")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.layers is not None:
@@ -395,6 +396,11 @@ def main():
             "clocks": clocks.summary(),
             "input_generation_s": t_gen}
 
+    # The prompt pass with the attention output (h2o_prefill_forward), timed on its own: not part of
+    # the step above, which builds the cache only.
+    if not args.no_prefill_forward:
+        line["prefill_forward"] = prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, args.warmup, K)
+
     # End to end through the public API with host buffers: every job copies its prompt and decode
     # inputs host->device (pinned) and the outputs and eviction indices device->host.
     if not args.no_e2e:
@@ -406,6 +412,52 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, warmup: int, reps: int) -> dict:
+    """h2o_prefill_forward (cache + the prompt's attention output) against h2o_prefill_select,
+    replayed from CUDA graphs and timed with CUDA events on the launching stream."""
+    import torch
+    P, D, U = w.prompt_len, w.head_dim, w.units
+    out = torch.empty((U, P, D), dtype=dv["q_prompt"].dtype, device=dev)
+    sp = stream.cuda_stream
+
+    def fwd():
+        h2o.h2o_prefill_forward(dims, None, P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], out,
+                                cache.k_cache, cache.v_cache, cache.scores, cache.slot_pos,
+                                cache.workspace, sp)
+
+    def sel():
+        h2o.h2o_prefill_select(dims, P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], cache.k_cache,
+                               cache.v_cache, cache.scores, cache.slot_pos, cache.workspace, sp)
+
+    times = {}
+    for name, fn in (("forward", fwd), ("select", sel)):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                g.replay()
+            ev[0].record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        times[name] = ev[0].elapsed_time(ev[1]) / reps
+    if h2o.h2o_get_device_error(sp) != 0:
+        raise RuntimeError("device error word set during the prefill-forward timing")
+    flops = 2.0 * D * P * (P + 1) * U  # causal Q K^T and P V: 2 D flops per (query, key <= query) each
+    return {"ms": times["forward"], "prefill_select_ms": times["select"],
+            "output_extra_ms": times["forward"] - times["select"],
+            "attention_tflops": flops / (times["forward"] / 1e3) / 1e12,
+            "kernels": "prefill_tc_kernel<D, row stats + output>, prefill_tc_kernel<D, column sums>, "
+                       "prefill_select_kernel" if w.dtype == "bf16" else "CUDA-core prefill kernels",
+            "output_bytes": U * P * D * w.elem_bytes}
 
 
 def e2e(args, w, h2o, dims, host, cache, stream, dev, world, tokens_per_job):

@@ -213,6 +213,22 @@ H2O_API h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy
                                           int32_t* evicted_slot, int32_t* evicted_pos, void* stream);
 
 /*
+ * Prefill forward of one attention layer with the budgeted cache built in the same pass
+ * (H2O post §2.1.1: the prompt's attention weights are Softmax(QK^T/sqrt(d)); their column sums are
+ * the scores h2o_prefill_select keeps by). Everything h2o_prefill_select_policy does, plus
+ *   out  [units, prompt_len, head_dim] dtype, device, caller-owned, 16-byte aligned: row i receives
+ *        the causal attention output sum_{j<=i} softmax_j(q_i . k_j / sqrt(D)) v_j of prompt row i.
+ * The bf16 path computes the probabilities in float32, rounds them to bf16 for the P V product
+ * (float32 accumulation) and the result to bf16; float32 stays in float32. The output shares the
+ * logits and exponentials of the row-statistics pass. NULL out: H2O_ERR_INVALID_ARG.
+ */
+H2O_API h2o_status h2o_prefill_forward(const h2o_dims* dims, const h2o_policy* policy,
+                                       int32_t prompt_len, const void* q, const void* k,
+                                       const void* v, void* out, void* k_cache, void* v_cache,
+                                       float* scores, int32_t* slot_pos, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, reads the current device's error word into *code (if code != NULL) and
  * clears it. Returns H2O_OK when the word was H2O_DEVERR_NONE, H2O_ERR_DEVICE when it was set, and
  * H2O_ERR_CUDA if the synchronisation or copy failed.

@@ -27,7 +27,7 @@ POLICY_H2O, POLICY_LOCAL, POLICY_SINK_WINDOW, POLICY_TOPK, POLICY_STRIDED = rang
 STATIC_SCRATCH_BYTES = 16 << 20  # H2O_STATIC_SCRATCH_BYTES
 
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
-           "h2o_prefill_select_static", "h2o_prefill_select_policy",
+           "h2o_prefill_select_static", "h2o_prefill_select_policy", "h2o_prefill_forward",
            "h2o_decode_step", "h2o_decode_step_policy", "h2o_get_device_error",
            "h2o_selftest_wait_timeout", "h2o_last_cuda_error", "h2o_status_string")
 
@@ -99,6 +99,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_prefill_select_policy.restype = ctypes.c_int
     lib.h2o_decode_step_policy.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.h2o_decode_step_policy.restype = ctypes.c_int
+    lib.h2o_prefill_forward.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.h2o_prefill_forward.restype = ctypes.c_int
     lib.h2o_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.h2o_get_device_error.restype = ctypes.c_int
     lib.h2o_selftest_wait_timeout.argtypes = [vp]
@@ -202,6 +204,18 @@ def h2o_prefill_select_policy(dims: Dims, policy: Policy | None, prompt_len: int
         _stream(stream)))
 
 
+def h2o_prefill_forward(dims: Dims, policy: Policy | None, prompt_len: int, q, k, v, out, k_cache,
+                        v_cache, scores, slot_pos, workspace, stream=None,
+                        workspace_bytes: int | None = None):
+    """h2o_prefill_select_policy that also writes the prompt's causal attention output ``out``
+    [units, P, D]."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check("h2o_prefill_forward", load().h2o_prefill_forward(
+        ctypes.byref(dims), _policy_ref(policy), prompt_len, _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+        _ptr(k_cache), _ptr(v_cache), _ptr(scores), _ptr(slot_pos), _ptr(workspace), wb,
+        _stream(stream)))
+
+
 def h2o_decode_step_policy(dims: Dims, policy: Policy | None, position: int, q, k_new, v_new,
                            k_cache, v_cache, scores, slot_pos, out, evicted_slot, evicted_pos,
                            stream=None):
@@ -249,9 +263,15 @@ class H2OCache:
         self.evicted_slot = torch.empty(u, dtype=torch.int32, device=device)
         self.evicted_pos = torch.empty(u, dtype=torch.int32, device=device)
 
-    def prefill(self, q, k, v, stream=None):
-        h2o_prefill_select_policy(self.dims, self.policy, self.prompt_len, q, k, v, self.k_cache,
-                                  self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
+    def prefill(self, q, k, v, out=None, stream=None):
+        """Build the cache from the prompt; with ``out`` ([units, P, D]) also write the prompt's
+        attention output."""
+        if out is None:
+            h2o_prefill_select_policy(self.dims, self.policy, self.prompt_len, q, k, v, self.k_cache,
+                                      self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
+        else:
+            h2o_prefill_forward(self.dims, self.policy, self.prompt_len, q, k, v, out, self.k_cache,
+                                self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
         self.position = self.prompt_len
 
     def step(self, q, k_new, v_new, out=None, evicted_slot=None, evicted_pos=None, stream=None):

@@ -143,7 +143,8 @@ size_t h2o_prefill_workspace_bytes(const h2o_dims* dims, int32_t prompt_len) {
 static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, const void* q,
                                       const void* k, float* colsum, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream,
-                                      bool last_row_only = false) {
+                                      bool last_row_only = false, const void* v = nullptr,
+                                      void* out = nullptr) {
   const int units = dims->units_b * dims->heads;
   const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
   PrefillParams p = {};
@@ -158,6 +159,8 @@ static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, 
   p.P = prompt_len;
   p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(dims->head_dim)));
   p.last_row_only = last_row_only ? 1 : 0;
+  p.v = v;
+  p.out = out;
   (void)workspace_bytes;
   // bf16: tcgen05 tensor cores (bf16 x bf16 products are exact in the fp32 accumulator); fp32 stays
   // on the CUDA cores, where the products are not rounded to tf32.
@@ -193,7 +196,7 @@ static h2o_status prefill_select_impl(const h2o_dims* dims, const h2o_policy* po
                                       int32_t prompt_len, const void* q, const void* k,
                                       const void* v, void* k_cache, void* v_cache, float* scores,
                                       int32_t* slot_pos, void* workspace, size_t workspace_bytes,
-                                      void* stream) {
+                                      void* stream, void* out = nullptr) {
   h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
   if (st != H2O_OK) return st;
   const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
@@ -210,7 +213,7 @@ static h2o_status prefill_select_impl(const h2o_dims* dims, const h2o_policy* po
   const size_t arr = round256(static_cast<size_t>(units) * prompt_len * 4);
   float* colsum = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + 2 * arr);
   st = prefill_scores_impl(dims, prompt_len, q, k, colsum, workspace, workspace_bytes, s,
-                           pol.kind == H2O_POLICY_TOPK);
+                           pol.kind == H2O_POLICY_TOPK, v, out);
   if (st != H2O_OK) return st;
   SelectParams p = {};
   p.colsum = colsum;
@@ -263,6 +266,15 @@ h2o_status h2o_prefill_select_policy(const h2o_dims* dims, const h2o_policy* pol
                                      void* stream) {
   return prefill_select_impl(dims, policy, prompt_len, q, k, v, k_cache, v_cache, scores, slot_pos,
                              workspace, workspace_bytes, stream);
+}
+
+h2o_status h2o_prefill_forward(const h2o_dims* dims, const h2o_policy* policy, int32_t prompt_len,
+                               const void* q, const void* k, const void* v, void* out,
+                               void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (dims != nullptr && dims->units_b > 0 && (out == nullptr || !aligned16(out))) return H2O_ERR_INVALID_ARG;
+  return prefill_select_impl(dims, policy, prompt_len, q, k, v, k_cache, v_cache, scores, slot_pos,
+                             workspace, workspace_bytes, stream, out);
 }
 
 static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* policy,

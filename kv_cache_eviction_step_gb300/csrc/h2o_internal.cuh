@@ -50,6 +50,8 @@ struct PrefillParams {
   int32_t P;
   float scale;
   int32_t last_row_only;  // column-sum pass: write the last prompt row's attention instead
+  const void* v;          // [units, P, D], with `out`
+  void* out;              // [units, P, D] prompt attention output, or nullptr
 };
 
 struct SelectParams {

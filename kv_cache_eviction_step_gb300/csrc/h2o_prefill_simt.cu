@@ -4,6 +4,7 @@
 //       s_ij = (q_i . k_j) / sqrt(D) (causal Softmax(QK^T/sqrt(d)), H2O post §2.1.1)
 //   P2  column sums c_j = sum_{i>=j} exp(s_ij - m_i) / l_i: the attention each prompt token has
 //       accumulated over the prompt (H2O post §2.1.2 / §2.2; "H2O Heavy-Hitter Oracle 分析" §3.1)
+//   and, when asked for, the prompt's attention output o_i = sum_{j<=i} exp(s_ij - m_i) / l_i v_j.
 //
 // This is the float32 path (a tensor-core f32 contraction would round the products through tf32)
 // and the plain reference-shaped path for bf16. A block of 128 threads owns 32 consecutive rows
@@ -134,12 +135,67 @@ __global__ void __launch_bounds__(kThreads) prefill_colsum_kernel(const PrefillP
   }
 }
 
+// The prompt's attention output with the final row statistics of P1:
+// o_i = sum_{j<=i} exp(s_ij - m_i) / l_i v_j. Block (x = unit, y = row tile); thread (r, c) computes
+// the weights of row r against keys c, c+4, ... of each streamed tile into shared memory, then
+// accumulates output elements c, c+4, ... of row r from the value tile staged in the same buffer.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) prefill_output_kernel(const PrefillParams p) {
+  __shared__ float qs[kTile][D + 1];
+  __shared__ float kv[kTile][D + 1];  // K tile, then V tile
+  __shared__ float ps[kTile][kTile + 1];
+  const int unit = blockIdx.x;
+  const int i0 = blockIdx.y * kTile;
+  const int r = threadIdx.x / kLanesX, c = threadIdx.x % kLanesX;
+  const size_t base = static_cast<size_t>(unit) * p.P;
+  const T* q = static_cast<const T*>(p.q) + base * D;
+  const T* k = static_cast<const T*>(p.k) + base * D;
+  const T* v = static_cast<const T*>(p.v) + base * D;
+  stage<T, D>(qs, q + static_cast<size_t>(i0) * D, p.P - i0);
+  const int i = i0 + r;
+  const float mi = i < p.P ? p.row_max[base + i] : 0.f;
+  const float il = i < p.P ? 1.f / p.row_sum[base + i] : 0.f;
+  float acc[D / kLanesX];
+#pragma unroll
+  for (int e = 0; e < D / kLanesX; ++e) acc[e] = 0.f;
+  for (int j0 = 0; j0 <= i0 + kTile - 1 && j0 < p.P; j0 += kTile) {
+    __syncthreads();
+    stage<T, D>(kv, k + static_cast<size_t>(j0) * D, p.P - j0);
+    __syncthreads();
+    for (int cc = c; cc < kTile; cc += kLanesX) {
+      const int j = j0 + cc;
+      ps[r][cc] = (j <= i && i < p.P && j < p.P) ? expf(dot_rows<D>(qs, r, kv, cc) * p.scale - mi) * il : 0.f;
+    }
+    __syncthreads();
+    stage<T, D>(kv, v + static_cast<size_t>(j0) * D, p.P - j0);
+    __syncthreads();
+    for (int jj = 0; jj < kTile; ++jj) {
+      const float w = ps[r][jj];
+#pragma unroll
+      for (int e = 0; e < D / kLanesX; ++e) acc[e] = fmaf(w, kv[jj][c + kLanesX * e], acc[e]);
+    }
+  }
+  if (i < p.P) {
+    T* o = static_cast<T*>(p.out) + (base + i) * D;
+#pragma unroll
+    for (int e = 0; e < D / kLanesX; ++e) {
+      if constexpr (sizeof(T) == 2) o[c + kLanesX * e] = __float2bfloat16_rn(acc[e]);
+      else o[c + kLanesX * e] = acc[e];
+    }
+  }
+}
+
 template <typename T, int D>
 cudaError_t launch_typed(const PrefillParams& p, cudaStream_t s) {
   const dim3 grid(p.units, (p.P + kTile - 1) / kTile);
   prefill_row_stats_kernel<T, D><<<grid, kThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.out != nullptr) {
+    prefill_output_kernel<T, D><<<grid, kThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   prefill_colsum_kernel<T, D><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -45,6 +45,7 @@ class Report:
     prefill_mismatches: int = 0
     max_out_err: float = 0.0
     max_score_rel_err: float = 0.0
+    max_prefill_out_err: float = 0.0
     topk: bool = False  # scores hold one step's weight, not a running sum
     notes: list = dataclasses.field(default_factory=list)
 
@@ -81,10 +82,12 @@ def widen(a: np.ndarray) -> np.ndarray:
 
 def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int = synth.DEFAULT_SEED,
         chunk_steps: int = 4096, state_every: int = 0, property_checks=None,
-        policy: tuple[int, int, int] | None = None) -> Report:
+        policy: tuple[int, int, int] | None = None, prefill_out: bool = False) -> Report:
     """Run ``steps`` decode steps (default: all) of workload ``w`` on the GPU for every unit, and the
     oracle in lockstep on ``check_units`` (default: all units). ``policy`` = (kind, n_sink, stride)
-    runs both sides under that eviction policy (None: H2O through the plain entry points)."""
+    runs both sides under that eviction policy (None: H2O through the plain entry points).
+    ``prefill_out`` builds the cache with h2o_prefill_forward and also compares the prompt's
+    attention output with the oracle's on the checked units."""
     import torch
 
     import kv_cache_eviction_step_gb300 as h2o
@@ -102,10 +105,19 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
     # Prefill for every unit on the GPU.
     prompt = synth.generate(w, seed, steps=0)
     q, kk, v = (to_device(a, w.dtype) for a in (prompt.q_prompt, prompt.k_prompt, prompt.v_prompt))
-    cache.prefill(q, kk, v)
+    pout = torch.empty_like(q) if prefill_out else None
+    cache.prefill(q, kk, v, out=pout)
     del q, kk, v
     torch.cuda.synchronize()
     assert h2o.h2o_get_device_error() == 0
+    if prefill_out and len(check_units) > 0:
+        got = widen(to_host(pout, w.dtype))[check_units]
+        ref = oracle.prefill_attention(prompt.q_prompt[check_units], prompt.k_prompt[check_units],
+                                       prompt.v_prompt[check_units])
+        rep.max_prefill_out_err = float(np.max(np.abs(got - ref)))
+        if rep.max_prefill_out_err > OUT_TOL[w.dtype]:
+            rep.notes.append(f"prefill output error {rep.max_prefill_out_err:.3e}")
+    del pout
 
     # Oracle prefill on the checked units, following the GPU's kept set only at near ties.
     follow = len(check_units) > 0

@@ -144,3 +144,19 @@ def test_policy_entry_points_accept_valid_policies(lib, pol):
     # the same argument checks as the plain entry points
     d = dims()
     assert lib.h2o_decode_step_policy(ctypes.byref(d), ref, 0, *([4096] * 10), None) == h2o.ERR_INVALID_ARG
+
+
+def test_prefill_forward_needs_an_aligned_output(lib):
+    d = dims()
+    ws = h2o.h2o_prefill_workspace_bytes(d, 64)
+    args = [4096 * (i + 1) for i in range(3)]
+    rest = [4096 * (i + 5) for i in range(4)]
+    assert lib.h2o_prefill_forward(ctypes.byref(d), None, 64, *args, None, *rest, 4096, ws, None) \
+        == h2o.ERR_INVALID_ARG
+    assert lib.h2o_prefill_forward(ctypes.byref(d), None, 64, *args, 4096 + 8, *rest, 4096, ws, None) \
+        == h2o.ERR_INVALID_ARG
+    bad = h2o.Policy(h2o.POLICY_STRIDED, stride=0)
+    assert lib.h2o_prefill_forward(ctypes.byref(d), ctypes.byref(bad), 64, *args, 4096, *rest, 4096, ws,
+                                   None) == h2o.ERR_INVALID_ARG
+    d0 = dims(units_b=0)
+    assert lib.h2o_prefill_forward(ctypes.byref(d0), None, 64, *([None] * 9), 0, None) == h2o.OK
