@@ -1,33 +1,37 @@
 // h2o_prefill_tc.cu -- prefill score pass (hot-path rows P1-P2) for bf16 on the 5th-generation
-// tensor cores (tcgen05, accumulators in tensor memory, operands staged by TMA).
+// tensor cores (tcgen05, accumulators in tensor memory, operands staged by TMA), and the prompt's
+// attention output when it is asked for.
 //
 //   P1  m_i = max_{j<=i} s_ij and l_i = sum_{j<=i} exp(s_ij - m_i), s_ij = (q_i . k_j) / sqrt(D)
 //       (causal Softmax(QK^T/sqrt(d)): H2O post §2.1.1)
 //   P2  c_j = sum_{i>=j} exp(s_ij - m_i) / l_i: the attention each prompt token accumulates over the
 //       prompt (H2O post §2.1.2 / §2.2; "H2O Heavy-Hitter Oracle 分析" §3.1)
-//
-//   P1+ with an output tensor, the row-stats pass is also the prompt's attention forward:
+//   P1+ with an output tensor, the row-statistics pass is also the prompt's attention forward:
 //       o_i = sum_{j<=i} exp(s_ij - m_i) / l_i v_j, sharing the logits and exponentials with P1.
 //
-// Both passes are the same kernel shape: one CTA keeps a 128-row "resident" tile of one operand and
-// streams 128-row tiles of the other, so that S = A B^T lands in tensor memory with one TMEM lane
-// (and so one epilogue thread) per resident row:
-//   row stats   resident = Q tile i, streamed = K tiles 0..i    -> rows are queries, reduce along j
-//   column sums resident = K tile j, streamed = Q tiles j..end  -> rows are keys, reduce along i,
-//               recomputing S instead of storing the P x P probabilities.
-// The output variant streams V tiles beside the K tiles; the epilogue writes exp(s - m) of each tile
-// as a bf16 128 x 128 probability tile in shared memory (K-major, 128-byte swizzle) and the tensor
-// core accumulates O += P V in a third tensor-memory region, with V read as an MN-major operand
-// straight from its TMA tile. The running maximum is updated lazily: O and l are rescaled only when a
-// tile's maximum exceeds the one in use by more than kLazyMax, so the probabilities stay below
-// e^kLazyMax and a rescale (tcgen05.ld / st of the row's O) is rare.
-// Warp roles: warps 0-3 are the epilogue (tcgen05.ld of their 32 TMEM lanes, masking, exp, running
-// reductions), warp 4 issues the TMA tensor loads (128-byte swizzle, two 64-column boxes per tile for
-// D = 128), warp 5 allocates tensor memory and one of its lanes issues tcgen05.mma (M = N = 128,
-// K = 16 per instruction, bf16 x bf16 -> fp32) into two alternating 128-column accumulators, so the
-// tensor core fills one while the epilogue drains the other. mbarriers link the roles: TMA ->
-// b_full -> MMA -> (tcgen05.commit) b_empty / acc_full -> epilogue -> acc_empty -> MMA. Every wait is
-// bounded (see mbar_wait); a CTA that gives up still frees its tensor memory before it exits.
+// One persistent kernel shape serves the three passes. A work item is one 128-row "resident" tile of
+// one unit; every CTA (one per SM) walks items blockIdx.x, +gridDim.x, ... and streams, per item,
+// 128-row tiles of the other operand, so that S = A B^T lands in tensor memory with one TMEM lane per
+// resident row:
+//   row stats    resident = Q tile i, streamed = K tiles 0..i   -> rows are queries, reduce along j
+//   column sums  resident = K tile j, streamed = Q tiles j..end -> rows are keys, reduce along i,
+//                recomputing S instead of storing the P x P probabilities.
+// Warp roles: warp 16 issues the TMA loads (resident tiles double-buffered, so the next item's tile
+// arrives while the current one is processed; streamed tiles through a ring), warp 17 allocates tensor
+// memory and one of its lanes issues tcgen05.mma (M = N = 128, K = 16 per instruction, bf16 x bf16 ->
+// fp32) into two alternating 128-column logit accumulators; warps 0-15 are the epilogue: warps q,
+// q + 4, q + 8, q + 12 share TMEM lanes 32q..32q+31 (rows) and take 32 columns each of every tile, so
+// sixteen warps keep the exponentials (the bound of this pass) busy; their partial row results are
+// combined once per item. Each exponential is one fma and one ex2: the 1/sqrt(D) scale and log2(e)
+// are folded into one multiplier.
+// The output pass also streams V tiles (ring order K_t, V_{t-1}: the product of tile t-1 runs while
+// the epilogue works on tile t). The epilogue writes exp(s - m) as a bf16 128 x 128 probability tile
+// (two buffers, K-major, 128-byte swizzle) from which the tensor core accumulates O += P V into a
+// third TMEM region, V read as an MN-major operand straight from its TMA tile. The maximum in use
+// moves only when a tile's maximum exceeds it by more than kLazyMax (log2 units): O and l are rescaled
+// then, rarely, and the probabilities stay below 2^kLazyMax. The warps of a row exchange their tile
+// maxima and sums through spare tensor-memory columns (shared memory is full).
+// Every wait is bounded (see mbar_wait); a CTA that gives up still frees its tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -44,43 +48,55 @@ namespace {
 constexpr int kTile = 128;                 // rows per operand tile (TMEM lanes / MMA M and N)
 constexpr int kBoxCols = 64;               // bf16 elements in one 128-byte swizzle row
 constexpr int kBoxBytes = kTile * 128;     // one [128 rows x 64 cols] bf16 box: 16 KB
-constexpr int kEpiWarps = 4;
+constexpr int kSplit = 4;                  // epilogue warps per TMEM lane quarter
+constexpr int kCols = kTile / kSplit;      // logit columns per epilogue warp and tile
+constexpr int kEpiWarps = 4 * kSplit;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr uint32_t kTmemCols = 2 * kTile;  // two fp32 128 x 128 accumulators
-constexpr int kCtrlBytes = 256;            // mbarriers + TMEM address slot
-constexpr int kAlign = 1024;               // 128-byte swizzle atoms repeat every 1024 bytes
-constexpr uint32_t kOCol = 2 * kTile;       // output variant: O accumulator columns [256, 256 + D)
-constexpr uint32_t kTmemColsOut = 512;
+constexpr uint32_t kTmemCols = 512;        // logits x2 [0, 256), output [256, 256 + D), exchange
+constexpr uint32_t kOCol = 2 * kTile;
+constexpr uint32_t kXCol = 448;            // output pass: [2][kSplit] max exchange, then [2][kSplit] l
 constexpr int kPBytes = 2 * kBoxBytes;     // 128 x 128 bf16 probability tile (two 64-key boxes)
-constexpr float kLazyMax = 8.f;            // rescale O only when the max grows by more than this
+constexpr int kAlign = 1024;               // 128-byte swizzle atoms repeat every 1024 bytes
+constexpr int kCtrlBytes = 256;            // mbarriers + TMEM address slot
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyMax = 8.f;            // output pass: rescale only when the max grows by > 2^8
+
+enum Mode { kRowStats = 0, kRowOut = 1, kColSums = 2 };
 
 struct TcParams {
   CUtensorMap tm_a;        // resident operand: Q (row stats) or K (column sums), [units][P][D]
   CUtensorMap tm_b;        // streamed operand: K (row stats) or Q (column sums)
-  CUtensorMap tm_v;        // output variant: V, [units][P][D]
-  __nv_bfloat16* out;      // output variant: [units][P][D]
+  CUtensorMap tm_v;        // output pass: V
   const float* row_max_in; // column sums: m_i from the row-stats pass, [units][P]
   const float* row_sum_in; // column sums: l_i
   float* row_max;          // row stats output
   float* row_sum;
   float* colsum;           // column sums output
+  __nv_bfloat16* out;      // output pass: [units][P][D]
   int32_t* err;
+  int32_t units;
   int32_t P;
   int32_t tiles;           // ceil(P / 128)
-  float scale;
+  float sl;                // log2(e) / sqrt(D)
   int32_t last_row_only;   // column sums: only the last query's weight (Top-K prefill)
 };
 
-template <int D>
+template <int D, int kMode>
 struct TcShape {
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = D == 128 ? 2 : 4;  // streamed-tile ring depth
-  static constexpr int kSmem = (1 + kStages) * kTileBytes + kCtrlBytes + 4 * kTile * 4 + kAlign;
-  // output variant: a V ring beside the K ring and the probability tile
-  static constexpr int kSmemOut = (1 + 2 * kStages) * kTileBytes + kPBytes + kCtrlBytes + 4 * kTile * 4 + kAlign;
+  // Streamed ring depth. The output pass also holds V tiles and two probability tiles, so its ring
+  // is shallower (it exchanges between warps through tensor memory); the other passes keep an
+  // exchange area for the partial row results ([2][kSplit][128] float2) and, for column sums, each
+  // warp's query statistics ([kEpiWarps][2][kCols] float).
+  static constexpr int kStages = kMode == kRowOut ? (D == 128 ? 3 : 6) : (D == 128 ? 4 : 8);
+  static constexpr int kXBytes = 2 * kSplit * kTile * 8;
+  static constexpr int kHeadBytes = kCtrlBytes + (kMode == kRowOut ? 0 : kXBytes + kEpiWarps * 2 * kCols * 4);
+  static constexpr int kBodyBytes = (2 + kStages) * kTileBytes + (kMode == kRowOut ? 2 * kPBytes : 0);
+  static constexpr int kSmem = kHeadBytes + kAlign + kBodyBytes;
 };
 
 // ---- tcgen05 / TMA wrappers --------------------------------------------------------------------
@@ -101,9 +117,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major operand tile written by TMA with 128-byte swizzle:
-// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor version 1,
-// layout type 2 = SWIZZLE_128B. Advancing along K inside the 128-byte row moves the start address.
+// Shared-memory matrix descriptor of a K-major operand tile written with 128-byte swizzle: rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor version 1, layout type
+// 2 = SWIZZLE_128B. Advancing along K inside the 128-byte row moves the start address.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;              // leading byte offset (unused when swizzled)
@@ -133,7 +149,7 @@ constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               (static_cast<uint32_t>(D >> 3) << 17) | (static_cast<uint32_t>(kTile >> 4) << 24);
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate,
-                                         uint32_t idesc = kIdesc) {
+                                         uint32_t idesc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
@@ -188,6 +204,86 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* v) {
+  tmem_ld32(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int x = 0; x < 16; ++x) v[x] = __uint_as_float(r[x]);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v);
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const float* v) {
+  tmem_st32(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// One value per thread (lane) into TMEM column `taddr`, and kSplit consecutive columns back.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\ntcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+               "r"(__float_as_uint(v))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+  uint32_t r0, r1, r2, r3;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\ntcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(taddr)
+      : "memory");
+  v[0] = __uint_as_float(r0);
+  v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3);
+}
+
+// 2^x by the special-function unit (ex2.approx, relative error ~2^-22; results below 2^-126 flush to
+// zero, far below what a softmax weight or a column sum can resolve next to its row's maximum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max32(const float* v) {
+  float m[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) m[x] = fmaxf(v[x], v[x + 16]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int x = 0; x < w; ++x) m[x] = fmaxf(m[x], m[x + w]);
+  return m[0];
+}
+
 // Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -196,70 +292,81 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void epilogue_sync() {
-  asm volatile("bar.sync 2, %0;" ::"n"(32 * kEpiWarps) : "memory");
+// The kSplit epilogue warps sharing TMEM lane quarter q (warps q, q + 4, ...): named barrier 1 + q.
+__device__ __forceinline__ void quarter_sync(int q) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "n"(32 * kSplit) : "memory");
 }
 
-template <int D, bool kColsum, bool kOut>
+// Work item i -> (unit, resident tile). Items are ordered tile-major, heaviest tiles first, so that
+// the static stride over CTAs hands every CTA a similar mix of item sizes.
+struct Item {
+  int unit, at, t_begin, nt;
+};
+template <int kMode>
+__device__ __forceinline__ Item item_of(const TcParams& p, int i) {
+  Item it;
+  const int k = i / p.units;
+  it.unit = i - k * p.units;
+  if constexpr (kMode == kColSums) {
+    it.at = k;  // query tiles at..end
+    it.t_begin = p.last_row_only ? p.tiles - 1 : it.at;
+    it.nt = p.tiles - it.t_begin;
+  } else {
+    it.at = p.tiles - 1 - k;  // key tiles 0..at
+    it.t_begin = 0;
+    it.nt = it.at + 1;
+  }
+  return it;
+}
+
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
-  static_assert(!(kColsum && kOut), "the output is produced by the row-statistics pass");
-  using S = TcShape<D>;
+  using S = TcShape<D, kMode>;
   constexpr int kStages = S::kStages;
-  constexpr int kRing = kStages * S::kTileBytes;
-  constexpr int kCtrlOff = kOut ? S::kTileBytes + 2 * kRing + kPBytes : S::kTileBytes + kRing;
+  constexpr bool kOut = kMode == kRowOut;
+  constexpr bool kCol = kMode == kColSums;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
-  unsigned char* sa = smem;                            // resident tile
-  unsigned char* sb = smem + S::kTileBytes;            // streamed-tile ring
-  unsigned char* sv = sb + kRing;                      // output variant: V-tile ring
-  unsigned char* sp = sv + kRing;                      // output variant: probability tile
-  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + kCtrlOff);
-  uint64_t* b_full = a_full + 1;
-  uint64_t* b_empty = b_full + kStages;
-  uint64_t* acc_full = b_empty + kStages;
+  // head: mbarriers, TMEM slot, exchange areas; body (1024-aligned): resident x2, ring, P x2
+  unsigned char* head = smem_raw;
+  unsigned char* body = smem_raw + S::kHeadBytes;
+  body += (kAlign - (smem_u32(body) & (kAlign - 1))) & (kAlign - 1);
+  unsigned char* res = body;                                  // [2][kTileBytes]
+  unsigned char* ring = body + 2 * S::kTileBytes;             // [kStages][kTileBytes]
+  unsigned char* ptile = ring + kStages * S::kTileBytes;      // output pass: [2][kPBytes]
+  uint64_t* res_full = reinterpret_cast<uint64_t*>(head);
+  uint64_t* res_empty = res_full + 2;
+  uint64_t* ring_full = res_empty + 2;
+  uint64_t* ring_empty = ring_full + kStages;
+  uint64_t* acc_full = ring_empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* v_full = acc_empty + 2;                    // output variant only
-  uint64_t* v_empty = v_full + kStages;
-  uint64_t* p_full = v_empty + kStages;                // the epilogue wrote this tile's P
-  uint64_t* o_prog = p_full + 1;                       // one completion per O += P V
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_prog + 1);
-  // column sums: m_i and 1/l_i of the current query tile, double-buffered by tile parity
-  float* sm_m = reinterpret_cast<float*>(smem + kCtrlOff + kCtrlBytes);
-  float* sm_il = sm_m + 2 * kTile;
-  constexpr uint32_t kCols = kOut ? kTmemColsOut : kTmemCols;
+  uint64_t* p_full = acc_empty + 2;   // output pass: the epilogue wrote probability tile b
+  uint64_t* p_free = p_full + 2;      // output pass: the product reading probability tile b finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + 2);
+  float2* xh = reinterpret_cast<float2*>(head + kCtrlBytes);  // row stats / column sums: [2][kSplit][128]
+  float* xq = reinterpret_cast<float*>(head + kCtrlBytes + S::kXBytes);  // column sums: [warps][2][kCols]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x;
-  const int at = blockIdx.y;                           // resident tile index
-  // streamed tiles [t_begin, t_end); the last-row variant only needs the tile holding query P-1
-  const int t_begin = kColsum ? (p.last_row_only ? p.tiles - 1 : at) : 0;
-  const int t_end = kColsum ? p.tiles : at + 1;
-  const int nt = t_end - t_begin;
+  const int items = p.units * p.tiles;
   const int P = p.P;
 
   if (tid == 0) {
-    mbar_init(a_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&res_full[b], 1);
+      mbar_init(&res_empty[b], 1);
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+      mbar_init(&p_full[b], kEpiWarps);
+      mbar_init(&p_free[b], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
-      if constexpr (kOut) {
-        mbar_init(&v_full[s], 1);
-        mbar_init(&v_empty[s], 1);
-      }
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kEpiWarps);
-    }
-    if constexpr (kOut) {
-      mbar_init(p_full, kEpiWarps);
-      mbar_init(o_prog, 1);
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
     }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kCols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -270,261 +377,324 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      mbar_expect_tx(a_full, S::kTileBytes);
-      for (int b = 0; b < S::kBoxes; ++b)
-        tma_load_3d(sa + b * kBoxBytes, &p.tm_a, b * kBoxCols, at * kTile, unit, a_full);
-      for (int t = 0; t < nt; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&b_empty[s], static_cast<uint32_t>(t / kStages - 1) & 1u, p.err)) break;
-        mbar_expect_tx(&b_full[s], S::kTileBytes);
+      uint32_t r = 0;  // streamed tiles issued so far
+      bool ok = true;
+      auto stream = [&](const CUtensorMap* map, int row, int unit) {
+        const int s = static_cast<int>(r % kStages);
+        if (r >= static_cast<uint32_t>(kStages) && !mbar_wait(&ring_empty[s], (r / kStages - 1) & 1u, p.err))
+          return false;
+        mbar_expect_tx(&ring_full[s], S::kTileBytes);
         for (int b = 0; b < S::kBoxes; ++b)
-          tma_load_3d(sb + s * S::kTileBytes + b * kBoxBytes, &p.tm_b, b * kBoxCols, (t_begin + t) * kTile,
-                      unit, &b_full[s]);
-        if constexpr (kOut) {
-          if (t >= kStages && !mbar_wait(&v_empty[s], static_cast<uint32_t>(t / kStages - 1) & 1u, p.err)) break;
-          mbar_expect_tx(&v_full[s], S::kTileBytes);
-          for (int b = 0; b < S::kBoxes; ++b)
-            tma_load_3d(sv + s * S::kTileBytes + b * kBoxBytes, &p.tm_v, b * kBoxCols, t * kTile, unit, &v_full[s]);
+          tma_load_3d(ring + s * S::kTileBytes + b * kBoxBytes, map, b * kBoxCols, row, unit, &ring_full[s]);
+        ++r;
+        return true;
+      };
+      int prev_unit = -1, prev_last = 0;  // output pass: the previous item's last V tile
+      int k = 0;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++k) {
+        const Item it = item_of<kMode>(p, i);
+        const int rb = k & 1;
+        if (k >= 2 && !mbar_wait(&res_empty[rb], static_cast<uint32_t>(k / 2 - 1) & 1u, p.err)) break;
+        mbar_expect_tx(&res_full[rb], S::kTileBytes);
+        for (int b = 0; b < S::kBoxes; ++b)
+          tma_load_3d(res + rb * S::kTileBytes + b * kBoxBytes, &p.tm_a, b * kBoxCols, it.at * kTile, it.unit,
+                      &res_full[rb]);
+        for (int t = 0; t < it.nt && ok; ++t) {
+          ok = stream(&p.tm_b, (it.t_begin + t) * kTile, it.unit);
+          if constexpr (kOut) {
+            // V in the order the products consume it: V_{t-1} after K_t, and the previous item's
+            // last V after this item's K_0
+            if (ok && t > 0) ok = stream(&p.tm_v, (t - 1) * kTile, it.unit);
+            else if (ok && prev_unit >= 0) ok = stream(&p.tm_v, prev_last * kTile, prev_unit);
+          }
         }
+        prev_unit = it.unit;
+        prev_last = it.nt - 1;
+      }
+      if constexpr (kOut) {
+        if (ok && prev_unit >= 0) stream(&p.tm_v, prev_last * kTile, prev_unit);
       }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && mbar_wait(a_full, 0, p.err)) {
-      const uint32_t a_base = smem_u32(sa);
-      // Logits of tile t, then (output variant) O += P V of tile t-1 once the epilogue has written
-      // its probabilities, so the epilogue of tile t overlaps the product of tile t-1.
-      for (int t = 0; t < nt + (kOut ? 1 : 0); ++t) {
-        if (t < nt) {
-          const int s = t % kStages;
-          const int a = t & 1;
-          if (!mbar_wait(&b_full[s], static_cast<uint32_t>(t / kStages) & 1u, p.err)) break;
-          if (t >= 2 && !mbar_wait(&acc_empty[a], static_cast<uint32_t>(t / 2 - 1) & 1u, p.err)) break;
+    if (lane == 0) {
+      uint32_t r = 0, g = 0, pv = 0;  // streamed tiles consumed, logit tiles, products issued
+      bool ok = true;
+      bool pending = false;           // output pass: a P V product waiting for its probabilities
+      int pending_t = 0;              // its tile index within its item (0: overwrite O)
+      auto product = [&]() {
+        const uint32_t b = pv & 1u;
+        const int s = static_cast<int>(r % kStages);
+        if (!mbar_wait(&p_full[b], (pv / 2) & 1u, p.err)) return false;
+        if (!mbar_wait(&ring_full[s], (r / kStages) & 1u, p.err)) return false;
+        tc_fence_after();
+        const uint32_t p_base = smem_u32(ptile + b * kPBytes);
+        const uint32_t v_base = smem_u32(ring + s * S::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          // P: K-major, 64 keys per box, 32 bytes per 16-key step; V: MN-major, 16 key rows of 128
+          // bytes per step, 64-column groups one box apart.
+          const uint32_t off_p = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+          mma_bf16(tmem + kOCol, sw128_desc(p_base + off_p), sw128_desc_mn(v_base + kk * 2048, kBoxBytes),
+                   (pending_t > 0 || kk > 0) ? 1u : 0u, kIdescPV<D>);
+        }
+        mma_commit(&ring_empty[s]);
+        mma_commit(&p_free[b]);  // probability tile b may be rewritten, O may be read or rescaled
+        ++r;
+        ++pv;
+        return true;
+      };
+      int k = 0;
+      for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++k) {
+        const Item it = item_of<kMode>(p, i);
+        const int rb = k & 1;
+        if (!mbar_wait(&res_full[rb], static_cast<uint32_t>(k / 2) & 1u, p.err)) break;
+        const uint32_t a_base = smem_u32(res + rb * S::kTileBytes);
+        for (int t = 0; t < it.nt; ++t, ++g) {
+          const int s = static_cast<int>(r % kStages);
+          const uint32_t a = g & 1u;
+          if (!mbar_wait(&ring_full[s], (r / kStages) & 1u, p.err) ||
+              (g >= 2 && !mbar_wait(&acc_empty[a], (g / 2 - 1) & 1u, p.err))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t b_base = smem_u32(sb + s * S::kTileBytes);
+          const uint32_t b_base = smem_u32(ring + s * S::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;  // 16 bf16 = 32 bytes per step
-            mma_bf16(tmem + a * kTile, sw128_desc(a_base + off), sw128_desc(b_base + off), kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + a * kTile, sw128_desc(a_base + off), sw128_desc(b_base + off), kk > 0 ? 1u : 0u,
+                     kIdesc);
           }
-          mma_commit(&b_empty[s]);   // the streamed tile may be overwritten once these MMAs finish
-          mma_commit(&acc_full[a]);  // and the accumulator may be read
-        }
-        if constexpr (kOut) {
-          if (t >= 1) {
-            const int u = t - 1;
-            const int s = u % kStages;
-            if (!mbar_wait(p_full, static_cast<uint32_t>(u) & 1u, p.err)) break;
-            if (!mbar_wait(&v_full[s], static_cast<uint32_t>(u / kStages) & 1u, p.err)) break;
-            tc_fence_after();
-            const uint32_t p_base = smem_u32(sp);
-            const uint32_t v_base = smem_u32(sv + s * S::kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              // P: K-major, 64 keys per box, 32 bytes per 16-key step; V: MN-major, 16 key rows of
-              // 128 bytes per step, 64-column groups one box apart.
-              const uint32_t off_p = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-              mma_bf16(tmem + kOCol, sw128_desc(p_base + off_p), sw128_desc_mn(v_base + kk * 2048, kBoxBytes),
-                       (u > 0 || kk > 0) ? 1u : 0u, kIdescPV<D>);
+          mma_commit(&ring_empty[s]);  // the streamed tile may be overwritten once these MMAs finish
+          mma_commit(&acc_full[a]);    // and the logits may be read
+          if (t == it.nt - 1) mma_commit(&res_empty[rb]);
+          ++r;
+          if constexpr (kOut) {
+            // the product of the previous logit tile (this item's, or the previous item's last)
+            if (pending && !product()) {
+              ok = false;
+              break;
             }
-            mma_commit(&v_empty[s]);
-            mma_commit(o_prog);  // P may be overwritten, O may be read or rescaled
+            pending = true;
+            pending_t = t;
           }
         }
+      }
+      if constexpr (kOut) {
+        if (ok && pending) product();
       }
     }
     __syncwarp();
   } else {
-    // Epilogue: thread r owns resident row `row` (a query for row stats, a key for column sums).
-    const int r = tid;
-    const int row = at * kTile + r;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const size_t ubase = static_cast<size_t>(unit) * P;
-    float m = -INFINITY, l = 0.f, c = 0.f;
-    float m_use = -INFINITY;  // output variant: the maximum the probabilities and O are taken against
+    // Epilogue: warp q + 4h owns TMEM lanes 32q.. (resident rows) and columns 32h..32h+31 of a tile.
+    const int q = warp & 3, h = warp >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const float sl = p.sl;
     bool ok = true;
-    float m_next = 0.f, il_next = 0.f;  // column sums: the next query tile's statistics, prefetched
-    if constexpr (kColsum) {
-      const int i = t_begin * kTile + r;
-      if (i < P) {
-        m_next = p.row_max_in[ubase + i];
-        il_next = 1.f / p.row_sum_in[ubase + i];
-      }
-    }
-    for (int t = 0; t < nt; ++t) {
-      const int a = t & 1;
-      const int col0 = (t_begin + t) * kTile;  // first key (row stats) or query (column sums)
-      // Tiles strictly off the diagonal and inside the prompt need no causal or tail mask.
-      const bool interior = (kColsum ? (t_begin + t > at) : (t_begin + t < at)) && col0 + kTile <= P &&
-                            !p.last_row_only;
-      const float* tm = sm_m + (t & 1) * kTile;
-      const float* til = sm_il + (t & 1) * kTile;
-      if constexpr (kColsum) {
-        sm_m[(t & 1) * kTile + r] = m_next;
-        sm_il[(t & 1) * kTile + r] = il_next;
-        if (t + 1 < nt) {
-          const int i = col0 + kTile + r;
-          m_next = 0.f;
-          il_next = 0.f;
-          if (i < P) {
-            m_next = p.row_max_in[ubase + i];
-            il_next = 1.f / p.row_sum_in[ubase + i];
-          }
+    uint32_t g = 0;  // logit tiles consumed (over all items)
+    int k = 0;
+    float* xw = xq + warp * 2 * kCols;  // column sums: this warp's query statistics, [2][kCols]
+    // column sums: b_i = m_i log2(e) + log2(l_i) of a query, so that its weight is 2^(s sl - b_i)
+    auto qstat = [&](int unit, int i) {
+      if (i >= P) return INFINITY;  // queries past the prompt weigh nothing
+      const size_t o = static_cast<size_t>(unit) * P + i;
+      return fmaf(p.row_max_in[o], kLog2e, log2f(p.row_sum_in[o]));
+    };
+    for (int i = blockIdx.x; i < items; i += gridDim.x, ++k) {
+      const Item it = item_of<kMode>(p, i);
+      const int row = it.at * kTile + r;
+      const size_t ubase = static_cast<size_t>(it.unit) * P;
+      float m2 = -INFINITY, l = 0.f, c = 0.f;  // this warp's partial statistics (log2 units)
+      float mu = -INFINITY;  // output pass: the maximum the probabilities are taken against
+      float b_next = 0.f;
+      if constexpr (kCol) b_next = qstat(it.unit, it.t_begin * kTile + h * kCols + lane);
+      for (int t = 0; t < it.nt; ++t, ++g) {
+        const uint32_t a = g & 1u;
+        const int x0 = (it.t_begin + t) * kTile + h * kCols;  // key (query) of this warp's column 0
+        if constexpr (kCol) {
+          // this tile's query statistics for this warp's columns; prefetch the next tile's
+          xw[a * kCols + lane] = b_next;
+          if (t + 1 < it.nt) b_next = qstat(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
+          __syncwarp();
         }
-        epilogue_sync();  // this tile's statistics are visible (the buffer's previous readers finished
-                          // before the last iteration's barrier)
-      }
-      if (ok) ok = mbar_wait(&acc_full[a], static_cast<uint32_t>(t / 2) & 1u, p.err);
-      tc_fence_after();
-      if constexpr (kOut) {
-        // Sweep 1: the tile's maximum; the maximum in use moves only when exceeded by > kLazyMax.
-        float tmax = -INFINITY;
-#pragma unroll 1
-        for (int ch = 0; ch < kTile / 32; ++ch) {
-          float v[32];
-          tmem_ld32(lane_addr + a * kTile + ch * 32, v);
-          const int x0 = col0 + ch * 32;
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const bool valid = interior || (x0 + x <= row && x0 + x < P);
-            tmax = fmaxf(tmax, valid ? v[x] * p.scale : -INFINITY);
-          }
-        }
-        m = fmaxf(m, tmax);
-        float alpha = 1.f;
-        if (tmax > m_use + kLazyMax) {
-          alpha = expf(m_use - tmax);  // 0 on the first tile
-          l *= alpha;
-          m_use = tmax;
-        }
-        // O += P V of the previous tile has finished: P may be overwritten and O rescaled.
-        if (t > 0 && ok) ok = mbar_wait(o_prog, static_cast<uint32_t>(t - 1) & 1u, p.err);
+        if (ok) ok = mbar_wait(&acc_full[a], (g / 2) & 1u, p.err);
         tc_fence_after();
-        if (t > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            float o[32];
-            tmem_ld32(lane_addr + kOCol + ch * 32, o);
+        float v[kCols];
+        tmem_ld32(lane_addr + a * kTile + h * kCols, v);
+        if constexpr (!kCol) {
+          // the diagonal tile: keys j <= row and j < P (earlier tiles lie wholly below the diagonal)
+          if (t == it.at) {
+            const int lim = min(row, P - 1) - x0;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= alpha;
-            tmem_st32(lane_addr + kOCol + ch * 32, o);
+            for (int x = 0; x < kCols; ++x) v[x] = x <= lim ? v[x] : -INFINITY;
           }
         }
-        // Sweep 2: probabilities against m_use into row r of the P tile (bf16, 128-byte swizzle).
-#pragma unroll 1
-        for (int ch = 0; ch < kTile / 32; ++ch) {
-          float v[32];
-          tmem_ld32(lane_addr + a * kTile + ch * 32, v);
-          const int x0 = col0 + ch * 32;
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const bool valid = interior || (x0 + x <= row && x0 + x < P);
-            v[x] = valid ? expf(v[x] * p.scale - m_use) : 0.f;
-            l += v[x];
+        if constexpr (kMode == kRowStats) {
+          const float cm = max32(v) * sl;
+          if (cm > m2) {
+            l *= ex2(m2 - cm);
+            m2 = cm;
           }
-          unsigned char* box = sp + (ch >> 1) * kBoxBytes + r * 128;
+          if (m2 != -INFINITY) {
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int x = 0; x < kCols; ++x) s4[x & 3] += ex2(fmaf(v[x], sl, -m2));
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          }
+        } else if constexpr (kCol) {
+          const float4* b4 = reinterpret_cast<const float4*>(xw + a * kCols);
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          if (p.last_row_only) {
+            const int xl = P - 1 - x0;  // the last query's column, if this warp holds it
+            if (xl >= 0 && xl < kCols) {
+#pragma unroll
+              for (int x = 0; x < kCols; ++x)
+                if (x == xl && row <= P - 1) s4[0] += ex2(fmaf(v[x], sl, -xw[a * kCols + x]));
+            }
+          } else if (it.t_begin + t > it.at) {  // queries all after the keys
+#pragma unroll
+            for (int x4 = 0; x4 < kCols / 4; ++x4) {
+              const float4 b = b4[x4];
+              s4[0] += ex2(fmaf(v[4 * x4 + 0], sl, -b.x));
+              s4[1] += ex2(fmaf(v[4 * x4 + 1], sl, -b.y));
+              s4[2] += ex2(fmaf(v[4 * x4 + 2], sl, -b.z));
+              s4[3] += ex2(fmaf(v[4 * x4 + 3], sl, -b.w));
+            }
+          } else {  // the diagonal tile: queries i >= row
+            const int lo = row - x0;
+#pragma unroll
+            for (int x4 = 0; x4 < kCols / 4; ++x4) {
+              const float4 b = b4[x4];
+              s4[0] += 4 * x4 + 0 >= lo ? ex2(fmaf(v[4 * x4 + 0], sl, -b.x)) : 0.f;
+              s4[1] += 4 * x4 + 1 >= lo ? ex2(fmaf(v[4 * x4 + 1], sl, -b.y)) : 0.f;
+              s4[2] += 4 * x4 + 2 >= lo ? ex2(fmaf(v[4 * x4 + 2], sl, -b.z)) : 0.f;
+              s4[3] += 4 * x4 + 3 >= lo ? ex2(fmaf(v[4 * x4 + 3], sl, -b.w)) : 0.f;
+            }
+          }
+          c += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        } else {
+          // Output pass. Probability tile a was last read by the product of logit tile g - 2.
+          if (g >= 2 && ok) ok = mbar_wait(&p_free[a], (g / 2 - 1) & 1u, p.err);
+          // The tile's maximum over the quarter's kSplit warps, exchanged through TMEM columns.
+          tmem_st1(lane_addr + kXCol + a * kSplit + h, max32(v));
+          tc_fence_before();
+          quarter_sync(q);
+          tc_fence_after();
+          float xm[4];
+          tmem_ld4(lane_addr + kXCol + a * kSplit, xm);
+          const float tmax = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) * sl;
+          m2 = fmaxf(m2, tmax);
+          float alpha = 1.f;
+          if (tmax > mu + kLazyMax) {
+            alpha = ex2(mu - tmax);  // 0 on the first tile
+            l *= alpha;
+            mu = tmax;
+          }
+          // Rescaling O needs the product of tile g - 1 finished.
+          if (t > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+            if (ok) ok = mbar_wait(&p_free[a ^ 1u], ((g - 1) / 2) & 1u, p.err);
+            tc_fence_after();
+            constexpr int kOC = D / kSplit;  // output columns per warp
+            float o[kOC];
+            const uint32_t oaddr = lane_addr + kOCol + h * kOC;
+            tmem_ld<kOC>(oaddr, o);
+#pragma unroll
+            for (int x = 0; x < kOC; ++x) o[x] *= alpha;
+            tmem_st<kOC>(oaddr, o);
+          }
+          // Probabilities against mu (masked logits give 0) into this warp's 32 keys of tile a:
+          // 16-byte chunks (h & 1) * 4 .. + 3 of box h >> 1, row r.
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int x = 0; x < kCols; ++x) {
+            v[x] = ex2(fmaf(v[x], sl, -mu));
+            s4[x & 3] += v[x];
+          }
+          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          unsigned char* rowp = ptile + a * kPBytes + (h >> 1) * kBoxBytes + r * 128;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const int chunk = (ch & 1) * 4 + c4;  // 16-byte chunk (8 keys) within the 128-byte row
+            const int chunk = (h & 1) * 4 + c4;
             uint4 w;
             w.x = pack_bf16(v[c4 * 8 + 0], v[c4 * 8 + 1]);
             w.y = pack_bf16(v[c4 * 8 + 2], v[c4 * 8 + 3]);
             w.z = pack_bf16(v[c4 * 8 + 4], v[c4 * 8 + 5]);
             w.w = pack_bf16(v[c4 * 8 + 6], v[c4 * 8 + 7]);
-            *reinterpret_cast<uint4*>(box + ((chunk ^ (r & 7)) << 4)) = w;
+            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) = w;
           }
+          fence_async_smem();
         }
-        fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(p_full);
+          if constexpr (kOut) mbar_arrive(&p_full[a]);
           mbar_arrive(&acc_empty[a]);
         }
-      } else {
-#pragma unroll 1
-        for (int ch = 0; ch < kTile / 32; ++ch) {
-          float v[32];
-          tmem_ld32(lane_addr + a * kTile + ch * 32, v);
-          const int x0 = col0 + ch * 32;
-          if constexpr (!kColsum) {
-            // running max / normaliser over the causal keys j <= row of this chunk
-            float cm = -INFINITY;
-            if (interior) {
+      }
+      // Item end: combine the kSplit partial results of every row.
+      if constexpr (kMode == kRowStats) {
+        float2* xk = xh + (k & 1) * kSplit * kTile;  // by item parity: read before it is reused
+        xk[h * kTile + r] = make_float2(m2, l);
+        quarter_sync(q);
+        if (h == 0 && row < P) {
+          float mm = m2;
 #pragma unroll
-              for (int x = 0; x < 32; ++x) {
-                v[x] *= p.scale;
-                cm = fmaxf(cm, v[x]);
-              }
-            } else {
+          for (int j = 1; j < kSplit; ++j) mm = fmaxf(mm, xk[j * kTile + r].x);
+          float lt = 0.f;
 #pragma unroll
-              for (int x = 0; x < 32; ++x) {
-                const int j = x0 + x;
-                v[x] = (j <= row && j < P) ? v[x] * p.scale : -INFINITY;
-                cm = fmaxf(cm, v[x]);
-              }
-            }
-            if (cm > m) {
-              l *= expf(m - cm);
-              m = cm;
-            }
-            if (cm != -INFINITY) {
-#pragma unroll
-              for (int x = 0; x < 32; ++x) l += expf(v[x] - m);
-            }
-          } else {
-            // probabilities of the queries i >= row of this chunk that attend this key
-            if (interior) {
-#pragma unroll
-              for (int x = 0; x < 32; ++x) c += expf(v[x] * p.scale - tm[ch * 32 + x]) * til[ch * 32 + x];
-            } else if (p.last_row_only) {
-#pragma unroll
-              for (int x = 0; x < 32; ++x)
-                if (x0 + x == P - 1 && row <= P - 1) c += expf(v[x] * p.scale - tm[ch * 32 + x]) * til[ch * 32 + x];
-            } else {
-#pragma unroll
-              for (int x = 0; x < 32; ++x) {
-                const int i = x0 + x;
-                if (i >= row && i < P) c += expf(v[x] * p.scale - tm[ch * 32 + x]) * til[ch * 32 + x];
-              }
-            }
+          for (int j = 0; j < kSplit; ++j) {
+            const float2 o = xk[j * kTile + r];
+            if (o.x != -INFINITY) lt += o.y * ex2(o.x - mm);
           }
+          p.row_max[ubase + row] = mm * kLn2;
+          p.row_sum[ubase + row] = lt;
         }
+      } else if constexpr (kCol) {
+        float2* xk = xh + (k & 1) * kSplit * kTile;
+        xk[h * kTile + r] = make_float2(c, 0.f);
+        quarter_sync(q);
+        if (h == 0 && row < P) {
+          float ct = 0.f;
+#pragma unroll
+          for (int j = 0; j < kSplit; ++j) ct += xk[j * kTile + r].x;
+          p.colsum[ubase + row] = ct;
+        }
+      } else {
+        // l over the quarter's warps (all taken against the same mu), through TMEM columns
+        const uint32_t lcol = lane_addr + kXCol + 2 * kSplit + (k & 1) * kSplit;
+        tmem_st1(lcol + h, l);
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[a]);
-      }
-    }
-    if constexpr (kOut) {
-      // The last O += P V has finished: normalise the row and write it (bf16).
-      if (ok) ok = mbar_wait(o_prog, static_cast<uint32_t>(nt - 1) & 1u, p.err);
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = p.out + (ubase + static_cast<size_t>(row)) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        float o[32];
-        tmem_ld32(lane_addr + kOCol + ch * 32, o);
+        quarter_sync(q);
+        tc_fence_after();
+        float xl[4];
+        tmem_ld4(lcol, xl);
+        const float lt = (xl[0] + xl[1]) + (xl[2] + xl[3]);
+        // the last product of this item has finished: normalise and write this warp's columns
+        if (ok) ok = mbar_wait(&p_free[(g - 1) & 1u], ((g - 1) / 2) & 1u, p.err);
+        tc_fence_after();
+        constexpr int kOC = D / kSplit;
+        float o[kOC];
+        tmem_ld<kOC>(lane_addr + kOCol + h * kOC, o);
         if (row < P) {
+          const float inv_l = 1.f / lt;
+          __nv_bfloat16* orow = p.out + (ubase + static_cast<size_t>(row)) * D + h * kOC;
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c8 = 0; c8 < kOC / 8; ++c8) {
             uint4 w;
-            w.x = pack_bf16(o[c4 * 8 + 0] * inv_l, o[c4 * 8 + 1] * inv_l);
-            w.y = pack_bf16(o[c4 * 8 + 2] * inv_l, o[c4 * 8 + 3] * inv_l);
-            w.z = pack_bf16(o[c4 * 8 + 4] * inv_l, o[c4 * 8 + 5] * inv_l);
-            w.w = pack_bf16(o[c4 * 8 + 6] * inv_l, o[c4 * 8 + 7] * inv_l);
-            *reinterpret_cast<uint4*>(orow + ch * 32 + c4 * 8) = w;
+            w.x = pack_bf16(o[c8 * 8 + 0] * inv_l, o[c8 * 8 + 1] * inv_l);
+            w.y = pack_bf16(o[c8 * 8 + 2] * inv_l, o[c8 * 8 + 3] * inv_l);
+            w.z = pack_bf16(o[c8 * 8 + 4] * inv_l, o[c8 * 8 + 5] * inv_l);
+            w.w = pack_bf16(o[c8 * 8 + 6] * inv_l, o[c8 * 8 + 7] * inv_l);
+            *reinterpret_cast<uint4*>(orow + c8 * 8) = w;
+          }
+          if (h == 0) {
+            p.row_max[ubase + row] = m2 * kLn2;
+            p.row_sum[ubase + row] = lt * ex2(mu - m2);  // the normaliser against the true maximum
           }
         }
-      }
-      l *= expf(m_use - m);  // the normaliser against the true maximum, for the column-sum pass
-    }
-    if (row < P) {
-      if constexpr (!kColsum) {
-        p.row_max[ubase + row] = m;
-        p.row_sum[ubase + row] = l;
-      } else {
-        p.colsum[ubase + row] = c;
+        tc_fence_before();  // the O reads are ordered before the next item's first product
       }
     }
   }
@@ -534,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -569,26 +739,31 @@ bool encode_operand(CUtensorMap* map, const void* base, int units, int P, int D)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kColsum, bool kOut = false>
-cudaError_t launch_pass(const TcParams& p, int units, cudaStream_t s) {
-  auto kernel = prefill_tc_kernel<D, kColsum, kOut>;
-  constexpr int kSmem = kOut ? TcShape<D>::kSmemOut : TcShape<D>::kSmem;
+template <int D, int kMode>
+cudaError_t launch_pass(const TcParams& p, cudaStream_t s) {
+  auto kernel = prefill_tc_kernel<D, kMode>;
+  constexpr int kSmem = TcShape<D, kMode>::kSmem;
   static std::mutex mu;
-  static std::vector<int> ready;
+  static std::vector<std::pair<int, int>> ready;  // (device, SM count)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  int sms = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
-    bool found = false;
-    for (int d : ready) found |= d == dev;
-    if (!found) {
+    for (auto& d : ready)
+      if (d.first == dev) sms = d.second;
+    if (sms == 0) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
       if (e != cudaSuccess) return e;
-      ready.push_back(dev);
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      ready.emplace_back(dev, sms);
     }
   }
-  kernel<<<dim3(units, p.tiles), kThreads, kSmem, s>>>(p);
+  const long long items = static_cast<long long>(p.units) * p.tiles;
+  const int grid = items < sms ? static_cast<int>(items) : sms;
+  kernel<<<grid, kThreads, kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -597,28 +772,35 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
   TcParams p;
   if (!encode_operand(&p.tm_a, pp.q, pp.units, pp.P, D) || !encode_operand(&p.tm_b, pp.k, pp.units, pp.P, D))
     return cudaErrorInvalidValue;
+  p.tm_v = p.tm_b;
   p.row_max_in = nullptr;
   p.row_sum_in = nullptr;
   p.row_max = pp.row_max;
   p.row_sum = pp.row_sum;
   p.colsum = pp.colsum;
+  p.out = static_cast<__nv_bfloat16*>(pp.out);
   p.err = pp.err;
+  p.units = pp.units;
   p.P = pp.P;
   p.tiles = (pp.P + kTile - 1) / kTile;
-  p.scale = pp.scale;
+  p.sl = pp.scale * kLog2e;
   p.last_row_only = 0;
-  p.out = static_cast<__nv_bfloat16*>(pp.out);
-  if (pp.out != nullptr && !encode_operand(&p.tm_v, pp.v, pp.units, pp.P, D)) return cudaErrorInvalidValue;
+  cudaError_t e;
   // resident Q, streamed K (and V when the prompt's attention output is wanted)
-  cudaError_t e = pp.out != nullptr ? launch_pass<D, false, true>(p, pp.units, s) : launch_pass<D, false>(p, pp.units, s);
+  if (pp.out != nullptr) {
+    if (!encode_operand(&p.tm_v, pp.v, pp.units, pp.P, D)) return cudaErrorInvalidValue;
+    e = launch_pass<D, kRowOut>(p, s);
+  } else {
+    e = launch_pass<D, kRowStats>(p, s);
+  }
   if (e != cudaSuccess) return e;
   const CUtensorMap q_map = p.tm_a;
-  p.tm_a = p.tm_b;                                         // resident K, streamed Q
+  p.tm_a = p.tm_b;  // resident K, streamed Q
   p.tm_b = q_map;
   p.row_max_in = pp.row_max;
   p.row_sum_in = pp.row_sum;
   p.last_row_only = pp.last_row_only;
-  return launch_pass<D, true>(p, pp.units, s);
+  return launch_pass<D, kColSums>(p, s);
 }
 
 }  // namespace
