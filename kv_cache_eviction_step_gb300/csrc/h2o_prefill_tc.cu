@@ -496,11 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint32_t g = 0;  // logit tiles consumed (over all items)
     int k = 0;
     float* xw = xq + warp * 2 * kCols;  // column sums: this warp's query statistics, [2][kCols]
-    // column sums: b_i = m_i log2(e) + log2(l_i) of a query, so that its weight is 2^(s sl - b_i)
-    auto qstat = [&](int unit, int i) {
-      if (i >= P) return INFINITY;  // queries past the prompt weigh nothing
-      const size_t o = static_cast<size_t>(unit) * P + i;
-      return fmaf(p.row_max_in[o], kLog2e, log2f(p.row_sum_in[o]));
+    // column sums: a query's row statistics, loaded one tile ahead of their use; its weight is
+    // 2^(s sl - b) with b = m log2(e) + log2(l) (queries past the prompt weigh nothing)
+    float qm = 0.f, ql = 0.f;
+    auto qload = [&](int unit, int i) {
+      qm = INFINITY;
+      ql = 1.f;
+      if (i < P) {
+        const size_t o = static_cast<size_t>(unit) * P + i;
+        qm = p.row_max_in[o];
+        ql = p.row_sum_in[o];
+      }
     };
     for (int i = blockIdx.x; i < items; i += gridDim.x, ++k) {
       const Item it = item_of<kMode>(p, i);
@@ -508,15 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const size_t ubase = static_cast<size_t>(it.unit) * P;
       float m2 = -INFINITY, l = 0.f, c = 0.f;  // this warp's partial statistics (log2 units)
       float mu = -INFINITY;  // output pass: the maximum the probabilities are taken against
-      float b_next = 0.f;
-      if constexpr (kCol) b_next = qstat(it.unit, it.t_begin * kTile + h * kCols + lane);
+      if constexpr (kCol) qload(it.unit, it.t_begin * kTile + h * kCols + lane);
       for (int t = 0; t < it.nt; ++t, ++g) {
         const uint32_t a = g & 1u;
         const int x0 = (it.t_begin + t) * kTile + h * kCols;  // key (query) of this warp's column 0
         if constexpr (kCol) {
           // this tile's query statistics for this warp's columns; prefetch the next tile's
-          xw[a * kCols + lane] = b_next;
-          if (t + 1 < it.nt) b_next = qstat(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
+          xw[a * kCols + lane] = fmaf(qm, kLog2e, log2f(ql));
+          if (t + 1 < it.nt) qload(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
           __syncwarp();
         }
         if (ok) ok = mbar_wait(&acc_full[a], (g / 2) & 1u, p.err);

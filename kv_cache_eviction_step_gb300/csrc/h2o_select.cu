@@ -7,7 +7,7 @@
 //   P4  kept tokens' K/V rows fill slots 0.. in ascending position, their scores start at the
 //       column sums, their positions go into the slot map; unused slots are emptied
 //
-// One block of 1024 threads per unit. The candidates' 64-bit keys (column sum made order-
+// One block of 256 threads per unit (several resident per SM). The candidates' 64-bit keys (column sum made order-
 // preserving in the high half, position in the low half) are bitonic-sorted in shared memory, the
 // k_heavy-th key is the keep threshold, a block scan over positions assigns the slots, and the
 // K/V rows are copied with 16-byte accesses spread over the whole block.
@@ -22,7 +22,7 @@
 namespace h2o {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;  // several units per SM: one sorts while another gathers
 constexpr int kMaxPrompt = 16384;
 constexpr int kMaxBudget = 16384;
 
@@ -132,15 +132,33 @@ __global__ void __launch_bounds__(kThreads) prefill_select_kernel(const SelectPa
   uint4* kdst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.k_cache) + ub * p.row_bytes);
   uint4* vdst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.v_cache) + ub * p.row_bytes);
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int e = tid; e < p.budget * vecs; e += kThreads) {
-    const int s = e / vecs, x = e % vecs;
-    if (s < nk) {
-      const size_t src = static_cast<size_t>(pos_of_slot[s]) * vecs + x;
-      kdst[e] = ksrc[src];
-      vdst[e] = vsrc[src];
-    } else {
-      kdst[e] = zero;
-      vdst[e] = zero;
+  // Four 16-byte rows pieces per thread per round, all loads issued before the stores, so each
+  // thread keeps eight reads in flight.
+  constexpr int kBatch = 4;
+  const int total = p.budget * vecs;
+  for (int e0 = tid; e0 < total; e0 += kBatch * kThreads) {
+    uint4 kr[kBatch], vr[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = e0 + b * kThreads;
+      kr[b] = zero;
+      vr[b] = zero;
+      if (e < total) {
+        const int s = e / vecs;
+        if (s < nk) {
+          const size_t src = static_cast<size_t>(pos_of_slot[s]) * vecs + (e - s * vecs);
+          kr[b] = __ldg(ksrc + src);
+          vr[b] = __ldg(vsrc + src);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = e0 + b * kThreads;
+      if (e < total) {
+        kdst[e] = kr[b];
+        vdst[e] = vr[b];
+      }
     }
   }
   for (int s = tid; s < p.budget; s += kThreads) {
