@@ -10,9 +10,9 @@
 //       o_i = sum_{j<=i} exp(s_ij - m_i) / l_i v_j, sharing the logits and exponentials with P1.
 //
 // One persistent kernel shape serves the three passes. A work item is one 128-row "resident" tile of
-// one unit; every CTA (one per SM) walks items blockIdx.x, +gridDim.x, ... and streams, per item,
-// 128-row tiles of the other operand, so that S = A B^T lands in tensor memory with one TMEM lane per
-// resident row:
+// one unit; every CTA (one per SM) walks its items (whole units when there are many, see item_at) and
+// streams, per item, 128-row tiles of the other operand, so that S = A B^T lands in tensor memory
+// with one TMEM lane per resident row:
 //   row stats    resident = Q tile i, streamed = K tiles 0..i   -> rows are queries, reduce along j
 //   column sums  resident = K tile j, streamed = Q tiles j..end -> rows are keys, reduce along i,
 //                recomputing S instead of storing the P x P probabilities.
@@ -82,6 +82,7 @@ struct TcParams {
   int32_t tiles;           // ceil(P / 128)
   float sl;                // log2(e) / sqrt(D)
   int32_t last_row_only;   // column sums: only the last query's weight (Top-K prefill)
+  int32_t unit_items;      // CTAs take whole units (see item_at)
 };
 
 template <int D, int kMode>
@@ -297,26 +298,37 @@ __device__ __forceinline__ void quarter_sync(int q) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "n"(32 * kSplit) : "memory");
 }
 
-// Work item i -> (unit, resident tile). Items are ordered tile-major, heaviest tiles first, so that
-// the static stride over CTAs hands every CTA a similar mix of item sizes.
+// The n-th resident tile a CTA processes. With many units (unit_items) a CTA takes whole units, all
+// their resident tiles in a row, so the tiles streamed for one resident tile are still in L2 for the
+// next; with few units the (unit, resident tile) pairs are spread over the CTAs one by one, ordered
+// tile-major and heaviest first so that the stride hands every CTA a similar mix.
 struct Item {
   int unit, at, t_begin, nt;
 };
 template <int kMode>
-__device__ __forceinline__ Item item_of(const TcParams& p, int i) {
-  Item it;
-  const int k = i / p.units;
-  it.unit = i - k * p.units;
-  if constexpr (kMode == kColSums) {
-    it.at = k;  // query tiles at..end
-    it.t_begin = p.last_row_only ? p.tiles - 1 : it.at;
-    it.nt = p.tiles - it.t_begin;
+__device__ __forceinline__ bool item_at(const TcParams& p, int n, Item* it) {
+  int k;
+  if (p.unit_items) {
+    const int u = blockIdx.x + (n / p.tiles) * gridDim.x;
+    if (u >= p.units) return false;
+    it->unit = u;
+    k = n % p.tiles;
   } else {
-    it.at = p.tiles - 1 - k;  // key tiles 0..at
-    it.t_begin = 0;
-    it.nt = it.at + 1;
+    const int i = blockIdx.x + n * gridDim.x;
+    if (i >= p.units * p.tiles) return false;
+    k = i / p.units;
+    it->unit = i - k * p.units;
   }
-  return it;
+  if constexpr (kMode == kColSums) {
+    it->at = k;  // query tiles at..end
+    it->t_begin = p.last_row_only ? p.tiles - 1 : it->at;
+    it->nt = p.tiles - it->t_begin;
+  } else {
+    it->at = p.tiles - 1 - k;  // key tiles 0..at
+    it->t_begin = 0;
+    it->nt = it->at + 1;
+  }
+  return true;
 }
 
 template <int D, int kMode>
@@ -346,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   float* xq = reinterpret_cast<float*>(head + kCtrlBytes + S::kXBytes);  // column sums: [warps][2][kCols]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int items = p.units * p.tiles;
   const int P = p.P;
 
   if (tid == 0) {
@@ -391,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
       int prev_unit = -1, prev_last = 0;  // output pass: the previous item's last V tile
       int k = 0;
-      for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++k) {
-        const Item it = item_of<kMode>(p, i);
+      Item it;
+      for (; ok && item_at<kMode>(p, k, &it); ++k) {
         const int rb = k & 1;
         if (k >= 2 && !mbar_wait(&res_empty[rb], static_cast<uint32_t>(k / 2 - 1) & 1u, p.err)) break;
         mbar_expect_tx(&res_full[rb], S::kTileBytes);
@@ -445,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         return true;
       };
       int k = 0;
-      for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++k) {
-        const Item it = item_of<kMode>(p, i);
+      Item it;
+      for (; ok && item_at<kMode>(p, k, &it); ++k) {
         const int rb = k & 1;
         if (!mbar_wait(&res_full[rb], static_cast<uint32_t>(k / 2) & 1u, p.err)) break;
         const uint32_t a_base = smem_u32(res + rb * S::kTileBytes);
@@ -508,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         ql = p.row_sum_in[o];
       }
     };
-    for (int i = blockIdx.x; i < items; i += gridDim.x, ++k) {
-      const Item it = item_of<kMode>(p, i);
+    Item it;
+    for (; item_at<kMode>(p, k, &it); ++k) {
       const int row = it.at * kTile + r;
       const size_t ubase = static_cast<size_t>(it.unit) * P;
       float m2 = -INFINITY, l = 0.f, c = 0.f;  // this warp's partial statistics (log2 units)
@@ -766,9 +777,12 @@ cudaError_t launch_pass(const TcParams& p, cudaStream_t s) {
       ready.emplace_back(dev, sms);
     }
   }
-  const long long items = static_cast<long long>(p.units) * p.tiles;
+  // Whole units per CTA once there are at least 8 per SM (so the last round idles few CTAs).
+  TcParams q = p;
+  q.unit_items = p.units >= 8 * sms ? 1 : 0;
+  const long long items = q.unit_items ? p.units : static_cast<long long>(p.units) * p.tiles;
   const int grid = items < sms ? static_cast<int>(items) : sms;
-  kernel<<<grid, kThreads, kSmem, s>>>(p);
+  kernel<<<grid, kThreads, kSmem, s>>>(q);
   return cudaGetLastError();
 }
 
@@ -790,6 +804,7 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
   p.tiles = (pp.P + kTile - 1) / kTile;
   p.sl = pp.scale * kLog2e;
   p.last_row_only = 0;
+  p.unit_items = 0;
   cudaError_t e;
   // resident Q, streamed K (and V when the prompt's attention output is wanted)
   if (pp.out != nullptr) {
