@@ -320,24 +320,43 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
     const bool cache_full = n == p.budget;
     int k = 0;
     bool ok = true;
+    // A unit's new token and state are loaded one unit ahead, so their latency hides behind the
+    // previous unit's epilogue.
+    __nv_bfloat16 nq = __float2bfloat16_rn(0.f), nkn = nq, nvn = nq;
+    float nsc[kMaxTiles];
+    int32_t nsp[kMaxTiles];
+    auto prefetch = [&](int u) {
+      if (u >= p.units) return;
+      const size_t row0 = static_cast<size_t>(u) * p.budget;
+      const size_t ud = static_cast<size_t>(u) * kD + tid;
+      nq = p.q[ud];
+      nkn = p.k_new[ud];
+      nvn = p.v_new[ud];
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int j = t * kTileRows + tid;
+        const bool valid = t < T && j < n;
+        nsc[t] = valid ? p.scores[row0 + j] : 0.f;
+        nsp[t] = valid ? p.slot_pos[row0 + j] : 0;
+      }
+    };
+    prefetch(blockIdx.x);
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
       const int r = k & 1;
       const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
       const size_t row0 = static_cast<size_t>(u) * p.budget;
       const size_t ud = static_cast<size_t>(u) * kD + tid;
-      // This unit's new token and state, loaded now and used after the logits arrive.
-      const float qd = __bfloat162float(p.q[ud]);
-      const __nv_bfloat16 kn = p.k_new[ud];
-      const __nv_bfloat16 vn = p.v_new[ud];
+      const float qd = __bfloat162float(nq);
+      const __nv_bfloat16 kn = nkn;
+      const __nv_bfloat16 vn = nvn;
       float sc[kMaxTiles];
       int32_t sp[kMaxTiles];
 #pragma unroll
       for (int t = 0; t < kMaxTiles; ++t) {
-        const int j = t * kTileRows + tid;
-        const bool valid = t < T && j < n;
-        sc[t] = valid ? p.scores[row0 + j] : 0.f;
-        sp[t] = valid ? p.slot_pos[row0 + j] : 0;
+        sc[t] = nsc[t];
+        sp[t] = nsp[t];
       }
+      prefetch(u + gridDim.x);
       // s_new = q . k_new / sqrt(D) across the 128 epilogue threads.
       float part = qd * __bfloat162float(kn);
 #pragma unroll
