@@ -83,6 +83,16 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.h2o_oracle_run_unit.restype = ctypes.c_int
     lib.h2o_oracle_prefill_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
     lib.h2o_oracle_prefill_attention.restype = ctypes.c_int
+    lib.h2o_oracle_prefill_select_e4m3.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                   vp, vp, vp, vp, vp, vp, vp, f64, f64, vp]
+    lib.h2o_oracle_prefill_select_e4m3.restype = ctypes.c_int
+    lib.h2o_oracle_decode_step_e4m3.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, vp, vp, vp, vp, vp, f64, f64, vp]
+    lib.h2o_oracle_decode_step_e4m3.restype = ctypes.c_int
+    lib.h2o_oracle_e4m3_code.argtypes = [ctypes.c_float]
+    lib.h2o_oracle_e4m3_code.restype = ctypes.c_uint8
+    lib.h2o_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.h2o_oracle_e4m3_value.restype = ctypes.c_double
     return lib
 
 
@@ -123,18 +133,37 @@ def _dtype_code(arr: np.ndarray) -> int:
     raise TypeError(f"oracle inputs must be float32 or uint16 (bf16 bits), got {arr.dtype}")
 
 
-class State:
-    """One H2O cache state on the host: K/V slots, fp32 score table and slot-to-position map."""
+def e4m3_code(f: float, lib_path: str = LIB) -> int:
+    """E4M3 code of a float32 (to nearest, ties to even, saturating at +-448)."""
+    return int(load(lib_path).h2o_oracle_e4m3_code(f))
 
-    def __init__(self, units: int, budget: int, head_dim: int, dtype):
-        self.k_cache = np.zeros((units, budget, head_dim), dtype=dtype)
-        self.v_cache = np.zeros((units, budget, head_dim), dtype=dtype)
+
+def e4m3_value(code: int, lib_path: str = LIB) -> float:
+    return float(load(lib_path).h2o_oracle_e4m3_value(code))
+
+
+class State:
+    """One H2O cache state on the host: K/V slots, fp32 score table and slot-to-position map. With
+    ``e4m3`` the K/V slots hold E4M3 codes (uint8) and ``k_scale``/``v_scale`` one scale per slot."""
+
+    def __init__(self, units: int, budget: int, head_dim: int, dtype, e4m3: bool = False):
+        cdt = np.uint8 if e4m3 else dtype
+        self.k_cache = np.zeros((units, budget, head_dim), dtype=cdt)
+        self.v_cache = np.zeros((units, budget, head_dim), dtype=cdt)
+        self.k_scale = np.zeros((units, budget), dtype=np.float32) if e4m3 else None
+        self.v_scale = np.zeros((units, budget), dtype=np.float32) if e4m3 else None
         self.scores = np.zeros((units, budget), dtype=np.float32)
         self.slot_pos = np.full((units, budget), -1, dtype=np.int32)
+
+    @property
+    def e4m3(self) -> bool:
+        return self.k_scale is not None
 
     def copy(self) -> "State":
         c = State.__new__(State)
         c.k_cache, c.v_cache = self.k_cache.copy(), self.v_cache.copy()
+        c.k_scale = None if self.k_scale is None else self.k_scale.copy()
+        c.v_scale = None if self.v_scale is None else self.v_scale.copy()
         c.scores, c.slot_pos = self.scores.copy(), self.slot_pos.copy()
         return c
 
@@ -151,8 +180,8 @@ class Oracle:
     def _pol(self):
         return None if self.policy is None else ctypes.cast(ctypes.pointer(self.policy), ctypes.c_void_p)
 
-    def new_state(self, units: int, head_dim: int, dtype) -> State:
-        return State(units, self.budget, head_dim, dtype)
+    def new_state(self, units: int, head_dim: int, dtype, e4m3: bool = False) -> State:
+        return State(units, self.budget, head_dim, dtype, e4m3)
 
     def prefill_select(self, q, k, v, state: State, prefer_pos=None, tie_rel=TIE_REL,
                        err_rel=TIE_REL, want_colsum=False):
@@ -162,11 +191,20 @@ class Oracle:
         colsum = np.empty((units, P), dtype=np.float64) if want_colsum else None
         infos = (PrefillInfo * max(units, 1))()
         pref = None if prefer_pos is None else np.ascontiguousarray(prefer_pos, dtype=np.int32)
-        rc = self.lib.h2o_oracle_prefill_select_policy(
-            units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), P,
-            _ptr(q), _ptr(k), _ptr(v), _ptr(state.k_cache), _ptr(state.v_cache),
-            _ptr(state.scores), _ptr(state.slot_pos), _ptr(colsum), self._pol(), _ptr(pref),
-            tie_rel, err_rel, ctypes.cast(infos, ctypes.c_void_p))
+        if state.e4m3:
+            if _dtype_code(q) != BF16:
+                raise TypeError("the E4M3 cache takes bf16 inputs")
+            rc = self.lib.h2o_oracle_prefill_select_e4m3(
+                units, D, self.budget, self.k_heavy, self.k_local, P, _ptr(q), _ptr(k), _ptr(v),
+                _ptr(state.k_cache), _ptr(state.v_cache), _ptr(state.k_scale), _ptr(state.v_scale),
+                _ptr(state.scores), _ptr(state.slot_pos), _ptr(colsum), self._pol(), _ptr(pref),
+                tie_rel, err_rel, ctypes.cast(infos, ctypes.c_void_p))
+        else:
+            rc = self.lib.h2o_oracle_prefill_select_policy(
+                units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), P,
+                _ptr(q), _ptr(k), _ptr(v), _ptr(state.k_cache), _ptr(state.v_cache),
+                _ptr(state.scores), _ptr(state.slot_pos), _ptr(colsum), self._pol(), _ptr(pref),
+                tie_rel, err_rel, ctypes.cast(infos, ctypes.c_void_p))
         if rc != 0:
             raise ValueError(f"h2o_oracle_prefill_select rejected its arguments (code {rc})")
         return colsum, infos[:units]
@@ -183,12 +221,22 @@ class Oracle:
         probs = np.full((units, self.budget + 1), np.nan) if want_probs else None
         infos = (StepInfo * max(units, 1))()
         pref = None if prefer_victim is None else np.ascontiguousarray(prefer_victim, dtype=np.int32)
-        rc = self.lib.h2o_oracle_decode_step_policy(
-            units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), t,
-            _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(state.k_cache), _ptr(state.v_cache),
-            _ptr(state.scores), _ptr(state.slot_pos), _ptr(out), _ptr(probs), _ptr(ev_slot),
-            _ptr(ev_pos), self._pol(), _ptr(pref), tie_rel, err_rel,
-            ctypes.cast(infos, ctypes.c_void_p))
+        if state.e4m3:
+            if _dtype_code(q) != BF16:
+                raise TypeError("the E4M3 cache takes bf16 inputs")
+            rc = self.lib.h2o_oracle_decode_step_e4m3(
+                units, D, self.budget, self.k_heavy, self.k_local, t, _ptr(q), _ptr(k_new),
+                _ptr(v_new), _ptr(state.k_cache), _ptr(state.v_cache), _ptr(state.k_scale),
+                _ptr(state.v_scale), _ptr(state.scores), _ptr(state.slot_pos), _ptr(out),
+                _ptr(probs), _ptr(ev_slot), _ptr(ev_pos), self._pol(), _ptr(pref), tie_rel,
+                err_rel, ctypes.cast(infos, ctypes.c_void_p))
+        else:
+            rc = self.lib.h2o_oracle_decode_step_policy(
+                units, D, self.budget, self.k_heavy, self.k_local, _dtype_code(q), t,
+                _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(state.k_cache), _ptr(state.v_cache),
+                _ptr(state.scores), _ptr(state.slot_pos), _ptr(out), _ptr(probs), _ptr(ev_slot),
+                _ptr(ev_pos), self._pol(), _ptr(pref), tie_rel, err_rel,
+                ctypes.cast(infos, ctypes.c_void_p))
         if rc != 0:
             raise ValueError(f"h2o_oracle_decode_step rejected its arguments (code {rc})")
         return out, ev_slot, ev_pos, probs, infos[:units]

@@ -66,6 +66,92 @@ static double dot(const double* q, const void* rows, int32_t dtype, size_t row, 
   return acc;
 }
 
+/* ---- FP8 E4M3 cache rows -------------------------------------------------------------------
+ * The OCP 8-bit floating-point format E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * no infinities; exponent 15 with mantissa 7 is NaN; the largest finite magnitude is 448. A cached
+ * row of the quantised cache is D such codes and one float32 scale: scale = amax / 448 (amax = the
+ * largest magnitude in the row; an all-zero row gets scale 1), code_d = E4M3(x_d / scale), each
+ * float32 operation rounded once, the conversion to nearest with ties to even and saturating at
+ * +-448. The cached value is scale * value(code). */
+
+static double e4m3_value(uint8_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);        /* subnormal: (m / 8) x 2^-6 */
+  else v = ldexp(8.0 + m, e - 10);              /* (1 + m / 8) x 2^(e - 7) */
+  return (b & 0x80) ? -v : v;
+}
+
+static uint8_t e4m3_code(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  const double a = fabs((double)f);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);                                /* a in [2^(e2-1), 2^e2) */
+  int binade = e2 - 1;
+  if (binade < -6) binade = -6;                 /* the subnormal spacing continues below 2^-6 */
+  const double quantum = ldexp(1.0, binade - 3);
+  double r = nearbyint(a / quantum) * quantum;  /* to nearest, ties to even */
+  if (r > 448.0) r = 448.0;                     /* saturate */
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+  frexp(r, &e2);
+  const int e = e2 - 1;                         /* r in [2^e, 2^(e+1)) */
+  const int m = (int)(r / ldexp(1.0, e - 3)) - 8;
+  return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)m);
+}
+
+uint8_t h2o_oracle_e4m3_code(float f) { return e4m3_code(f); }
+double h2o_oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+
+/* One row of the quantised cache from D input values (float32 or bf16). Returns the scale. */
+static float e4m3_quantise_row(const void* src, int32_t dtype, size_t row, int32_t D, uint8_t* codes) {
+  float amax = 0.0f;
+  for (int32_t d = 0; d < D; ++d) {
+    const float x = fabsf((float)elem(src, dtype, row * (size_t)D + (size_t)d));
+    if (x > amax) amax = x;
+  }
+  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int32_t d = 0; d < D; ++d)
+    codes[d] = e4m3_code((float)elem(src, dtype, row * (size_t)D + (size_t)d) / scale);
+  return scale;
+}
+
+/* The cache of one unit: rows stored as the input dtype, or as E4M3 codes with per-row scales. */
+typedef struct {
+  int32_t fmt;       /* H2O_ORACLE_F32, H2O_ORACLE_BF16 or H2O_ORACLE_E4M3 */
+  char* rows;        /* [budget][D] elements of fmt */
+  float* scales;     /* E4M3: [budget] */
+  int32_t D;
+} cache_rows;
+
+static size_t cache_row_bytes(int32_t fmt, int32_t D) {
+  return (size_t)D * (fmt == H2O_ORACLE_E4M3 ? 1 : elem_bytes(fmt));
+}
+
+static double cached(const cache_rows* c, size_t j, int32_t d) {
+  if (c->fmt == H2O_ORACLE_E4M3)
+    return (double)c->scales[j] * e4m3_value((uint8_t)c->rows[j * (size_t)c->D + (size_t)d]);
+  return elem(c->rows, c->fmt, j * (size_t)c->D + (size_t)d);
+}
+
+/* Write input row `src_row` of `src` (dtype) into cache slot j. */
+static void store_row(cache_rows* c, size_t j, const void* src, int32_t dtype, size_t src_row) {
+  if (c->fmt == H2O_ORACLE_E4M3) {
+    c->scales[j] = e4m3_quantise_row(src, dtype, src_row, c->D, (uint8_t*)c->rows + j * (size_t)c->D);
+    return;
+  }
+  const size_t row = cache_row_bytes(c->fmt, c->D);
+  memcpy(c->rows + j * row, (const char*)src + src_row * row, row);
+}
+
+static void clear_row(cache_rows* c, size_t j) {
+  memset(c->rows + j * cache_row_bytes(c->fmt, c->D), 0, cache_row_bytes(c->fmt, c->D));
+  if (c->fmt == H2O_ORACLE_E4M3) c->scales[j] = 0.0f;
+}
+
 static int check_dims(int32_t units, int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local,
                       int32_t dtype) {
   if (units < 0 || D < 1 || budget < 1 || k_heavy < 0 || k_local < 0) return -1;
@@ -194,12 +280,12 @@ int h2o_oracle_prefill_select(int32_t units, int32_t D, int32_t budget, int32_t 
                                           prefer_pos, tie_rel, err_rel, infos);
 }
 
-int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
-                                     int32_t k_local, int32_t dtype, int32_t P, const void* q,
-                                     const void* k, const void* v, void* k_cache, void* v_cache,
-                                     float* scores, int32_t* slot_pos, double* colsum,
-                                     const h2o_oracle_policy* policy, const int32_t* prefer_pos,
-                                     double tie_rel, double err_rel, h2o_oracle_prefill_info* infos) {
+static int prefill_select(int32_t units, int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local,
+                          int32_t dtype, int32_t cache_fmt, int32_t P, const void* q, const void* k,
+                          const void* v, void* k_cache, void* v_cache, float* k_scale,
+                          float* v_scale, float* scores, int32_t* slot_pos, double* colsum,
+                          const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                          double tie_rel, double err_rel, h2o_oracle_prefill_info* infos) {
   const h2o_oracle_policy h2o_rule = {H2O_ORACLE_POLICY_H2O, 0, 0};
   const h2o_oracle_policy* pol = policy ? policy : &h2o_rule;
   int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
@@ -227,8 +313,11 @@ int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, i
     const char* qu = (const char*)q + (size_t)u * P * row;
     const char* ku = (const char*)k + (size_t)u * P * row;
     const char* vu = (const char*)v + (size_t)u * P * row;
-    char* kc = (char*)k_cache + (size_t)u * budget * row;
-    char* vc = (char*)v_cache + (size_t)u * budget * row;
+    const size_t crow = cache_row_bytes(cache_fmt, D);
+    cache_rows kc = {cache_fmt, (char*)k_cache + (size_t)u * budget * crow,
+                     k_scale ? k_scale + (size_t)u * budget : NULL, D};
+    cache_rows vc = {cache_fmt, (char*)v_cache + (size_t)u * budget * crow,
+                     v_scale ? v_scale + (size_t)u * budget : NULL, D};
     float* sc = scores + (size_t)u * budget;
     int32_t* sp = slot_pos + (size_t)u * budget;
     h2o_oracle_prefill_info info = {H2O_ORACLE_NO_EVICTION, 0, INFINITY};
@@ -290,16 +379,16 @@ int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, i
     int32_t slot = 0;
     for (int32_t p = 0; p < P; ++p) {
       if (!keep[p]) continue;
-      memcpy(kc + (size_t)slot * row, ku + (size_t)p * row, row);
-      memcpy(vc + (size_t)slot * row, vu + (size_t)p * row, row);
+      store_row(&kc, (size_t)slot, ku, dtype, (size_t)p);
+      store_row(&vc, (size_t)slot, vu, dtype, (size_t)p);
       sc[slot] = (float)start[p];
       sp[slot] = p;
       ++slot;
     }
     info.kept = slot;
     for (; slot < budget; ++slot) {
-      memset(kc + (size_t)slot * row, 0, row);
-      memset(vc + (size_t)slot * row, 0, row);
+      clear_row(&kc, (size_t)slot);
+      clear_row(&vc, (size_t)slot);
       sc[slot] = 0.0f;
       sp[slot] = -1;
     }
@@ -307,6 +396,30 @@ int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, i
   }
   free(c); free(a); free(s); free(qrow); free(cand); free(keep); free(keep_pref);
   return 0;
+}
+
+int h2o_oracle_prefill_select_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                     int32_t k_local, int32_t dtype, int32_t P, const void* q,
+                                     const void* k, const void* v, void* k_cache, void* v_cache,
+                                     float* scores, int32_t* slot_pos, double* colsum,
+                                     const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                                     double tie_rel, double err_rel, h2o_oracle_prefill_info* infos) {
+  return prefill_select(units, D, budget, k_heavy, k_local, dtype, dtype, P, q, k, v, k_cache, v_cache,
+                        NULL, NULL, scores, slot_pos, colsum, policy, prefer_pos, tie_rel, err_rel,
+                        infos);
+}
+
+int h2o_oracle_prefill_select_e4m3(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                   int32_t k_local, int32_t P, const void* q, const void* k,
+                                   const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                                   float* k_scale, float* v_scale, float* scores,
+                                   int32_t* slot_pos, double* colsum,
+                                   const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                                   double tie_rel, double err_rel, h2o_oracle_prefill_info* infos) {
+  if (!k_scale || !v_scale) return -8;
+  return prefill_select(units, D, budget, k_heavy, k_local, H2O_ORACLE_BF16, H2O_ORACLE_E4M3, P, q, k, v,
+                        k_cache, v_cache, k_scale, v_scale, scores, slot_pos, colsum, policy,
+                        prefer_pos, tie_rel, err_rel, infos);
 }
 
 /* ---- decode: attend, accumulate, evict, overwrite in place --------------------------------- */
@@ -323,13 +436,13 @@ int h2o_oracle_decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_h
                                        evicted_pos, NULL, prefer_victim, tie_rel, err_rel, infos);
 }
 
-int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
-                                  int32_t k_local, int32_t dtype, int32_t t, const void* q,
-                                  const void* k_new, const void* v_new, void* k_cache,
-                                  void* v_cache, float* scores, int32_t* slot_pos, double* out,
-                                  double* probs, int32_t* evicted_slot, int32_t* evicted_pos,
-                                  const h2o_oracle_policy* policy, const int32_t* prefer_victim,
-                                  double tie_rel, double err_rel, h2o_oracle_step_info* infos) {
+static int decode_step(int32_t units, int32_t D, int32_t budget, int32_t k_heavy, int32_t k_local,
+                       int32_t dtype, int32_t cache_fmt, int32_t t, const void* q, const void* k_new,
+                       const void* v_new, void* k_cache, void* v_cache, float* k_scale,
+                       float* v_scale, float* scores, int32_t* slot_pos, double* out, double* probs,
+                       int32_t* evicted_slot, int32_t* evicted_pos, const h2o_oracle_policy* policy,
+                       const int32_t* prefer_victim, double tie_rel, double err_rel,
+                       h2o_oracle_step_info* infos) {
   const h2o_oracle_policy h2o_rule = {H2O_ORACLE_POLICY_H2O, 0, 0};
   const h2o_oracle_policy* pol = policy ? policy : &h2o_rule;
   int rc = check_dims(units, D, budget, k_heavy, k_local, dtype);
@@ -338,8 +451,7 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
   rc = check_policy(pol, budget);
   if (rc) return rc;
   const int32_t n = t < budget ? t : budget;   /* valid cached slots before this step */
-  const size_t eb = elem_bytes(dtype);
-  const size_t row = (size_t)D * eb;
+  const size_t crow = cache_row_bytes(cache_fmt, D);
   const double scale = 1.0 / sqrt((double)D);
 
   /* Every unit's slot map must hold exactly n valid, distinct-looking entries. */
@@ -358,15 +470,19 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
 
   for (int32_t u = 0; u < units; ++u) {
     const size_t ub = (size_t)u * budget;
-    char* kc = (char*)k_cache + ub * row;
-    char* vc = (char*)v_cache + ub * row;
+    cache_rows kc = {cache_fmt, (char*)k_cache + ub * crow, k_scale ? k_scale + ub : NULL, D};
+    cache_rows vc = {cache_fmt, (char*)v_cache + ub * crow, v_scale ? v_scale + ub : NULL, D};
     float* sc = scores + ub;
     int32_t* sp = slot_pos + ub;
     h2o_oracle_step_info info = {H2O_ORACLE_NO_EVICTION, -1, -1, -1, -1, 0, INFINITY};
 
     /* Logits over the n cached slots and the new token (index n): [post] §2.1.1. */
     for (int32_t d = 0; d < D; ++d) qv[d] = elem(q, dtype, (size_t)u * D + d);
-    for (int32_t j = 0; j < n; ++j) s[j] = dot(qv, kc, dtype, (size_t)j, D) * scale;
+    for (int32_t j = 0; j < n; ++j) {
+      double acc = 0.0;
+      for (int32_t d = 0; d < D; ++d) acc += qv[d] * cached(&kc, (size_t)j, d);
+      s[j] = acc * scale;
+    }
     s[n] = dot(qv, k_new, dtype, (size_t)u, D) * scale;
 
     double m = -INFINITY;
@@ -379,7 +495,7 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
     /* Output o = sum_j p_j v_j over the same n + 1 keys. */
     for (int32_t d = 0; d < D; ++d) {
       double acc = 0.0;
-      for (int32_t j = 0; j < n; ++j) acc += p[j] * elem(vc, dtype, (size_t)j * D + d);
+      for (int32_t j = 0; j < n; ++j) acc += p[j] * cached(&vc, (size_t)j, d);
       acc += p[n] * elem(v_new, dtype, (size_t)u * D + d);
       out[(size_t)u * D + d] = acc;
     }
@@ -446,8 +562,8 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
 
     /* In-place overwrite, no compaction ([post] §2.3): the new token takes the slot, starting
      * from its own attention weight as score. */
-    memcpy(kc + (size_t)target * row, (const char*)k_new + (size_t)u * row, row);
-    memcpy(vc + (size_t)target * row, (const char*)v_new + (size_t)u * row, row);
+    store_row(&kc, (size_t)target, k_new, dtype, (size_t)u);
+    store_row(&vc, (size_t)target, v_new, dtype, (size_t)u);
     sc[target] = (float)p[n];
     sp[target] = t;
     info.written_slot = target;
@@ -458,6 +574,32 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
   }
   free(qv); free(s); free(p);
   return 0;
+}
+
+int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                  int32_t k_local, int32_t dtype, int32_t t, const void* q,
+                                  const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, float* scores, int32_t* slot_pos, double* out,
+                                  double* probs, int32_t* evicted_slot, int32_t* evicted_pos,
+                                  const h2o_oracle_policy* policy, const int32_t* prefer_victim,
+                                  double tie_rel, double err_rel, h2o_oracle_step_info* infos) {
+  return decode_step(units, D, budget, k_heavy, k_local, dtype, dtype, t, q, k_new, v_new, k_cache,
+                     v_cache, NULL, NULL, scores, slot_pos, out, probs, evicted_slot, evicted_pos,
+                     policy, prefer_victim, tie_rel, err_rel, infos);
+}
+
+int h2o_oracle_decode_step_e4m3(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                int32_t k_local, int32_t t, const void* q, const void* k_new,
+                                const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                                float* k_scale, float* v_scale, float* scores, int32_t* slot_pos,
+                                double* out, double* probs, int32_t* evicted_slot,
+                                int32_t* evicted_pos, const h2o_oracle_policy* policy,
+                                const int32_t* prefer_victim, double tie_rel, double err_rel,
+                                h2o_oracle_step_info* infos) {
+  if (!k_scale || !v_scale) return -8;
+  return decode_step(units, D, budget, k_heavy, k_local, H2O_ORACLE_BF16, H2O_ORACLE_E4M3, t, q, k_new,
+                     v_new, k_cache, v_cache, k_scale, v_scale, scores, slot_pos, out, probs,
+                     evicted_slot, evicted_pos, policy, prefer_victim, tie_rel, err_rel, infos);
 }
 
 /* Causal attention output of the prompt ([post] §2.1.1: the weights are Softmax(QK^T / sqrt(d)) over

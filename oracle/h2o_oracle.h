@@ -18,7 +18,7 @@
 extern "C" {
 #endif
 
-enum { H2O_ORACLE_F32 = 0, H2O_ORACLE_BF16 = 1 };
+enum { H2O_ORACLE_F32 = 0, H2O_ORACLE_BF16 = 1, H2O_ORACLE_E4M3 = 2 /* cache rows only */ };
 
 /* How one unit's eviction decision was reached (decode) or its kept set chosen (prefill). */
 enum {
@@ -119,6 +119,33 @@ int h2o_oracle_decode_step_policy(int32_t units, int32_t D, int32_t budget, int3
                                   double* probs, int32_t* evicted_slot, int32_t* evicted_pos,
                                   const h2o_oracle_policy* policy, const int32_t* prefer_victim,
                                   double tie_rel, double err_rel, h2o_oracle_step_info* infos);
+
+/*
+ * The same two operations with a quantised cache: q, k, v, k_new, v_new in bf16, cached rows as
+ * FP8 E4M3 codes (k_cache, v_cache: [units, budget, D] bytes) with one float32 scale per row
+ * (k_scale, v_scale: [units, budget]); see h2o_oracle.c for the quantisation. Attention reads the
+ * cached rows as scale x value(code); the new token attends with its bf16 values and is stored
+ * quantised. Everything else as the policy forms above. Returns -8 without scale arrays.
+ */
+int h2o_oracle_prefill_select_e4m3(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                   int32_t k_local, int32_t P, const void* q, const void* k,
+                                   const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                                   float* k_scale, float* v_scale, float* scores,
+                                   int32_t* slot_pos, double* colsum,
+                                   const h2o_oracle_policy* policy, const int32_t* prefer_pos,
+                                   double tie_rel, double err_rel, h2o_oracle_prefill_info* infos);
+int h2o_oracle_decode_step_e4m3(int32_t units, int32_t D, int32_t budget, int32_t k_heavy,
+                                int32_t k_local, int32_t t, const void* q, const void* k_new,
+                                const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                                float* k_scale, float* v_scale, float* scores, int32_t* slot_pos,
+                                double* out, double* probs, int32_t* evicted_slot,
+                                int32_t* evicted_pos, const h2o_oracle_policy* policy,
+                                const int32_t* prefer_victim, double tie_rel, double err_rel,
+                                h2o_oracle_step_info* infos);
+/* E4M3 code of a float32 (to nearest, ties to even, saturating) and the value of a code; exported
+ * for the format pins. */
+uint8_t h2o_oracle_e4m3_code(float f);
+double h2o_oracle_e4m3_value(uint8_t code);
 
 /*
  * Prompt pass of the attention layer: out[u][i] = sum over j <= i of softmax_j(q_i . k_j / sqrt(D))

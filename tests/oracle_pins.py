@@ -487,10 +487,130 @@ def pin_prefill_attention_weights_are_the_column_sum_weights(lib):
         _close(out[P - 1], o[0], 1e-12, 1e-13, "last prompt row vs decode step")
 
 
+# ---- the E4M3 (FP8) cache --------------------------------------------------------------------
+
+def _e4m3_table(lib):
+    """Values of all 256 E4M3 codes as the oracle decodes them."""
+    return np.array([oracle.e4m3_value(c, lib) for c in range(256)])
+
+
+def _nearest_code(x: float, table) -> int:
+    """Brute force: the finite code nearest to x, ties to the even mantissa, saturating at 448."""
+    x = float(np.float32(x))
+    x = max(-448.0, min(448.0, x))
+    best = None
+    for c in range(256):
+        v = table[c]
+        if np.isnan(v) or (v == 0.0 and c == 0x80):  # NaNs; -0 (x == 0 maps to the signed zero)
+            continue
+        d = abs(v - x)
+        if best is None or d < best[0] or (d == best[0] and (c & 1) == 0 and (best[1] & 1) == 1):
+            best = (d, c)
+    c = best[1]
+    if c == 0 and np.signbit(x):
+        c = 0x80
+    return c
+
+
+def pin_e4m3_format(lib):
+    """The E4M3 format (OCP 8-bit floating point): its stated limit values, NaN, and every
+    conversion = the nearest finite code found by brute force, ties to the even mantissa,
+    saturating at +-448."""
+    t = _e4m3_table(lib)
+    fixed = {0x7E: 448.0, 0x08: 2.0 ** -6, 0x07: 0.875 * 2.0 ** -6, 0x01: 2.0 ** -9, 0x38: 1.0,
+             0x3F: 1.875, 0x40: 2.0, 0xB8: -1.0, 0xFE: -448.0, 0x00: 0.0}
+    for c, v in fixed.items():
+        assert t[c] == v, (hex(c), t[c], v)
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    finite = [c for c in range(256) if not np.isnan(t[c])]
+    for c in finite:  # every finite code round-trips
+        assert oracle.e4m3_code(float(t[c]), lib) == c or t[c] == 0.0, hex(c)
+    pos = [t[c] for c in range(0x7F)]
+    assert all(a < b for a, b in zip(pos, pos[1:])), "codes 0..0x7E are increasing"
+    # ties: 1.0625 lies between 1.0 (mantissa 0) and 1.125 (1): to 1.0; 1.1875 -> 1.25 (mantissa 2)
+    assert oracle.e4m3_code(1.0625, lib) == 0x38 and oracle.e4m3_code(1.1875, lib) == 0x3A
+    assert oracle.e4m3_code(464.0, lib) == 0x7E and oracle.e4m3_code(-1e9, lib) == 0xFE
+    rng = np.random.default_rng(44)
+    xs = np.concatenate([rng.standard_normal(300) * 10.0 ** rng.uniform(-4, 3, 300),
+                         [t[c] + (t[c + 1] - t[c]) / 2 for c in range(0x7E)]])  # every midpoint
+    for x in xs:
+        want = _nearest_code(x, t)
+        got = oracle.e4m3_code(float(x), lib)
+        assert got == want or (t[got] == t[want]), (x, hex(got), hex(want))
+
+
+def _quantise_row_bruteforce(x_bf16: np.ndarray, table):
+    x = bf.widen(x_bf16).astype(np.float32)
+    amax = np.float32(np.max(np.abs(x)))
+    scale = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+    codes = np.array([_nearest_code(float(np.float32(xi / scale)), table) for xi in x], dtype=np.uint8)
+    return codes, scale
+
+
+def pin_e4m3_cache_rows(lib):
+    """Every row the quantised cache holds after prefill and after each decode step is the row's
+    bf16 values quantised by brute force (scale = amax / 448 in float32, nearest codes), and the
+    outputs under a full budget are dense attention over the dequantised prompt rows plus the new
+    token's bf16 values."""
+    t = _e4m3_table(lib)
+    rng = np.random.default_rng(45)
+    for _ in range(6):
+        D = int(rng.choice([4, 8, 16]))
+        P, S = int(rng.integers(1, 7)), int(rng.integers(1, 6))
+        budget = P + S + 1
+        q, k, v = tj.random_sequence(rng, P + S, D, "bf16", hh=2)
+        k[0] = 0  # an all-zero row: scale 1, zero codes
+        tr = tj.run(lib, q, k, v, P, S, budget, budget // 2, budget - budget // 2, e4m3=True)
+        Q, K, V = bf.widen(q), bf.widen(k), bf.widen(v)
+        deq_k, deq_v = K.copy(), V.copy()
+        for rec in tr.steps:
+            for j, pos in enumerate(rec.slot_pos_after):
+                if pos < 0:
+                    continue
+                ck, sk = _quantise_row_bruteforce(k[pos], t)
+                cv, sv = _quantise_row_bruteforce(v[pos], t)
+                assert np.array_equal(rec.k_after[j], ck) and rec.k_scale_after[j] == sk, (pos, j)
+                assert np.array_equal(rec.v_after[j], cv) and rec.v_scale_after[j] == sv, (pos, j)
+                deq_k[pos] = sk * t[ck]
+                deq_v[pos] = sv * t[cv]
+            # dense attention: cached (dequantised) rows 0..t-1, the new token's own bf16 row
+            keys = np.concatenate([deq_k[: rec.t], K[rec.t: rec.t + 1]])
+            vals = np.concatenate([deq_v[: rec.t], V[rec.t: rec.t + 1]])
+            _close(rec.out, bf.attention(Q[rec.t], keys, vals)[0], 1e-12, 1e-13,
+                   f"E4M3 full-budget output at t={rec.t}")
+
+
+def pin_e4m3_exact_rows_reduce_to_bf16(lib):
+    """K/V rows whose values are E4M3 values with magnitude maximum 448 are stored exactly (scale 1),
+    so the quantised cache must then make every decision and output of the bf16 cache."""
+    t = _e4m3_table(lib)
+    finite = np.array([t[c] for c in range(256) if not np.isnan(t[c]) and abs(t[c]) <= 448.0])
+    rng = np.random.default_rng(46)
+    for _ in range(8):
+        D = int(rng.choice([4, 8]))
+        P, S = int(rng.integers(3, 12)), int(rng.integers(4, 12))
+        budget = int(rng.integers(2, 6))
+        kl = int(rng.integers(0, budget + 1))
+        q, _, _ = tj.random_sequence(rng, P + S, D, "bf16", hh=2)
+        rows = rng.choice(finite, size=(2, P + S, D))
+        rows[:, :, 0] = 448.0 * rng.choice([-1.0, 1.0], size=(2, P + S))  # amax 448: scale 1
+        k, v = (synth.to_bf16_bits(r.astype(np.float32)) for r in rows)
+        assert np.array_equal(bf.widen(k), rows[0]), "E4M3 values are exact in bf16"
+        plain = tj.run(lib, q, k, v, P, S, budget, budget - kl, kl)
+        quant = tj.run(lib, q, k, v, P, S, budget, budget - kl, kl, e4m3=True)
+        assert np.array_equal(plain.prefill_state.slot_pos, quant.prefill_state.slot_pos)
+        for a, b in zip(plain.steps, quant.steps):
+            assert (a.evicted_slot, a.evicted_pos) == (b.evicted_slot, b.evicted_pos)
+            assert np.array_equal(a.scores_after, b.scores_after)
+            _close(b.out, a.out, 1e-13, 1e-13, "E4M3 exact rows vs bf16")
+            assert np.all(b.k_scale_after[b.slot_pos_after >= 0] == 1.0)
+
+
 PINS = [pin_full_budget_is_dense, pin_no_heavy_is_sliding_window,
         pin_victim_is_argmin_of_recomputed_scores, pin_uniform_attention_closed_form,
         pin_mass_and_slot_invariants, pin_small_local_is_unprotected_argmin,
         pin_hand_built_ties_and_protection, pin_prefill_equal_sums_keep_later, pin_prompt_fits_budget, pin_bf16_is_exact_widening,
         pin_near_tie_adoption, pin_local_policy_is_the_window, pin_sink_window_keeps_sinks_and_recent,
         pin_strided_keeps_its_grid, pin_topk_ranks_by_current_attention,
-        pin_prefill_attention_closed_forms, pin_prefill_attention_weights_are_the_column_sum_weights]
+        pin_prefill_attention_closed_forms, pin_prefill_attention_weights_are_the_column_sum_weights,
+        pin_e4m3_format, pin_e4m3_cache_rows, pin_e4m3_exact_rows_reduce_to_bf16]

@@ -58,8 +58,15 @@ MUTANTS = {
     "attention_skips_diagonal": ("for (int32_t j = 0; j <= i; ++j) acc += w[j] / l",
                                  "for (int32_t j = 0; j < i; ++j) acc += w[j] / l"),
     "attention_values_from_keys": ("acc += w[j] / l * elem(vu, dtype", "acc += w[j] / l * elem(ku, dtype"),
-    "new_value_row_from_key": ("memcpy(vc + (size_t)target * row, (const char*)v_new",
-                               "memcpy(vc + (size_t)target * row, (const char*)k_new"),
+    "e4m3_ties_away_from_zero": ("double r = nearbyint(a / quantum) * quantum;",
+                                 "double r = round(a / quantum) * quantum;"),
+    "e4m3_no_saturation": ("  if (r > 448.0) r = 448.0;                     /* saturate */\n", "\n"),
+    "e4m3_subnormal_spacing": ("if (binade < -6) binade = -6;", "if (binade < -7) binade = -7;"),
+    "e4m3_scale_127": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 127.0f : 1.0f"),
+    "e4m3_read_ignores_scale": ("return (double)c->scales[j] * e4m3_value(", "return 1.0 * e4m3_value("),
+    "e4m3_exponent_bias": ("v = ldexp(8.0 + m, e - 10);", "v = ldexp(8.0 + m, e - 11);"),
+    "new_value_row_from_key": ("store_row(&vc, (size_t)target, v_new, dtype, (size_t)u);",
+                               "store_row(&vc, (size_t)target, k_new, dtype, (size_t)u);"),
 }
 
 

@@ -55,11 +55,12 @@ def random_sequence(rng: np.random.Generator, length: int, D: int, dtype: str,
 
 
 def run(lib_path: str, q_seq, k_seq, v_seq, P: int, S: int, budget: int, k_heavy: int,
-        k_local: int, prefer=None, policy=None) -> Trajectory:
-    """One unit: prefill on positions 0..P-1, then decode positions P..P+S-1."""
+        k_local: int, prefer=None, policy=None, e4m3: bool = False) -> Trajectory:
+    """One unit: prefill on positions 0..P-1, then decode positions P..P+S-1 (``e4m3``: with the
+    quantised cache; the records then hold the codes, and the scales are in ``k_scale_after``)."""
     D = q_seq.shape[1]
     orc = oracle.Oracle(budget, k_heavy, k_local, lib_path=lib_path, policy=policy)
-    st = orc.new_state(1, D, q_seq.dtype)
+    st = orc.new_state(1, D, q_seq.dtype, e4m3=e4m3)
     colsum, pinfo = orc.prefill_select(q_seq[None, :P], k_seq[None, :P], v_seq[None, :P], st,
                                        want_colsum=True)
     pre = st.copy()
@@ -71,7 +72,10 @@ def run(lib_path: str, q_seq, k_seq, v_seq, P: int, S: int, budget: int, k_heavy
             t, q_seq[None, t], k_seq[None, t], v_seq[None, t], st, want_probs=True,
             prefer_victim=None if prefer is None else np.array([prefer(s)], dtype=np.int32))
         n = min(t, budget)
-        steps.append(StepRecord(t, out[0], probs[0, : n + 1].copy(), int(es[0]), int(ep[0]),
-                                infos[0], sp0, sc0, st.slot_pos[0].copy(), st.scores[0].copy(),
-                                st.k_cache[0].copy(), st.v_cache[0].copy()))
+        rec = StepRecord(t, out[0], probs[0, : n + 1].copy(), int(es[0]), int(ep[0]),
+                         infos[0], sp0, sc0, st.slot_pos[0].copy(), st.scores[0].copy(),
+                         st.k_cache[0].copy(), st.v_cache[0].copy())
+        if e4m3:
+            rec.k_scale_after, rec.v_scale_after = st.k_scale[0].copy(), st.v_scale[0].copy()
+        steps.append(rec)
     return Trajectory(colsum[0], pinfo[0], pre, steps)
