@@ -48,6 +48,38 @@ def decode_bytes_per_unit(n: int, head_dim: int, elem_bytes: int) -> int:
     return n * (2 * head_dim * elem_bytes + 12) + 6 * head_dim * elem_bytes + 16
 
 
+def decode_bytes_per_unit_e4m3(n: int, head_dim: int) -> int:
+    """The same for the E4M3 cache: K and V codes (2 n D), row scales read (8 n), score read + write
+    and position read (12 n); bf16 q/k_new/v_new read and the output written (8 D); the victim's
+    codes (2 D) and scales (8); written score, position and the two eviction indices (16)."""
+    return n * (2 * head_dim + 20) + 10 * head_dim + 24
+
+
+class Calls:
+    """The library calls of one job, for the bf16 or the E4M3 cache."""
+
+    def __init__(self, h2o, dims, cache, e4m3: bool):
+        self.h2o, self.dims, self.cache, self.e4m3 = h2o, dims, cache, e4m3
+
+    def prefill(self, P, q, k, v, stream):
+        c = self.cache
+        if self.e4m3:
+            self.h2o.h2o_prefill_select_e4m3(self.dims, None, P, q, k, v, c.k_cache, c.v_cache, c.k_scale,
+                                             c.v_scale, c.scores, c.slot_pos, c.workspace, stream)
+        else:
+            self.h2o.h2o_prefill_select(self.dims, P, q, k, v, c.k_cache, c.v_cache, c.scores, c.slot_pos,
+                                        c.workspace, stream)
+
+    def decode(self, t, q, k_new, v_new, out, evs, evp, stream):
+        c = self.cache
+        if self.e4m3:
+            self.h2o.h2o_decode_step_e4m3(self.dims, None, t, q, k_new, v_new, c.k_cache, c.v_cache,
+                                          c.k_scale, c.v_scale, c.scores, c.slot_pos, out, evs, evp, stream)
+        else:
+            self.h2o.h2o_decode_step(self.dims, t, q, k_new, v_new, c.k_cache, c.v_cache, c.scores,
+                                     c.slot_pos, out, evs, evp, stream)
+
+
 def measured_peaks() -> tuple[dict, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -61,10 +93,13 @@ def source_sha(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def decode_kernel(w: synth.Workload, sms: int) -> tuple[str, str]:
+def decode_kernel(w: synth.Workload, sms: int, e4m3: bool = False) -> tuple[str, str]:
     """Which decode kernel the library launches for this workload (the C ABI's dispatch rule:
     persistent tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512, the cluster-split
-    tcgen05 kernel for other bf16 D = 128 caches up to 8192 slots, the CUDA-core kernel otherwise)."""
+    tcgen05 kernel for other bf16 D = 128 caches up to 8192 slots, the CUDA-core kernel otherwise;
+    the E4M3 cache always runs its persistent tcgen05 kernel)."""
+    if e4m3:
+        return "h2o_decode_e4m3_kernel", os.path.join(CSRC, "h2o_decode_e4m3.cu")
     if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 512 and w.units >= 4 * sms:
         return "h2o_decode_tc_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
     if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 8192:
@@ -241,6 +276,8 @@ def config_of(w: synth.Workload, args) -> dict:
             "head_dim": w.head_dim, "prompt_len": w.prompt_len, "decode_steps": w.decode_steps,
             "budget": w.budget, "k_heavy": w.k_heavy, "k_local": w.k_local, "units": w.units,
             "parallelism": f"replicas x{args.gpus} (units independent, no collective)",
+            "kv_cache": ("E4M3 codes + float32 row scales (bf16 q/k/v/out)" if args.kv_cache == "e4m3"
+                         else w.dtype),
             "l2": "no flush: KV cache and per-step inputs exceed the 129 MB L2",
             "timing": "CUDA events between replays of two CUDA graphs per job (3 prefill launches, "
                       "then the decode launches)"}
@@ -260,6 +297,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill-forward", action="store_true")
+    ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "e4m3"],
+                    help="cache format: the workload's dtype, or E4M3 codes with per-row scales")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.layers is not None:
@@ -298,7 +337,11 @@ def main():
     host = {k: pinned(getattr(inp, k)) for k in ("q_prompt", "k_prompt", "v_prompt", "q_dec", "k_dec", "v_dec")}
     del inp
     dv = {k: v.to(dev) for k, v in host.items()}
-    cache = h2o.H2OCache(dims, P, device=dev)
+    e4m3 = args.kv_cache == "e4m3"
+    if e4m3 and (w.dtype != "bf16" or D != 128):
+        raise SystemExit("--kv-cache e4m3 needs a bf16 workload with head_dim 128")
+    cache = h2o.H2OCache(dims, P, device=dev, e4m3=e4m3)
+    calls = Calls(h2o, dims, cache, e4m3)
     out = torch.empty((S, U, D), dtype=tdt, device=dev)
     evs = torch.empty((S, U), dtype=torch.int32, device=dev)
     evp = torch.empty((S, U), dtype=torch.int32, device=dev)
@@ -306,14 +349,11 @@ def main():
     sp_ptr = stream.cuda_stream
 
     def prefill():
-        h2o.h2o_prefill_select(dims, P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], cache.k_cache,
-                               cache.v_cache, cache.scores, cache.slot_pos, cache.workspace, sp_ptr)
+        calls.prefill(P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], sp_ptr)
 
     def decode_range(s0, s1):
         for s in range(s0, s1):
-            h2o.h2o_decode_step(dims, P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s],
-                                cache.k_cache, cache.v_cache, cache.scores, cache.slot_pos, out[s],
-                                evs[s], evp[s], sp_ptr)
+            calls.decode(P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s], out[s], evs[s], evp[s], sp_ptr)
 
     # One direct run initialises the library's per-device state (kernel attributes, launch plans,
     # error word) outside any capture; then the job is captured as two CUDA graphs (the prefill
@@ -374,11 +414,12 @@ def main():
 
     # Roofline of the decode kernel (the dominant kernel).
     peaks, peak_kind = measured_peaks()
-    bytes_per_launch = [U * decode_bytes_per_unit(min(P + s, w.budget), D, eb) for s in range(S)]
+    bytes_per_launch = [U * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
+                             decode_bytes_per_unit(min(P + s, w.budget), D, eb)) for s in range(S)]
     avg_bytes = float(np.mean(bytes_per_launch))
     avg_decode_s = float(np.mean(decode_ms)) / 1000.0
     achieved = avg_bytes / avg_decode_s / 1e9
-    kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count)
+    kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count, e4m3)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc),
                 "kernel": kname, "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
@@ -386,8 +427,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": config_of(w, args), "roofline": roofline,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else w.dtype,
+            "data": "synthetic", "config": config_of(w, args), "roofline": roofline,
             "kv_read_gbs": achieved,
             "decode_tokens_per_s": world * tokens_per_job / (sum(decode_ms) / K / 1000.0),
             "prefill_ms": float(np.mean(prefill_ms)),
@@ -398,14 +439,14 @@ def main():
 
     # The prompt pass with the attention output (h2o_prefill_forward), timed on its own: not part of
     # the step above, which builds the cache only.
-    if not args.no_prefill_forward:
+    if not args.no_prefill_forward and not e4m3:
         line["prefill_forward"] = prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, args.warmup, K)
 
     # End to end through the public API with host buffers: every job copies its prompt and decode
     # inputs host->device (pinned) and the outputs and eviction indices device->host.
     if not args.no_e2e:
-        line["e2e"] = e2e(args, w, h2o, dims, host, cache, stream, dev, world, tokens_per_job)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["e2e"] = e2e(args, w, calls, host, stream, dev, world, tokens_per_job)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not e4m3:
         line["cpu_baseline"] = cpu_oracle_baseline(w, seed)
     if rank == 0:
         print(json.dumps(line))
@@ -460,10 +501,10 @@ def prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, warmup: int, re
             "output_bytes": U * P * D * w.elem_bytes}
 
 
-def e2e(args, w, h2o, dims, host, cache, stream, dev, world, tokens_per_job):
+def e2e(args, w, calls, host, stream, dev, world, tokens_per_job):
     import torch
     U, D, P, S = w.units, w.head_dim, w.prompt_len, w.decode_steps
-    tdt = cache.dtype
+    tdt = calls.cache.dtype
     chunk = 64
     copy = torch.cuda.Stream(device=dev)
     d_prompt = {k: torch.empty_like(host[k], device=dev) for k in ("q_prompt", "k_prompt", "v_prompt")}
@@ -490,14 +531,12 @@ def e2e(args, w, h2o, dims, host, cache, stream, dev, world, tokens_per_job):
                 e.record(copy)
                 ready.append(e)
         stream.wait_event(ready[0])
-        h2o.h2o_prefill_select(dims, P, d_prompt["q_prompt"], d_prompt["k_prompt"], d_prompt["v_prompt"],
-                               cache.k_cache, cache.v_cache, cache.scores, cache.slot_pos, cache.workspace, sp)
+        calls.prefill(P, d_prompt["q_prompt"], d_prompt["k_prompt"], d_prompt["v_prompt"], sp)
         for ci, c0 in enumerate(range(0, S, chunk)):
             stream.wait_event(ready[ci])
             for s in range(c0, min(S, c0 + chunk)):
-                h2o.h2o_decode_step(dims, P + s, d_dec["q_dec"][s], d_dec["k_dec"][s], d_dec["v_dec"][s],
-                                    cache.k_cache, cache.v_cache, cache.scores, cache.slot_pos, out[s],
-                                    evs[s], evp[s], sp)
+                calls.decode(P + s, d_dec["q_dec"][s], d_dec["k_dec"][s], d_dec["v_dec"][s], out[s], evs[s],
+                             evp[s], sp)
             done = torch.cuda.Event()
             done.record(stream)
             copy.wait_event(done)

@@ -213,6 +213,36 @@ H2O_API h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy
                                           int32_t* evicted_slot, int32_t* evicted_pos, void* stream);
 
 /*
+ * The same two operations over a quantised cache (the H2O post §3.3 discusses combining H2O with
+ * KV-cache quantisation): q, k, v, k_new, v_new and out stay as dims->dtype, which must be
+ * H2O_BF16 with head_dim 128 and budget <= 512 (else H2O_ERR_UNSUPPORTED); the caches hold FP8
+ * E4M3 codes (OCP 8-bit float: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest
+ * finite 448) with one float32 scale per cached row:
+ *   k_cache, v_cache  [units, budget, 128] uint8, device, 16-byte aligned
+ *   k_scale, v_scale  [units, budget] float32, device, 4-byte aligned
+ * A row x is stored as scale = amax(|x|) / 448 (1 for an all-zero row) and codes E4M3(x_d / scale),
+ * each float32 operation rounded once, the conversion to nearest with ties to even, saturating;
+ * attention reads scale * value(code). The new token attends with its bf16 values and is then stored
+ * quantised into its slot; empty slots hold zero codes and scale 0. Everything else (selection,
+ * scores, eviction, policies, errors) as h2o_prefill_select_policy / h2o_decode_step_policy. The
+ * logits and the output run on the tensor cores straight from the 8-bit tiles: the query is split
+ * exactly into two E4M3 rows after a power-of-two rescale, the weights into three (about 12
+ * significant bits).
+ */
+H2O_API h2o_status h2o_prefill_select_e4m3(const h2o_dims* dims, const h2o_policy* policy,
+                                           int32_t prompt_len, const void* q, const void* k,
+                                           const void* v, void* k_cache, void* v_cache,
+                                           float* k_scale, float* v_scale, float* scores,
+                                           int32_t* slot_pos, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+H2O_API h2o_status h2o_decode_step_e4m3(const h2o_dims* dims, const h2o_policy* policy,
+                                        int32_t position, const void* q, const void* k_new,
+                                        const void* v_new, void* k_cache, void* v_cache,
+                                        float* k_scale, float* v_scale, float* scores,
+                                        int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                                        int32_t* evicted_pos, void* stream);
+
+/*
  * Prefill forward of one attention layer with the budgeted cache built in the same pass
  * (H2O post §2.1.1: the prompt's attention weights are Softmax(QK^T/sqrt(d)); their column sums are
  * the scores h2o_prefill_select keeps by). Everything h2o_prefill_select_policy does, plus

@@ -28,7 +28,8 @@ STATIC_SCRATCH_BYTES = 16 << 20  # H2O_STATIC_SCRATCH_BYTES
 
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
            "h2o_prefill_select_static", "h2o_prefill_select_policy", "h2o_prefill_forward",
-           "h2o_decode_step", "h2o_decode_step_policy", "h2o_get_device_error",
+           "h2o_decode_step", "h2o_decode_step_policy", "h2o_prefill_select_e4m3",
+           "h2o_decode_step_e4m3", "h2o_get_device_error",
            "h2o_selftest_wait_timeout", "h2o_last_cuda_error", "h2o_status_string")
 
 
@@ -101,6 +102,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_decode_step_policy.restype = ctypes.c_int
     lib.h2o_prefill_forward.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.h2o_prefill_forward.restype = ctypes.c_int
+    lib.h2o_prefill_select_e4m3.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.h2o_prefill_select_e4m3.restype = ctypes.c_int
+    lib.h2o_decode_step_e4m3.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.h2o_decode_step_e4m3.restype = ctypes.c_int
     lib.h2o_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.h2o_get_device_error.restype = ctypes.c_int
     lib.h2o_selftest_wait_timeout.argtypes = [vp]
@@ -226,6 +231,27 @@ def h2o_decode_step_policy(dims: Dims, policy: Policy | None, position: int, q, 
         _ptr(evicted_pos), _stream(stream)))
 
 
+def h2o_prefill_select_e4m3(dims: Dims, policy: Policy | None, prompt_len: int, q, k, v, k_cache,
+                            v_cache, k_scale, v_scale, scores, slot_pos, workspace, stream=None,
+                            workspace_bytes: int | None = None):
+    """Prefill selection into an E4M3 cache (uint8 codes + float32 per-row scales)."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    _check("h2o_prefill_select_e4m3", load().h2o_prefill_select_e4m3(
+        ctypes.byref(dims), _policy_ref(policy), prompt_len, _ptr(q), _ptr(k), _ptr(v),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(scores), _ptr(slot_pos),
+        _ptr(workspace), wb, _stream(stream)))
+
+
+def h2o_decode_step_e4m3(dims: Dims, policy: Policy | None, position: int, q, k_new, v_new, k_cache,
+                         v_cache, k_scale, v_scale, scores, slot_pos, out, evicted_slot, evicted_pos,
+                         stream=None):
+    """One decode step over an E4M3 cache."""
+    _check("h2o_decode_step_e4m3", load().h2o_decode_step_e4m3(
+        ctypes.byref(dims), _policy_ref(policy), position, _ptr(q), _ptr(k_new), _ptr(v_new),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(scores), _ptr(slot_pos),
+        _ptr(out), _ptr(evicted_slot), _ptr(evicted_pos), _stream(stream)))
+
+
 def h2o_get_device_error(stream=None) -> int:
     """Synchronise ``stream``, return and clear the device error word (0 = none)."""
     code = ctypes.c_int32(0)
@@ -244,17 +270,23 @@ class H2OCache:
     """Device buffers of one budgeted cache (caller-owned memory, allocated here with torch) and the
     running position. A convenience wrapper over the ABI calls; it computes nothing itself."""
 
-    def __init__(self, dims: Dims, prompt_len: int, device="cuda", policy: Policy | None = None):
+    def __init__(self, dims: Dims, prompt_len: int, device="cuda", policy: Policy | None = None,
+                 e4m3: bool = False):
+        """``e4m3``: the K/V caches hold E4M3 codes with per-row scales (bf16, head_dim 128)."""
         import torch
         self.dims = dims
         self.policy = policy
+        self.e4m3 = e4m3
         self.prompt_len = prompt_len
         self.position = prompt_len
         dt = torch.float32 if dims.dtype == F32 else torch.bfloat16
         u, k, d = dims.units, dims.budget, dims.head_dim
         self.dtype = dt
-        self.k_cache = torch.empty((u, k, d), dtype=dt, device=device)
-        self.v_cache = torch.empty((u, k, d), dtype=dt, device=device)
+        cdt = torch.uint8 if e4m3 else dt
+        self.k_cache = torch.empty((u, k, d), dtype=cdt, device=device)
+        self.v_cache = torch.empty((u, k, d), dtype=cdt, device=device)
+        self.k_scale = torch.empty((u, k), dtype=torch.float32, device=device) if e4m3 else None
+        self.v_scale = torch.empty((u, k), dtype=torch.float32, device=device) if e4m3 else None
         self.scores = torch.empty((u, k), dtype=torch.float32, device=device)
         self.slot_pos = torch.empty((u, k), dtype=torch.int32, device=device)
         self.workspace = torch.empty(h2o_prefill_workspace_bytes(dims, prompt_len), dtype=torch.uint8,
@@ -266,7 +298,13 @@ class H2OCache:
     def prefill(self, q, k, v, out=None, stream=None):
         """Build the cache from the prompt; with ``out`` ([units, P, D]) also write the prompt's
         attention output."""
-        if out is None:
+        if self.e4m3:
+            if out is not None:
+                raise ValueError("the prompt output is not produced with an E4M3 cache")
+            h2o_prefill_select_e4m3(self.dims, self.policy, self.prompt_len, q, k, v, self.k_cache,
+                                    self.v_cache, self.k_scale, self.v_scale, self.scores,
+                                    self.slot_pos, self.workspace, stream)
+        elif out is None:
             h2o_prefill_select_policy(self.dims, self.policy, self.prompt_len, q, k, v, self.k_cache,
                                       self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
         else:
@@ -278,7 +316,13 @@ class H2OCache:
         out = self.out if out is None else out
         es = self.evicted_slot if evicted_slot is None else evicted_slot
         ep = self.evicted_pos if evicted_pos is None else evicted_pos
-        h2o_decode_step_policy(self.dims, self.policy, self.position, q, k_new, v_new, self.k_cache,
-                               self.v_cache, self.scores, self.slot_pos, out, es, ep, stream)
+        if self.e4m3:
+            h2o_decode_step_e4m3(self.dims, self.policy, self.position, q, k_new, v_new, self.k_cache,
+                                 self.v_cache, self.k_scale, self.v_scale, self.scores, self.slot_pos,
+                                 out, es, ep, stream)
+        else:
+            h2o_decode_step_policy(self.dims, self.policy, self.position, q, k_new, v_new,
+                                   self.k_cache, self.v_cache, self.scores, self.slot_pos, out, es,
+                                   ep, stream)
         self.position += 1
         return out, es, ep

@@ -196,7 +196,8 @@ static h2o_status prefill_select_impl(const h2o_dims* dims, const h2o_policy* po
                                       int32_t prompt_len, const void* q, const void* k,
                                       const void* v, void* k_cache, void* v_cache, float* scores,
                                       int32_t* slot_pos, void* workspace, size_t workspace_bytes,
-                                      void* stream, void* out = nullptr) {
+                                      void* stream, void* out = nullptr, float* k_scale = nullptr,
+                                      float* v_scale = nullptr) {
   h2o_status st = check_prefill(dims, prompt_len, q, k, workspace, workspace_bytes);
   if (st != H2O_OK) return st;
   const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
@@ -231,6 +232,8 @@ static h2o_status prefill_select_impl(const h2o_dims* dims, const h2o_policy* po
   p.row_bytes = dims->head_dim * elem_bytes(dims);
   p.key_mode = 0;
   p.stride = 1;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   switch (pol.kind) {
     case H2O_POLICY_LOCAL:  // the last `budget` positions
       p.k_heavy = 0;
@@ -268,6 +271,27 @@ h2o_status h2o_prefill_select_policy(const h2o_dims* dims, const h2o_policy* pol
                              workspace, workspace_bytes, stream);
 }
 
+static h2o_status check_e4m3(const h2o_dims* dims, const float* k_scale, const float* v_scale) {
+  h2o_status st = check_dims(dims);
+  if (st != H2O_OK) return st;
+  if (!decode_e4m3_supported(dims->head_dim, dims->dtype, dims->budget)) return H2O_ERR_UNSUPPORTED;
+  if (dims->units_b > 0 && (!k_scale || !v_scale || !aligned4(k_scale) || !aligned4(v_scale)))
+    return H2O_ERR_INVALID_ARG;
+  return H2O_OK;
+}
+
+h2o_status h2o_prefill_select_e4m3(const h2o_dims* dims, const h2o_policy* policy,
+                                   int32_t prompt_len, const void* q, const void* k, const void* v,
+                                   void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                   float* scores, int32_t* slot_pos, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  const h2o_status st = check_e4m3(dims, k_scale, v_scale);
+  if (st != H2O_OK) return st;
+  return prefill_select_impl(dims, policy, prompt_len, q, k, v, k_cache, v_cache, scores, slot_pos,
+                             workspace, workspace_bytes, stream, nullptr, k_scale, v_scale);
+}
+
+
 h2o_status h2o_prefill_forward(const h2o_dims* dims, const h2o_policy* policy, int32_t prompt_len,
                                const void* q, const void* k, const void* v, void* out,
                                void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
@@ -281,7 +305,8 @@ static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* polic
                                    int32_t position, const void* q, const void* k_new,
                                    const void* v_new, void* k_cache, void* v_cache, float* scores,
                                    int32_t* slot_pos, void* out, int32_t* evicted_slot,
-                                   int32_t* evicted_pos, void* stream) {
+                                   int32_t* evicted_pos, void* stream, float* k_scale = nullptr,
+                                   float* v_scale = nullptr) {
   h2o_status st = check_dims(dims);
   if (st != H2O_OK) return st;
   const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
@@ -318,6 +343,10 @@ static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* polic
   p.policy = pol.kind;
   p.n_sink = pol.n_sink;
   p.stride = pol.kind == H2O_POLICY_STRIDED ? pol.stride : 1;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  // E4M3 caches: the tensor-core kernel over 8-bit tiles (bf16, D = 128, budgets up to 512).
+  if (k_scale != nullptr) return from_cuda(launch_decode_e4m3(p, static_cast<cudaStream_t>(stream)));
   // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
   // over units. Other shapes (fp32, D = 64, caches beyond 8192 slots) use the CUDA-core kernel, each
   // unit split over a CTA cluster when units are few.
@@ -348,6 +377,17 @@ h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy* policy
                                   void* stream) {
   return decode_step_impl(dims, policy, position, q, k_new, v_new, k_cache, v_cache, scores,
                           slot_pos, out, evicted_slot, evicted_pos, stream);
+}
+
+h2o_status h2o_decode_step_e4m3(const h2o_dims* dims, const h2o_policy* policy, int32_t position,
+                                const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale, float* scores,
+                                int32_t* slot_pos, void* out, int32_t* evicted_slot,
+                                int32_t* evicted_pos, void* stream) {
+  const h2o_status st = check_e4m3(dims, k_scale, v_scale);
+  if (st != H2O_OK) return st;
+  return decode_step_impl(dims, policy, position, q, k_new, v_new, k_cache, v_cache, scores, slot_pos,
+                          out, evicted_slot, evicted_pos, stream, k_scale, v_scale);
 }
 
 h2o_status h2o_selftest_wait_timeout(void* stream) {

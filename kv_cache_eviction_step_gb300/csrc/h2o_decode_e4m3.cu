@@ -1,0 +1,721 @@
+// h2o_decode_e4m3.cu -- the fused H2O decode step (hot-path rows D1-D7) over a quantised cache: K/V
+// rows stored as FP8 E4M3 codes with one float32 scale per row (the combination of H2O with KV-cache
+// quantisation discussed in the H2O post §3.3), bf16 queries and new tokens, D = 128, budgets up to
+// 512 slots. Both contractions run on the 5th-generation tensor cores straight from the 8-bit tiles
+// (tcgen05.mma kind::f8f6f4), so a slot costs 2 x 128 bytes of K/V instead of 2 x 256.
+//
+// Per unit with n = min(t, budget) cached slots (code rows K8, V8, scales ks, vs):
+//   D2  logits s_j = ks_j (q . K8_j) / sqrt(D). q is rescaled by 2^kq (max |q| into [128, 256)) and
+//       split into two E4M3 rows, q' = q1 + q2, exact for bf16 values in the normal E4M3 range;
+//       MMA M = 128 slots x N = 16 (q1, q2, zeros) x K = 128, the two columns summed in the
+//       epilogue                                                           (H2O post §2.1.1)
+//   D3  softmax over the n logits and the new token (bf16 k_new) on the epilogue warps, the logits
+//       taken in log2 units so that each weight is one ex2
+//   D4  o = (sum_j e_j vs_j V8_j) / l + p_new v_new: the weights w_j = e_j vs_j c (c = 2^kc puts the
+//       largest scale below 256) split into three E4M3 rows (about 12 significant bits), V8^T read as
+//       an MN-major operand straight from the TMA tile; MMA M = 128 (d) x N = 16 x K = slots
+//   D5  scores[j] += p_j in fp32, p_j = e_j / l from the fp32 logits  (H2O post §2.2; 分析 §3.2)
+//   D6  victim = argmin over slots with position <= t - k_local of the policy's key
+//   D7  the new token quantised (scale = amax / 448, codes to nearest even, saturating) into the
+//       victim slot with its score p_new and position                      (H2O post §2.3)
+//
+// Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... Warps 0-7 are
+// the epilogue, two groups of four (one warp per TMEM lane quarter) that take alternate units, each
+// with its own tensor-memory unit slot: with half the bytes per unit, one group's serial chain of
+// reductions and barriers per unit would be slower than the memory system. Warp 8 is the producer
+// (all lanes prepare the split query of each unit, lane 0 streams the unit's K then V code tiles
+// through a ring of 16 KB tiles), warp 9 allocates tensor memory and issues the MMAs, the logits of
+// unit k before the product of unit k - 1. Each group loads its units' tokens and state a unit
+// ahead. All waits are bounded (mbar_wait); tensor memory is always freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "h2o_internal.cuh"
+
+namespace h2o {
+namespace {
+
+constexpr int kD = 128;                    // head dim of this path: one 128-byte code row
+constexpr int kTileRows = 128;             // cache rows per tile (MMA M for the logits)
+constexpr int kTileBytes = kTileRows * kD; // [128 rows x 128 codes]: 16 KB, 128-byte swizzle
+constexpr int kStages = 10;
+constexpr int kMaxTiles = 4;               // budgets up to 512 slots
+constexpr int kNRows = 16;                 // rows of the small operand (q split, or w split): MMA N
+constexpr int kSmallBox = kNRows * 128;    // [16 rows x 128 codes]: 2 KB
+constexpr int kWBytes = kMaxTiles * kSmallBox;  // w operand: 128 slots per 2 KB box
+constexpr int kGroupWarps = 4;             // one epilogue group: a warp per TMEM lane quarter
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kEpiWarps = 2 * kGroupWarps;  // two groups, alternate units
+constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kTmaWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr uint32_t kTmemCols = 256;        // two unit slots of 128 columns
+constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
+constexpr int kAlign = 1024;
+
+// Shared-memory layout (offsets from a 1024-aligned base).
+constexpr int kRingOff = 0;
+constexpr int kQOff = kRingOff + kStages * kTileBytes;
+constexpr int kWOff = kQOff + 2 * kSmallBox;
+constexpr int kCtrlOff = kWOff + 2 * kWBytes;
+constexpr int kCtrlBytes = 1024;
+constexpr int kSmem = kCtrlOff + kCtrlBytes + kAlign;
+
+struct Q8Params {
+  CUtensorMap tm_k;        // K codes [units][budget][128] u8, box 128 x 128 x 1, 128-byte swizzle
+  CUtensorMap tm_v;        // V codes, same
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  float* k_scale;          // [units][budget]
+  float* v_scale;
+  float* scores;
+  int32_t* slot_pos;
+  __nv_bfloat16* out;
+  int32_t* evicted_slot;
+  int32_t* evicted_pos;
+  int32_t* err;
+  int32_t units, budget, k_local, position, n, tiles;
+  float scale;
+  int32_t policy, n_sink, stride;
+};
+
+// ---- PTX wrappers --------------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 128-byte-swizzled operand descriptor. K-major: rows of 128 bytes, 8-row groups `sbo` apart.
+// MN-major: 128-byte MN groups `lbo` apart, 8-row K groups `sbo` apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// kind::f8f6f4 instruction descriptors: fp32 accumulate, E4M3 A and B (format code 0), M = 128,
+// N = 16; K = 32 codes per instruction.
+constexpr uint32_t kIdescQK = (1u << 4) | ((kNRows >> 3) << 17) | ((128 >> 4) << 24);  // A = K8 (K-major)
+constexpr uint32_t kIdescPV = kIdescQK | (1u << 15);  // A = V8^T (MN-major), B = w (K-major)
+
+__device__ __forceinline__ void mma8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, float& a, float& b) {
+  uint32_t r0, r1;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1)
+      : "r"(taddr)
+      : "memory");
+  a = __uint_as_float(r0);
+  b = __uint_as_float(r1);
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+  uint32_t r0, r1, r2, r3;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(taddr)
+      : "memory");
+  v[0] = __uint_as_float(r0);
+  v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3);
+}
+
+// E4M3 code of x (to nearest, ties to even, saturating at +-448) and the value of a code.
+__device__ __forceinline__ uint8_t e4m3(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the special-function unit (ex2.approx, relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Power-of-two exponent that brings a positive maximum into [128, 256) (0 for an all-zero vector).
+__device__ __forceinline__ int range_exp(float mx) { return mx > 0.f ? 7 - ilogbf(mx) : 0; }
+
+// Byte offset of code j (0..127 within its 128-byte row) of row `row` in a 128-byte-swizzled box.
+__device__ __forceinline__ int sw_offset(int row, int j) { return row * 128 + ((((j >> 4) ^ row) & 7) << 4) + (j & 15); }
+
+template <bool kAnyPolicy>
+__global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __grid_constant__ Q8Params p) {
+  const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
+  unsigned char* ring = smem + kRingOff;
+  unsigned char* qbuf = smem + kQOff;
+  unsigned char* wbuf = smem + kWOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCtrlOff);
+  uint64_t* full = bars;                     // [kStages]
+  uint64_t* empty = full + kStages;          // [kStages]
+  uint64_t* q_full = empty + kStages;        // [2] split query written
+  uint64_t* q_empty = q_full + 2;            // [2]
+  uint64_t* s_full = q_empty + 2;            // [2] logits ready
+  uint64_t* w_ready = s_full + 2;            // [2] weights written
+  uint64_t* o_full = w_ready + 2;            // [2] output ready
+  uint64_t* tm_free = o_full + 2;            // [2] unit slot of tensor memory free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_free + 2);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.tiles;
+  const int n = p.n;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&q_full[r], 1);
+      mbar_init(&q_empty[r], 1);
+      mbar_init(&s_full[r], 1);
+      mbar_init(&w_ready[r], 1);
+      mbar_init(&o_full[r], 1);
+      mbar_init(&tm_free[r], kGroupWarps);
+    }
+    fence_mbar_init();
+  }
+  // Rows 2..15 of the q operand and rows 3..15 of the w operand stay zero.
+  for (int i = tid; i < (2 * kSmallBox + 2 * kWBytes) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // Producer: every lane splits four query elements (d = 4 lane .. 4 lane + 3); lane 0 streams.
+    uint32_t g = 0;
+    int k = 0;
+    bool ok = true;
+    uint2 qn = make_uint2(0, 0);  // the next unit's four bf16 query elements
+    auto qload = [&](int u) {
+      if (u < p.units) qn = *reinterpret_cast<const uint2*>(p.q + static_cast<size_t>(u) * kD + 4 * lane);
+    };
+    qload(blockIdx.x);
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
+      const int r = k & 1;
+      float x[4];
+      {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&qn.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&qn.y);
+        x[0] = __low2float(a);
+        x[1] = __high2float(a);
+        x[2] = __low2float(b);
+        x[3] = __high2float(b);
+      }
+      qload(u + gridDim.x);
+      float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const int kq = range_exp(mx);
+      uint32_t w1 = 0, w2 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float xs = ldexpf(x[i], kq);
+        const uint8_t c1 = e4m3(xs);
+        const uint8_t c2 = e4m3(xs - e4m3_value(c1));
+        w1 |= static_cast<uint32_t>(c1) << (8 * i);
+        w2 |= static_cast<uint32_t>(c2) << (8 * i);
+      }
+      if (lane == 0 && k >= 2) ok = mbar_wait(&q_empty[r], static_cast<uint32_t>((k >> 1) - 1) & 1u, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      unsigned char* qb = qbuf + r * kSmallBox;
+      *reinterpret_cast<uint32_t*>(qb + sw_offset(0, 4 * lane)) = w1;
+      *reinterpret_cast<uint32_t*>(qb + sw_offset(1, 4 * lane)) = w2;
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&q_full[r]);
+        for (int i = 0; i < 2 * T; ++i, ++g) {
+          const int s = static_cast<int>(g % kStages);
+          if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
+          const int row0 = (i < T ? i : i - T) * kTileRows;
+          mbar_expect_tx(&full[s], kTileBytes);
+          tma_load_3d(ring + s * kTileBytes, map, 0, row0, u, &full[s]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // Ring positions: unit k's K tiles are 2 T k .. 2 T k + T - 1, its V tiles the next T. The
+      // logits of unit k are issued before the product of unit k - 1, so the epilogue finds the next
+      // unit's logits ready while the tensor core still works on the previous unit's output.
+      bool ok = true;
+      auto wait_tile = [&](uint32_t pos) {
+        return mbar_wait(&full[pos % kStages], (pos / kStages) & 1u, p.err);
+      };
+      auto product = [&](int k) {  // D4 of the k-th unit: o = V8^T w
+        const int r = k & 1;
+        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        const uint32_t slot = tmem + static_cast<uint32_t>(r) * 128;
+        if (!mbar_wait(&w_ready[r], ph, p.err)) return false;
+        tc_fence_after();
+        const uint32_t w_base = smem_u32(wbuf + r * kWBytes);
+        for (int t = 0; t < T; ++t) {
+          const uint32_t pos = static_cast<uint32_t>(2 * T * k + T + t);
+          if (!wait_tile(pos)) return false;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(ring + (pos % kStages) * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 32; ++kk) {
+            // V8^T as MN-major A: the 128 codes of d form one MN group; 32 slots (four 8-row groups
+            // of 1024 bytes) per instruction. w as K-major B: 128 slots per 2 KB box.
+            mma8(slot + kPvCol, sw128_desc(v_base + kk * 4096, kTileBytes, 1024),
+                 sw128_desc(w_base + t * kSmallBox + kk * 32, 16, 1024), kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[pos % kStages]);
+        }
+        mma_commit(&o_full[r]);
+        return true;
+      };
+      int k = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
+        const int r = k & 1;
+        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        const uint32_t slot = tmem + static_cast<uint32_t>(r) * 128;
+        if (k >= 2 && !mbar_wait(&tm_free[r], ph ^ 1u, p.err)) break;
+        if (!mbar_wait(&q_full[r], ph, p.err)) break;
+        tc_fence_after();
+        const uint32_t q_base = smem_u32(qbuf + r * kSmallBox);
+        // D2: logits of each 128-row K tile into columns 16 t, 16 t + 1 of this unit's slot.
+        for (int t = 0; t < T; ++t) {
+          const uint32_t pos = static_cast<uint32_t>(2 * T * k + t);
+          if (!wait_tile(pos)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(ring + (pos % kStages) * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kD / 32; ++kk)  // 32 codes = 32 bytes of each row per instruction
+            mma8(slot + 16 * t, sw128_desc(a_base + kk * 32, 16, 1024), sw128_desc(q_base + kk * 32, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+          mma_commit(&empty[pos % kStages]);
+        }
+        if (!ok) break;
+        mma_commit(&q_empty[r]);
+        mma_commit(&s_full[r]);
+        if (k >= 1 && !product(k - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && k >= 1) product(k - 1);
+    }
+    __syncwarp();
+  } else {
+    // Epilogue: two groups of four warps take alternate units (group g the units k = g, g + 2, ...,
+    // which use tensor-memory slot g). Thread (warp, lane) of a group owns slot 128 t + 32 (warp % 4)
+    // + lane of every tile t, and output element d = its index in the group.
+    const int grp = warp / kGroupWarps;
+    const int gtid = tid - grp * kGroupThreads;
+    const int gwarp = warp % kGroupWarps;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(gwarp * 32) << 16);
+    float* red = reinterpret_cast<float*>(smem + kCtrlOff + 512 + grp * 256);            // [32]
+    unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + kCtrlOff + 640 + grp * 256);
+    int32_t* sred = reinterpret_cast<int32_t*>(smem + kCtrlOff + 704 + grp * 256);
+    auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(3 + grp), "n"(kGroupThreads) : "memory"); };
+    const int32_t last_candidate = p.position - p.k_local;
+    const bool cache_full = n == p.budget;
+    bool ok = true;
+    const int ustep = 2 * gridDim.x;
+    // This thread's w entries (slot gtid of each tile) in rows 0..2 of the swizzled w boxes.
+    const int woff0 = sw_offset(0, gtid), woff1 = sw_offset(1, gtid), woff2 = sw_offset(2, gtid);
+    // A unit's new token and state are loaded one unit (of this group) ahead.
+    __nv_bfloat16 nq = __float2bfloat16_rn(0.f), nkn = nq, nvn = nq;
+    float nsc[kMaxTiles], nks[kMaxTiles], nvs[kMaxTiles];
+    int32_t nsp[kMaxTiles];
+    auto prefetch = [&](int u) {
+      if (u >= p.units) return;
+      const size_t row0 = static_cast<size_t>(u) * p.budget;
+      const size_t ud = static_cast<size_t>(u) * kD + gtid;
+      nq = p.q[ud];
+      nkn = p.k_new[ud];
+      nvn = p.v_new[ud];
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int j = t * kTileRows + gtid;
+        const bool valid = t < T && j < n;
+        nsc[t] = valid ? p.scores[row0 + j] : 0.f;
+        nsp[t] = valid ? p.slot_pos[row0 + j] : 0;
+        nks[t] = valid ? p.k_scale[row0 + j] : 0.f;
+        nvs[t] = valid ? p.v_scale[row0 + j] : 0.f;
+      }
+    };
+    prefetch(blockIdx.x + grp * gridDim.x);
+    for (int u = blockIdx.x + grp * gridDim.x, k = grp; u < p.units && ok; u += ustep, k += 2) {
+      const int r = k & 1;  // == grp
+      const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+      const size_t row0 = static_cast<size_t>(u) * p.budget;
+      const size_t ud = static_cast<size_t>(u) * kD + gtid;
+      const float qd = __bfloat162float(nq);
+      const float knf = __bfloat162float(nkn), vnf = __bfloat162float(nvn);
+      float sc[kMaxTiles], ks[kMaxTiles], vs[kMaxTiles];
+      int32_t sp[kMaxTiles];
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        sc[t] = nsc[t];
+        sp[t] = nsp[t];
+        ks[t] = nks[t];
+        vs[t] = nvs[t];
+      }
+      prefetch(u + ustep);
+      // Round 1 (one barrier): s_new partial, max |q| (the producer's split exponent), the largest
+      // value scale, and the new row's max |k_new|, |v_new| for its quantisation.
+      float part = qd * knf;
+      float qm = fabsf(qd), vsm = fmaxf(fmaxf(vs[0], vs[1]), fmaxf(vs[2], vs[3]));
+      float km = fabsf(knf), vm = fabsf(vnf);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        part += __shfl_xor_sync(0xffffffffu, part, off);
+        qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, off));
+        vsm = fmaxf(vsm, __shfl_xor_sync(0xffffffffu, vsm, off));
+        km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, off));
+        vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+      }
+      float* r1 = red + 16;  // [4 values][kGroupWarps] for this round
+      if (lane == 0) {
+        red[gwarp] = part;
+        r1[gwarp] = qm;
+        r1[4 + gwarp] = vsm;
+        r1[8 + gwarp] = km;
+        r1[12 + gwarp] = vm;
+      }
+
+      if (!mbar_wait(&s_full[r], ph, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      gsync();  // round-1 partials visible
+      const float s_new = (red[0] + red[1] + red[2] + red[3]) * p.scale;
+      const float qmax = fmaxf(fmaxf(r1[0], r1[1]), fmaxf(r1[2], r1[3]));
+      const float vsmax = fmaxf(fmaxf(r1[4], r1[5]), fmaxf(r1[6], r1[7]));
+      const float kamax = fmaxf(fmaxf(r1[8], r1[9]), fmaxf(r1[10], r1[11]));
+      const float vamax = fmaxf(fmaxf(r1[12], r1[13]), fmaxf(r1[14], r1[15]));
+      // Logits in log2 units (the exponentials below are 2^x): ks_j 2^-kq (1/sqrt(D)) log2(e).
+      const float qinv = ldexpf(1.f, -range_exp(qmax)) * p.scale * kLog2e;
+      const float s_new2 = s_new * kLog2e;
+      float s[kMaxTiles];
+      float m = s_new2;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        s[t] = -INFINITY;
+        if (t < T) {
+          float c0, c1;
+          tmem_ld2(lane_base + r * 128 + 16 * t, c0, c1);
+          if (t * kTileRows + gtid < n) s[t] = (c0 + c1) * (qinv * ks[t]);
+        }
+        m = fmaxf(m, s[t]);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      gsync();  // round-1 values read: red[] free
+      if (lane == 0) red[gwarp] = m;
+      gsync();
+      m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+      // D3 + D4 weights: w_j = e_j vs_j 2^kc split into three E4M3 rows of the w operand.
+      const float cw = ldexpf(1.f, range_exp(vsmax));
+      float e[kMaxTiles];
+      float lsum = 0.f;
+      unsigned char* wb = wbuf + r * kWBytes;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        if (t < T) {
+          e[t] = ex2(s[t] - m);  // 0 for -inf (slots past n)
+          lsum += e[t];
+          const float w = e[t] * vs[t] * cw;
+          const uint8_t c1 = e4m3(w);
+          const float r1v = w - e4m3_value(c1);
+          const uint8_t c2 = e4m3(r1v);
+          const uint8_t c3 = e4m3(r1v - e4m3_value(c2));
+          unsigned char* box = wb + t * kSmallBox;
+          box[woff0] = c1;
+          box[woff1] = c2;
+          box[woff2] = c3;
+        } else {
+          e[t] = 0.f;
+        }
+      }
+      fence_async_smem();
+      const float w_new = ex2(s_new2 - m);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      gsync();  // every thread's w entries are written (and fenced); red[] free again
+      if (gtid == 0) mbar_arrive(&w_ready[r]);
+      if (lane == 0) red[gwarp] = lsum;
+      gsync();
+      const float l = red[0] + red[1] + red[2] + red[3] + w_new;
+
+      // D5 + D6 while the tensor core computes the output.
+      unsigned long long best = ~0ull;
+      int32_t best_slot = -1;
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        if (t < T && t * kTileRows + gtid < n) {
+          const float pr = e[t] / l;
+          sc[t] = policy == H2O_POLICY_TOPK ? pr : sc[t] + pr;  // Top-K: this step's weight
+          bool cand = false;
+          const unsigned long long key =
+              policy_key(policy, sc[t], sp[t], last_candidate, p.n_sink, p.stride, &cand);
+          if (cache_full && cand && key < best) {
+            best = key;
+            best_slot = t * kTileRows + gtid;
+          }
+        }
+      }
+      const float p_new = w_new / l;
+      int32_t victim = -1;
+      unsigned long long vkey = ~0ull;
+      if (cache_full) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int32_t os = __shfl_xor_sync(0xffffffffu, best_slot, off);
+          if (ob < best) {
+            best = ob;
+            best_slot = os;
+          }
+        }
+        if (lane == 0) {
+          kred[gwarp] = best;
+          sred[gwarp] = best_slot;
+        }
+        gsync();
+        vkey = kred[0];
+        victim = sred[0];
+#pragma unroll
+        for (int w = 1; w < kGroupWarps; ++w)
+          if (kred[w] < vkey) {
+            vkey = kred[w];
+            victim = sred[w];
+          }
+        if (gtid == 0 && victim < 0) atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
+      }
+
+      // D4 result: o[d] = (sum_j w_j V8_j[d] / 2^kc + w_new v_new[d]) / l.
+      if (!mbar_wait(&o_full[r], ph, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float c[4];
+      tmem_ld4(lane_base + r * 128 + kPvCol, c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tm_free[r]);
+      p.out[ud] = __float2bfloat16_rn(((c[0] + c[1] + c[2]) / cw + w_new * vnf) / l);
+
+      // D7: scores back, the new token quantised into its slot, eviction indices.
+#pragma unroll
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int j = t * kTileRows + gtid;
+        if (t < T && j < n) p.scores[row0 + j] = (j == victim) ? p_new : sc[t];
+      }
+      const int32_t target = cache_full ? victim : n;
+      if (target >= 0) {
+        const float k_s = kamax > 0.f ? kamax / 448.f : 1.f;
+        const float v_s = vamax > 0.f ? vamax / 448.f : 1.f;
+        p.k_cache[(row0 + target) * kD + gtid] = e4m3(knf / k_s);
+        p.v_cache[(row0 + target) * kD + gtid] = e4m3(vnf / v_s);
+        if (gtid == 0) {
+          p.k_scale[row0 + target] = k_s;
+          p.v_scale[row0 + target] = v_s;
+          p.slot_pos[row0 + target] = p.position;
+          if (!cache_full) p.scores[row0 + target] = p_new;
+        }
+      }
+      if (gtid == 0) {
+        p.evicted_slot[u] = cache_full ? victim : -1;
+        p.evicted_pos[u] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
+      }
+      gsync();  // red / kred reuse by this group's next unit
+    }
+  }
+
+  // Tensor memory is freed by the warp that allocated it, after every reader is done.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [units][budget][128] codes as a 3-D tensor; one box = 128 codes x 128 rows x 1 unit, 128-byte
+// swizzle; rows past the budget read as zeros.
+bool encode_codes(CUtensorMap* map, const void* base, int units, int budget) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(budget), static_cast<cuuint64_t>(units)};
+  const cuuint64_t strides[2] = {kD, static_cast<cuuint64_t>(budget) * kD};
+  const cuuint32_t box[3] = {kD, kTileRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct MapCache {
+  const void *k = nullptr, *v = nullptr;
+  int units = -1, budget = -1;
+  CUtensorMap tm_k, tm_v;
+};
+
+const void* const kKernels[2] = {reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<false>),
+                                 reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<true>)};
+
+}  // namespace
+
+// Shapes this kernel serves (a driver without tensor-map encoding fails the launch instead).
+bool decode_e4m3_supported(int head_dim, int dtype, int budget) {
+  return head_dim == kD && dtype == H2O_BF16 && budget <= kMaxTiles * kTileRows;
+}
+
+cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
+  Q8Params p;
+  thread_local MapCache mc;
+  if (mc.k != dp.k_cache || mc.units != dp.units || mc.budget != dp.budget) {
+    if (!encode_codes(&mc.tm_k, dp.k_cache, dp.units, dp.budget)) return cudaErrorInvalidValue;
+    mc.k = dp.k_cache;
+  }
+  if (mc.v != dp.v_cache || mc.units != dp.units || mc.budget != dp.budget) {
+    if (!encode_codes(&mc.tm_v, dp.v_cache, dp.units, dp.budget)) return cudaErrorInvalidValue;
+    mc.v = dp.v_cache;
+  }
+  mc.units = dp.units;
+  mc.budget = dp.budget;
+  p.tm_k = mc.tm_k;
+  p.tm_v = mc.tm_v;
+  p.q = static_cast<const __nv_bfloat16*>(dp.q);
+  p.k_new = static_cast<const __nv_bfloat16*>(dp.k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(dp.v_new);
+  p.k_cache = static_cast<uint8_t*>(dp.k_cache);
+  p.v_cache = static_cast<uint8_t*>(dp.v_cache);
+  p.k_scale = dp.k_scale;
+  p.v_scale = dp.v_scale;
+  p.scores = dp.scores;
+  p.slot_pos = dp.slot_pos;
+  p.out = static_cast<__nv_bfloat16*>(dp.out);
+  p.evicted_slot = dp.evicted_slot;
+  p.evicted_pos = dp.evicted_pos;
+  p.err = dp.err;
+  p.units = dp.units;
+  p.budget = dp.budget;
+  p.k_local = dp.k_local;
+  p.position = dp.position;
+  p.n = dp.n;
+  p.tiles = (dp.n + kTileRows - 1) / kTileRows;
+  p.scale = dp.scale;
+  p.policy = dp.policy;
+  p.n_sink = dp.n_sink;
+  p.stride = dp.stride;
+
+  static std::mutex mu;
+  static std::vector<std::pair<int, int>> ready;  // (device, SM count)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& d : ready)
+      if (d.first == dev) sms = d.second;
+    if (sms == 0) {
+      for (const void* fn : kKernels) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+      }
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      ready.emplace_back(dev, sms);
+    }
+  }
+  const int grid = dp.units < sms ? dp.units : sms;
+  if (dp.policy == H2O_POLICY_H2O)
+    h2o_decode_e4m3_kernel<false><<<grid, kThreads, kSmem, stream>>>(p);
+  else
+    h2o_decode_e4m3_kernel<true><<<grid, kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace h2o

@@ -37,6 +37,8 @@ struct DecodeParams {
   int32_t policy;       // h2o_policy_kind
   int32_t n_sink;       // sink + window
   int32_t stride;       // strided
+  float* k_scale;       // E4M3 caches: [units, budget] per-row scales
+  float* v_scale;
 };
 
 struct PrefillParams {
@@ -70,6 +72,8 @@ struct SelectParams {
   int32_t row_bytes;    // D * element size
   int32_t key_mode;     // 0: by colsum value, 1: stride grid, 2: lowest positions
   int32_t stride;
+  float* k_scale;       // non-null: the caches hold E4M3 codes (D = 128, bf16 inputs) with
+  float* v_scale;       // these per-row scales [units, budget]
 };
 
 // ---- launchers (host) ---------------------------------------------------------------------
@@ -84,6 +88,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
 // Tensor-core decode step with each unit split over a CTA cluster (bf16, D = 128, few units).
 bool decode_tc_split_supported(int head_dim, int dtype, int units, int n);
 cudaError_t launch_decode_tc_split(const DecodeParams& p, cudaStream_t s);
+bool decode_e4m3_supported(int head_dim, int dtype, int budget);
+cudaError_t launch_decode_e4m3(const DecodeParams& p, cudaStream_t s);  // E4M3 caches
 int select_max_prompt();
 int select_max_budget();
 

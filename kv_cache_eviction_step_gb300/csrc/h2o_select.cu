@@ -11,6 +11,8 @@
 // preserving in the high half, position in the low half) are bitonic-sorted in shared memory, the
 // k_heavy-th key is the keep threshold, a block scan over positions assigns the slots, and the
 // K/V rows are copied with 16-byte accesses spread over the whole block.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -64,6 +66,29 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
   }
   __syncthreads();
   return warp_tot[warp] + incl - v;
+}
+
+// Four bf16 values (this lane's 8 bytes) of a 128-element row quantised to
+// E4M3 against the row's scale (amax over the warp / 448, or 1 for an all-zero row); returns the
+// scale and packs the four codes into *codes.
+__device__ __forceinline__ float quantise4(uint2 raw, uint32_t* codes) {
+  float x[4];
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  x[0] = __low2float(a);
+  x[1] = __high2float(a);
+  x[2] = __low2float(b);
+  x[3] = __high2float(b);
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(x[i] / scale, __NV_SATFINITE, __NV_E4M3)) << (8 * i);
+  *codes = w;
+  return scale;
 }
 
 __global__ void __launch_bounds__(kThreads) prefill_select_kernel(const SelectParams p) {
@@ -131,33 +156,60 @@ __global__ void __launch_bounds__(kThreads) prefill_select_kernel(const SelectPa
                                                      static_cast<size_t>(unit) * P * p.row_bytes);
   uint4* kdst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.k_cache) + ub * p.row_bytes);
   uint4* vdst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.v_cache) + ub * p.row_bytes);
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  // Four 16-byte rows pieces per thread per round, all loads issued before the stores, so each
-  // thread keeps eight reads in flight.
-  constexpr int kBatch = 4;
-  const int total = p.budget * vecs;
-  for (int e0 = tid; e0 < total; e0 += kBatch * kThreads) {
-    uint4 kr[kBatch], vr[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int e = e0 + b * kThreads;
-      kr[b] = zero;
-      vr[b] = zero;
-      if (e < total) {
-        const int s = e / vecs;
-        if (s < nk) {
-          const size_t src = static_cast<size_t>(pos_of_slot[s]) * vecs + (e - s * vecs);
-          kr[b] = __ldg(ksrc + src);
-          vr[b] = __ldg(vsrc + src);
-        }
+  if (p.k_scale != nullptr) {
+    // E4M3 caches (D = 128): one warp per slot, four elements per lane; scale = amax / 448 over the
+    // row, codes to nearest even, saturating; empty slots get zero codes and scale 0.
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint2* k2 = reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(p.k) +
+                                                     static_cast<size_t>(unit) * P * 256);
+    const uint2* v2 = reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(p.v) +
+                                                     static_cast<size_t>(unit) * P * 256);
+    uint32_t* kc = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(p.k_cache) + ub * 128);
+    uint32_t* vc = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(p.v_cache) + ub * 128);
+    for (int s = warp; s < p.budget; s += kThreads / 32) {
+      uint32_t kw = 0, vw = 0;
+      float ks = 0.f, vs = 0.f;
+      if (s < nk) {
+        const size_t src = static_cast<size_t>(pos_of_slot[s]) * 32 + lane;  // 32 uint2 per row
+        ks = quantise4(__ldg(k2 + src), &kw);
+        vs = quantise4(__ldg(v2 + src), &vw);
+      }
+      kc[static_cast<size_t>(s) * 32 + lane] = kw;
+      vc[static_cast<size_t>(s) * 32 + lane] = vw;
+      if (lane == 0) {
+        p.k_scale[ub + s] = ks;
+        p.v_scale[ub + s] = vs;
       }
     }
+  } else {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    // Four 16-byte rows pieces per thread per round, all loads issued before the stores, so each
+    // thread keeps eight reads in flight.
+    constexpr int kBatch = 4;
+    const int total = p.budget * vecs;
+    for (int e0 = tid; e0 < total; e0 += kBatch * kThreads) {
+      uint4 kr[kBatch], vr[kBatch];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int e = e0 + b * kThreads;
-      if (e < total) {
-        kdst[e] = kr[b];
-        vdst[e] = vr[b];
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = e0 + b * kThreads;
+        kr[b] = zero;
+        vr[b] = zero;
+        if (e < total) {
+          const int s = e / vecs;
+          if (s < nk) {
+            const size_t src = static_cast<size_t>(pos_of_slot[s]) * vecs + (e - s * vecs);
+            kr[b] = __ldg(ksrc + src);
+            vr[b] = __ldg(vsrc + src);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = e0 + b * kThreads;
+        if (e < total) {
+          kdst[e] = kr[b];
+          vdst[e] = vr[b];
+        }
       }
     }
   }

@@ -82,12 +82,14 @@ def widen(a: np.ndarray) -> np.ndarray:
 
 def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int = synth.DEFAULT_SEED,
         chunk_steps: int = 4096, state_every: int = 0, property_checks=None,
-        policy: tuple[int, int, int] | None = None, prefill_out: bool = False) -> Report:
+        policy: tuple[int, int, int] | None = None, prefill_out: bool = False,
+        e4m3: bool = False) -> Report:
     """Run ``steps`` decode steps (default: all) of workload ``w`` on the GPU for every unit, and the
     oracle in lockstep on ``check_units`` (default: all units). ``policy`` = (kind, n_sink, stride)
     runs both sides under that eviction policy (None: H2O through the plain entry points).
     ``prefill_out`` builds the cache with h2o_prefill_forward and also compares the prompt's
-    attention output with the oracle's on the checked units."""
+    attention output with the oracle's on the checked units. ``e4m3`` runs both sides with the
+    quantised (E4M3 codes + per-row scales) cache; codes and scales must then match bit for bit."""
     import torch
 
     import kv_cache_eviction_step_gb300 as h2o
@@ -99,7 +101,7 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
     check_units = np.arange(U) if check_units is None else np.asarray(check_units)
     rep = Report(w.name, len(check_units), steps)
     dims = dims_of(w)
-    cache = h2o.H2OCache(dims, P, policy=None if policy is None else h2o.Policy(*policy))
+    cache = h2o.H2OCache(dims, P, policy=None if policy is None else h2o.Policy(*policy), e4m3=e4m3)
     rep.topk = policy is not None and policy[0] == oracle.POLICY_TOPK
 
     # Prefill for every unit on the GPU.
@@ -123,7 +125,7 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
     follow = len(check_units) > 0
     orc = oracle.Oracle(k, w.k_heavy, w.k_local,
                         policy=None if policy is None else oracle.Policy(*policy))
-    st = orc.new_state(len(check_units), D, synth.storage_dtype(w))
+    st = orc.new_state(len(check_units), D, synth.storage_dtype(w), e4m3=e4m3)
     if follow:
         gpu_pos = to_host(cache.slot_pos, "i32")[check_units]
         _, pinfo = orc.prefill_select(prompt.q_prompt[check_units], prompt.k_prompt[check_units],
@@ -202,7 +204,13 @@ def compare_state(rep: Report, w, cache, st: oracle.State, check_units, steps_do
     kc = to_host(cache.k_cache, w.dtype)[check_units]
     vc = to_host(cache.v_cache, w.dtype)[check_units]
     if not (np.array_equal(kc, st.k_cache) and np.array_equal(vc, st.v_cache)):
-        rep.notes.append(f"after {steps_done} steps: K/V cache rows differ")
+        bad = np.argwhere((kc != st.k_cache).any(axis=-1) | (vc != st.v_cache).any(axis=-1))
+        rep.notes.append(f"after {steps_done} steps: K/V cache rows differ at {bad[:4].tolist()}")
+    if st.e4m3:
+        ks = cache.k_scale.cpu().numpy()[check_units]
+        vs = cache.v_scale.cpu().numpy()[check_units]
+        if not (np.array_equal(ks, st.k_scale) and np.array_equal(vs, st.v_scale)):
+            rep.notes.append(f"after {steps_done} steps: E4M3 row scales differ")
     sc = to_host(cache.scores, "f32")[check_units].astype(np.float64)
     ref = st.scores.astype(np.float64)
     rel = np.abs(sc - ref) / np.maximum(np.abs(ref), 1e-6)

@@ -160,3 +160,27 @@ def test_prefill_forward_needs_an_aligned_output(lib):
                                    None) == h2o.ERR_INVALID_ARG
     d0 = dims(units_b=0)
     assert lib.h2o_prefill_forward(ctypes.byref(d0), None, 64, *([None] * 9), 0, None) == h2o.OK
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(head_dim=64), h2o.ERR_UNSUPPORTED),
+    (dict(dtype=h2o.F32), h2o.ERR_UNSUPPORTED),
+    (dict(budget=520, k_heavy=260, k_local=260), h2o.ERR_UNSUPPORTED),
+])
+def test_e4m3_entry_points_reject_unsupported_shapes(lib, bad, status):
+    d = dims(**bad)
+    ptrs = [4096 * (i + 1) for i in range(12)]
+    assert lib.h2o_decode_step_e4m3(ctypes.byref(d), None, 10, *ptrs, None) == status
+    ws = h2o.h2o_prefill_workspace_bytes(d, 64)
+    assert lib.h2o_prefill_select_e4m3(ctypes.byref(d), None, 64, *ptrs[:9], 4096, ws, None) == status
+
+
+def test_e4m3_entry_points_need_aligned_scales(lib):
+    d = dims()
+    ptrs = [4096 * (i + 1) for i in range(12)]
+    for i in (5, 6):  # k_scale, v_scale (after q, k_new, v_new, k_cache, v_cache)
+        p = list(ptrs)
+        p[i] = None
+        assert lib.h2o_decode_step_e4m3(ctypes.byref(d), None, 10, *p, None) == h2o.ERR_INVALID_ARG
+        p[i] = ptrs[i] + 2
+        assert lib.h2o_decode_step_e4m3(ctypes.byref(d), None, 10, *p, None) == h2o.ERR_INVALID_ARG
