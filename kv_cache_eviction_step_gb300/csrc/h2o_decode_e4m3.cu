@@ -19,13 +19,13 @@
 //   D7  the new token quantised (scale = amax / 448, codes to nearest even, saturating) into the
 //       victim slot with its score p_new and position                      (H2O post §2.3)
 //
-// Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... Warps 0-7 are
-// the epilogue, two groups of four (one warp per TMEM lane quarter) that take alternate units, each
+// Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... Warps 0-15 are
+// the epilogue, four groups of four (one warp per TMEM lane quarter) that take units in turn, each
 // with its own tensor-memory unit slot: with half the bytes per unit, one group's serial chain of
-// reductions and barriers per unit would be slower than the memory system. Warp 8 is the producer
-// (all lanes prepare the split query of each unit, lane 0 streams the unit's K then V code tiles
-// through a ring of 16 KB tiles), warp 9 allocates tensor memory and issues the MMAs, the logits of
-// unit k before the product of unit k - 1. Each group loads its units' tokens and state a unit
+// reductions and barriers per unit would be slower than the memory system, and more warps hide
+// more latency. Warp 16 is the producer (all lanes prepare the split query of each unit, lane 0
+// streams the unit's K then V code tiles through a ring of 16 KB tiles), warp 17 allocates tensor
+// memory and issues the MMAs, the logits of unit k before the product of unit k - 1. Each group loads its units' tokens and state a unit
 // ahead. All waits are bounded (mbar_wait); tensor memory is always freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -52,20 +52,21 @@ constexpr int kSmallBox = kNRows * 128;    // [16 rows x 128 codes]: 2 KB
 constexpr int kWBytes = kMaxTiles * kSmallBox;  // w operand: 128 slots per 2 KB box
 constexpr int kGroupWarps = 4;             // one epilogue group: a warp per TMEM lane quarter
 constexpr int kGroupThreads = 32 * kGroupWarps;
-constexpr int kEpiWarps = 2 * kGroupWarps;  // two groups, alternate units
+constexpr int kGroups = 4;                 // epilogue groups; unit k goes to group (and slot) k % 4
+constexpr int kEpiWarps = kGroups * kGroupWarps;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr uint32_t kTmemCols = 256;        // two unit slots of 128 columns
+constexpr uint32_t kTmemCols = 128 * kGroups;  // one unit slot of 128 columns per group
 constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
 constexpr int kAlign = 1024;
 
 // Shared-memory layout (offsets from a 1024-aligned base).
 constexpr int kRingOff = 0;
 constexpr int kQOff = kRingOff + kStages * kTileBytes;
-constexpr int kWOff = kQOff + 2 * kSmallBox;
-constexpr int kCtrlOff = kWOff + 2 * kWBytes;
-constexpr int kCtrlBytes = 1024;
+constexpr int kWOff = kQOff + kGroups * kSmallBox;
+constexpr int kCtrlOff = kWOff + kGroups * kWBytes;
+constexpr int kCtrlBytes = 512 + 256 * kGroups;  // mbarriers + TMEM slot, then per-group scratch
 constexpr int kSmem = kCtrlOff + kCtrlBytes + kAlign;
 
 struct Q8Params {
@@ -196,13 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCtrlOff);
   uint64_t* full = bars;                     // [kStages]
   uint64_t* empty = full + kStages;          // [kStages]
-  uint64_t* q_full = empty + kStages;        // [2] split query written
-  uint64_t* q_empty = q_full + 2;            // [2]
-  uint64_t* s_full = q_empty + 2;            // [2] logits ready
-  uint64_t* w_ready = s_full + 2;            // [2] weights written
-  uint64_t* o_full = w_ready + 2;            // [2] output ready
-  uint64_t* tm_free = o_full + 2;            // [2] unit slot of tensor memory free again
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_free + 2);
+  uint64_t* q_full = empty + kStages;        // [kGroups] split query written
+  uint64_t* q_empty = q_full + kGroups;      // [kGroups]
+  uint64_t* s_full = q_empty + kGroups;      // [kGroups] logits ready
+  uint64_t* w_ready = s_full + kGroups;      // [kGroups] weights written
+  uint64_t* o_full = w_ready + kGroups;      // [kGroups] output ready
+  uint64_t* tm_free = o_full + kGroups;      // [kGroups] unit slot of tensor memory free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_free + kGroups);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.tiles;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < kGroups; ++r) {
       mbar_init(&q_full[r], 1);
       mbar_init(&q_empty[r], 1);
       mbar_init(&s_full[r], 1);
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
     fence_mbar_init();
   }
   // Rows 2..15 of the q operand and rows 3..15 of the w operand stay zero.
-  for (int i = tid; i < (2 * kSmallBox + 2 * kWBytes) / 16; i += kThreads)
+  for (int i = tid; i < (kGroups * kSmallBox + kGroups * kWBytes) / 16; i += kThreads)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
   fence_async_smem();
   if (warp == kMmaWarp) {
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
     };
     qload(blockIdx.x);
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
-      const int r = k & 1;
+      const int r = k % kGroups;
       float x[4];
       {
         const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&qn.x);
@@ -273,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
         w1 |= static_cast<uint32_t>(c1) << (8 * i);
         w2 |= static_cast<uint32_t>(c2) << (8 * i);
       }
-      if (lane == 0 && k >= 2) ok = mbar_wait(&q_empty[r], static_cast<uint32_t>((k >> 1) - 1) & 1u, p.err);
+      if (lane == 0 && k >= kGroups)
+        ok = mbar_wait(&q_empty[r], static_cast<uint32_t>(k / kGroups - 1) & 1u, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       unsigned char* qb = qbuf + r * kSmallBox;
@@ -308,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
         return mbar_wait(&full[pos % kStages], (pos / kStages) & 1u, p.err);
       };
       auto product = [&](int k) {  // D4 of the k-th unit: o = V8^T w
-        const int r = k & 1;
-        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        const int r = k % kGroups;
+        const uint32_t ph = static_cast<uint32_t>(k / kGroups) & 1u;
         const uint32_t slot = tmem + static_cast<uint32_t>(r) * 128;
         if (!mbar_wait(&w_ready[r], ph, p.err)) return false;
         tc_fence_after();
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
       };
       int k = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++k) {
-        const int r = k & 1;
-        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        const int r = k % kGroups;
+        const uint32_t ph = static_cast<uint32_t>(k / kGroups) & 1u;
         const uint32_t slot = tmem + static_cast<uint32_t>(r) * 128;
-        if (k >= 2 && !mbar_wait(&tm_free[r], ph ^ 1u, p.err)) break;
+        if (k >= kGroups && !mbar_wait(&tm_free[r], ph ^ 1u, p.err)) break;
         if (!mbar_wait(&q_full[r], ph, p.err)) break;
         tc_fence_after();
         const uint32_t q_base = smem_u32(qbuf + r * kSmallBox);
@@ -367,21 +369,26 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
     }
     __syncwarp();
   } else {
-    // Epilogue: two groups of four warps take alternate units (group g the units k = g, g + 2, ...,
-    // which use tensor-memory slot g). Thread (warp, lane) of a group owns slot 128 t + 32 (warp % 4)
+    // Epilogue: kGroups groups of four warps take units in turn (group g the units k = g,
+    // g + kGroups, ..., which use tensor-memory slot g). Thread (warp, lane) of a group owns slot 128 t + 32 (warp % 4)
     // + lane of every tile t, and output element d = its index in the group.
     const int grp = warp / kGroupWarps;
     const int gtid = tid - grp * kGroupThreads;
     const int gwarp = warp % kGroupWarps;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(gwarp * 32) << 16);
-    float* red = reinterpret_cast<float*>(smem + kCtrlOff + 512 + grp * 256);            // [32]
+    // Per-group reduction scratch, one array per round, so that each round needs one barrier: a
+    // round's array is rewritten only after the group has passed the next rounds' barriers.
+    float* red = reinterpret_cast<float*>(smem + kCtrlOff + 512 + grp * 256);    // s_new partials [4]
+    float* r1 = red + 4;                                                          // maxima [4][4]
+    float* rm = red + 20;                                                         // logit max [4]
+    float* rl = red + 24;                                                         // sums [4]
     unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + kCtrlOff + 640 + grp * 256);
     int32_t* sred = reinterpret_cast<int32_t*>(smem + kCtrlOff + 704 + grp * 256);
     auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(3 + grp), "n"(kGroupThreads) : "memory"); };
     const int32_t last_candidate = p.position - p.k_local;
     const bool cache_full = n == p.budget;
     bool ok = true;
-    const int ustep = 2 * gridDim.x;
+    const int ustep = kGroups * gridDim.x;
     // This thread's w entries (slot gtid of each tile) in rows 0..2 of the swizzled w boxes.
     const int woff0 = sw_offset(0, gtid), woff1 = sw_offset(1, gtid), woff2 = sw_offset(2, gtid);
     // A unit's new token and state are loaded one unit (of this group) ahead.
@@ -406,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
       }
     };
     prefetch(blockIdx.x + grp * gridDim.x);
-    for (int u = blockIdx.x + grp * gridDim.x, k = grp; u < p.units && ok; u += ustep, k += 2) {
-      const int r = k & 1;  // == grp
-      const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+    for (int u = blockIdx.x + grp * gridDim.x, k = grp; u < p.units && ok; u += ustep, k += kGroups) {
+      const int r = grp;  // == k % kGroups
+      const uint32_t ph = static_cast<uint32_t>(k / kGroups) & 1u;
       const size_t row0 = static_cast<size_t>(u) * p.budget;
       const size_t ud = static_cast<size_t>(u) * kD + gtid;
       const float qd = __bfloat162float(nq);
@@ -436,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
         km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, off));
         vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
       }
-      float* r1 = red + 16;  // [4 values][kGroupWarps] for this round
       if (lane == 0) {
         red[gwarp] = part;
         r1[gwarp] = qm;
@@ -473,10 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      gsync();  // round-1 values read: red[] free
-      if (lane == 0) red[gwarp] = m;
+      if (lane == 0) rm[gwarp] = m;
       gsync();
-      m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+      m = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
       // D3 + D4 weights: w_j = e_j vs_j 2^kc split into three E4M3 rows of the w operand.
       const float cw = ldexpf(1.f, range_exp(vsmax));
       float e[kMaxTiles];
@@ -504,11 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
       const float w_new = ex2(s_new2 - m);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-      gsync();  // every thread's w entries are written (and fenced); red[] free again
+      if (lane == 0) rl[gwarp] = lsum;
+      gsync();  // every thread's w entries are written (and fenced), and the sums
       if (gtid == 0) mbar_arrive(&w_ready[r]);
-      if (lane == 0) red[gwarp] = lsum;
-      gsync();
-      const float l = red[0] + red[1] + red[2] + red[3] + w_new;
+      const float l = rl[0] + rl[1] + rl[2] + rl[3] + w_new;
 
       // D5 + D6 while the tensor core computes the output.
       unsigned long long best = ~0ull;
@@ -592,7 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __gr
         p.evicted_slot[u] = cache_full ? victim : -1;
         p.evicted_pos[u] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
       }
-      gsync();  // red / kred reuse by this group's next unit
     }
   }
 
