@@ -19,13 +19,14 @@
 //   D7  the new token quantised (scale = amax / 448, codes to nearest even, saturating) into the
 //       victim slot with its score p_new and position                      (H2O post §2.3)
 //
-// Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... Warps 0-15 are
-// the epilogue, four groups of four (one warp per TMEM lane quarter) that take units in turn, each
-// with its own tensor-memory unit slot: with half the bytes per unit, one group's serial chain of
-// reductions and barriers per unit would be slower than the memory system, and more warps hide
-// more latency. Warp 16 is the producer (all lanes prepare the split query of each unit, lane 0
-// streams the unit's K then V code tiles through a ring of 16 KB tiles), warp 17 allocates tensor
-// memory and issues the MMAs, the logits of unit k before the product of unit k - 1. Each group loads its units' tokens and state a unit
+// Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... The first warps
+// are the epilogue, G groups of four (one warp per TMEM lane quarter; G = 4 for caches up to 256
+// slots, 2 beyond) that take units in turn, each with its own tensor-memory unit slot: with half the
+// bytes per unit, one group's serial chain of reductions and barriers per unit would be slower than
+// the memory system, and more warps hide more latency. The next warp is the producer (all lanes
+// prepare the split query of each unit, lane 0 streams the unit's K then V code tiles through a ring
+// of 16 KB tiles), the last allocates tensor memory and issues the MMAs, the logits of unit k before
+// the product of unit k - 1. Each group loads its units' tokens and state a unit
 // ahead. All waits are bounded (mbar_wait); tensor memory is always freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -45,29 +46,32 @@ namespace {
 constexpr int kD = 128;                    // head dim of this path: one 128-byte code row
 constexpr int kTileRows = 128;             // cache rows per tile (MMA M for the logits)
 constexpr int kTileBytes = kTileRows * kD; // [128 rows x 128 codes]: 16 KB, 128-byte swizzle
-constexpr int kStages = 10;
 constexpr int kMaxTiles = 4;               // budgets up to 512 slots
 constexpr int kNRows = 16;                 // rows of the small operand (q split, or w split): MMA N
 constexpr int kSmallBox = kNRows * 128;    // [16 rows x 128 codes]: 2 KB
 constexpr int kWBytes = kMaxTiles * kSmallBox;  // w operand: 128 slots per 2 KB box
 constexpr int kGroupWarps = 4;             // one epilogue group: a warp per TMEM lane quarter
 constexpr int kGroupThreads = 32 * kGroupWarps;
-constexpr int kGroups = 4;                 // epilogue groups; unit k goes to group (and slot) k % 4
-constexpr int kEpiWarps = kGroups * kGroupWarps;
-constexpr int kThreads = 32 * (kEpiWarps + 2);
-constexpr int kTmaWarp = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr uint32_t kTmemCols = 128 * kGroups;  // one unit slot of 128 columns per group
 constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
 constexpr int kAlign = 1024;
 
-// Shared-memory layout (offsets from a 1024-aligned base).
-constexpr int kRingOff = 0;
-constexpr int kQOff = kRingOff + kStages * kTileBytes;
-constexpr int kWOff = kQOff + kGroups * kSmallBox;
-constexpr int kCtrlOff = kWOff + kGroups * kWBytes;
-constexpr int kCtrlBytes = 512 + 256 * kGroups;  // mbarriers + TMEM slot, then per-group scratch
-constexpr int kSmem = kCtrlOff + kCtrlBytes + kAlign;
+// Per group count G: epilogue groups take units in turn (unit k -> group and tensor-memory slot
+// k % G); four groups for caches of up to two 128-slot tiles, two (with a deeper ring) beyond, where
+// four groups' units would not fit in the ring. Shared-memory offsets are from a 1024-aligned base.
+template <int G>
+struct Layout {
+  static constexpr int kStages = G == 4 ? 10 : 12;   // streamed 16 KB tiles
+  static constexpr int kEpiWarps = G * kGroupWarps;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static constexpr int kTmaWarp = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr uint32_t kTmemCols = 128 * G;     // one unit slot of 128 columns per group
+  static constexpr int kQOff = kStages * kTileBytes;
+  static constexpr int kWOff = kQOff + G * kSmallBox;
+  static constexpr int kCtrlOff = kWOff + G * kWBytes;
+  static constexpr int kCtrlBytes = 512 + 256 * G;   // mbarriers + TMEM slot, then per-group scratch
+  static constexpr int kSmem = kCtrlOff + kCtrlBytes + kAlign;
+};
 
 struct Q8Params {
   CUtensorMap tm_k;        // K codes [units][budget][128] u8, box 128 x 128 x 1, 128-byte swizzle
@@ -186,12 +190,19 @@ __device__ __forceinline__ int range_exp(float mx) { return mx > 0.f ? 7 - ilogb
 // Byte offset of code j (0..127 within its 128-byte row) of row `row` in a 128-byte-swizzled box.
 __device__ __forceinline__ int sw_offset(int row, int j) { return row * 128 + ((((j >> 4) ^ row) & 7) << 4) + (j & 15); }
 
-template <bool kAnyPolicy>
-__global__ void __launch_bounds__(kThreads, 1) h2o_decode_e4m3_kernel(const __grid_constant__ Q8Params p) {
+template <bool kAnyPolicy, int kGroups>
+__global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
+    h2o_decode_e4m3_kernel(const __grid_constant__ Q8Params p) {
+  using L = Layout<kGroups>;
+  constexpr int kStages = L::kStages, kEpiWarps = L::kEpiWarps, kThreads = L::kThreads;
+  constexpr int kTmaWarp = L::kTmaWarp, kMmaWarp = L::kMmaWarp;
+  constexpr uint32_t kTmemCols = L::kTmemCols;
+  constexpr int kRingOff = 0, kQOff = L::kQOff, kWOff = L::kWOff, kCtrlOff = L::kCtrlOff;
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
+  (void)kEpiWarps;
   unsigned char* qbuf = smem + kQOff;
   unsigned char* wbuf = smem + kWOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCtrlOff);
@@ -644,8 +655,12 @@ struct MapCache {
   CUtensorMap tm_k, tm_v;
 };
 
-const void* const kKernels[2] = {reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<false>),
-                                 reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<true>)};
+// [groups == 4][any policy]
+const void* const kKernels[2][2] = {
+    {reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<false, 2>),
+     reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<true, 2>)},
+    {reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<false, 4>),
+     reinterpret_cast<const void*>(h2o_decode_e4m3_kernel<true, 4>)}};
 
 }  // namespace
 
@@ -704,20 +719,26 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
     for (auto& d : ready)
       if (d.first == dev) sms = d.second;
     if (sms == 0) {
-      for (const void* fn : kKernels) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-      }
+      for (int g4 = 0; g4 < 2; ++g4)
+        for (int any = 0; any < 2; ++any) {
+          e = cudaFuncSetAttribute(kKernels[g4][any], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   g4 ? Layout<4>::kSmem : Layout<2>::kSmem);
+          if (e != cudaSuccess) return e;
+        }
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
       ready.emplace_back(dev, sms);
     }
   }
   const int grid = dp.units < sms ? dp.units : sms;
-  if (dp.policy == H2O_POLICY_H2O)
-    h2o_decode_e4m3_kernel<false><<<grid, kThreads, kSmem, stream>>>(p);
-  else
-    h2o_decode_e4m3_kernel<true><<<grid, kThreads, kSmem, stream>>>(p);
+  const bool any = dp.policy != H2O_POLICY_H2O;
+  if (p.tiles <= 2) {
+    if (any) h2o_decode_e4m3_kernel<true, 4><<<grid, Layout<4>::kThreads, Layout<4>::kSmem, stream>>>(p);
+    else h2o_decode_e4m3_kernel<false, 4><<<grid, Layout<4>::kThreads, Layout<4>::kSmem, stream>>>(p);
+  } else {
+    if (any) h2o_decode_e4m3_kernel<true, 2><<<grid, Layout<2>::kThreads, Layout<2>::kSmem, stream>>>(p);
+    else h2o_decode_e4m3_kernel<false, 2><<<grid, Layout<2>::kThreads, Layout<2>::kSmem, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
