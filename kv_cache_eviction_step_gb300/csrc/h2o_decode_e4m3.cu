@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         vs[t] = nvs[t];
       }
       prefetch(u + ustep);
-      // Round 1 (one barrier): s_new partial, max |q| (the producer's split exponent), the largest
+      // First reduction (one barrier): s_new partial, max |q| (the producer's split exponent), the largest
       // value scale, and the new row's max |k_new|, |v_new| for its quantisation.
       float part = qd * knf;
       float qm = fabsf(qd), vsm = fmaxf(fmaxf(vs[0], vs[1]), fmaxf(vs[2], vs[3]));
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      gsync();  // round-1 partials visible
+      gsync();  // first-reduction partials visible
       const float s_new = (red[0] + red[1] + red[2] + red[3]) * p.scale;
       const float qmax = fmaxf(fmaxf(r1[0], r1[1]), fmaxf(r1[2], r1[3]));
       const float vsmax = fmaxf(fmaxf(r1[4], r1[5]), fmaxf(r1[6], r1[7]));

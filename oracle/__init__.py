@@ -26,7 +26,7 @@ F32, BF16 = 0, 1
 NO_EVICTION, RULE, NEAR_TIE, ERROR_BOUND, REJECTED = range(5)
 KIND_NAMES = ["no_eviction", "rule", "near_tie", "error_bound", "rejected"]
 
-# The spec near-tie threshold: two candidate scores closer than this (relative) are a tie.
+# The near-tie threshold of the parity rule: two candidate scores closer than this (relative) are a tie.
 TIE_REL = 1e-6
 
 

@@ -243,7 +243,7 @@ static int eviction_candidate(const h2o_oracle_policy* pol, int32_t pos, int32_t
 }
 
 /* Decide whether a preferred kept set (slot_pos layout) may replace the rule's. */
-static int32_t judge_prefill_preference(int32_t budget, int32_t k_local, int32_t P,
+static int32_t assess_prefill_preference(int32_t budget, int32_t k_local, int32_t P,
                                         const double* c, const unsigned char* keep_rule,
                                         const int32_t* prefer, double tie_rel, double err_rel,
                                         unsigned char* keep_pref) {
@@ -357,15 +357,15 @@ static int prefill_select(int32_t units, int32_t D, int32_t budget, int32_t k_he
       info.kind = H2O_ORACLE_RULE;
       if (k_heavy > 0 && k_heavy < nc) info.gap_rel = rel_gap(cand[k_heavy].c, cand[k_heavy - 1].c);
       if (prefer_pos) {
-        int32_t kind = judge_prefill_preference(budget, k_local, P, c, keep,
+        int32_t kind = assess_prefill_preference(budget, k_local, P, c, keep,
                                                 prefer_pos + (size_t)u * budget, tie_rel, err_rel,
                                                 keep_pref);
         if (pol->kind != H2O_ORACLE_POLICY_H2O) {
-          /* Same judgement on the values this policy ranks by. */
+          /* Same assessment on the values this policy ranks by. */
           double* vals = s;  /* row scratch is free here */
           for (int32_t p = 0; p < P; ++p)
             vals[p] = pol->kind == H2O_ORACLE_POLICY_STRIDED ? (double)(p % pol->stride == 0) : a[p];
-          kind = judge_prefill_preference(budget, k_local, P, vals, keep,
+          kind = assess_prefill_preference(budget, k_local, P, vals, keep,
                                           prefer_pos + (size_t)u * budget, tie_rel, err_rel, keep_pref);
           if (by_position(pol) && kind != H2O_ORACLE_RULE) kind = H2O_ORACLE_REJECTED;
         }
