@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
   constexpr uint32_t kTmemCols = L::kTmemCols;
   constexpr int kRingOff = 0, kQOff = L::kQOff, kWOff = L::kWOff, kCtrlOff = L::kCtrlOff;
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
+  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous step's cache, scales, scores and slot map are complete from here on
 
   if (warp == kTmaWarp) {
     // Producer: every lane splits four query elements (d = 4 lane .. 4 lane + 3); lane 0 streams.
@@ -732,14 +734,8 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
   }
   const int grid = dp.units < sms ? dp.units : sms;
   const bool any = dp.policy != H2O_POLICY_H2O;
-  if (p.tiles <= 2) {
-    if (any) h2o_decode_e4m3_kernel<true, 4><<<grid, Layout<4>::kThreads, Layout<4>::kSmem, stream>>>(p);
-    else h2o_decode_e4m3_kernel<false, 4><<<grid, Layout<4>::kThreads, Layout<4>::kSmem, stream>>>(p);
-  } else {
-    if (any) h2o_decode_e4m3_kernel<true, 2><<<grid, Layout<2>::kThreads, Layout<2>::kSmem, stream>>>(p);
-    else h2o_decode_e4m3_kernel<false, 2><<<grid, Layout<2>::kThreads, Layout<2>::kSmem, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (p.tiles <= 2) return launch_pdl(kKernels[1][any], grid, Layout<4>::kThreads, Layout<4>::kSmem, stream, &p);
+  return launch_pdl(kKernels[0][any], grid, Layout<2>::kThreads, Layout<2>::kSmem, stream, &p);
 }
 
 }  // namespace h2o

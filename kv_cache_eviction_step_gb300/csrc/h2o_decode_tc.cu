@@ -171,6 +171,7 @@ __device__ __forceinline__ int w_offset(int j, int row) {
 template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid_constant__ TcDecodeParams p) {
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
+  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
@@ -602,6 +604,7 @@ template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const __grid_constant__ TcSplitParams sp_) {
   const TcDecodeParams& p = sp_.d;
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
+  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem;
@@ -652,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
   cluster_sync_all();  // every CTA's exchange barriers exist before any peer arrives on them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
   const size_t row0 = static_cast<size_t>(unit) * p.budget;
 
   if (warp == kTmaWarp) {
@@ -1010,8 +1014,10 @@ cudaLaunchConfig_t split_config(int units, int splits, cudaStream_t stream, cuda
   attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -1061,8 +1067,9 @@ bool plan_split(int units, int n, int* splits_out, int* chunk_out) {
     }
   }
   if (splits > 1) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = split_config(splits, splits, nullptr, attr);
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
     for (const void* fn : kSplitKernels) {
       int clusters = 0;
       if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters == 0) {
@@ -1092,7 +1099,7 @@ cudaError_t launch_decode_tc_split(const DecodeParams& dp, cudaStream_t stream) 
   cudaError_t e = fill_params(dp, sp.d);
   if (e != cudaSuccess) return e;
   if (!plan_split(dp.units, dp.n, &sp.splits, &sp.chunk)) return cudaErrorInvalidConfiguration;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = split_config(dp.units, sp.splits, stream, attr);
   void* args[] = {&sp};
   return cudaLaunchKernelExC(&cfg, kSplitKernels[dp.policy != H2O_POLICY_H2O], args);
@@ -1128,11 +1135,7 @@ cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
     }
   }
   const int grid = dp.units < sms ? dp.units : sms;
-  if (dp.policy == H2O_POLICY_H2O)
-    h2o_decode_tc_kernel<false><<<grid, kThreads, kSmem, stream>>>(p);
-  else
-    h2o_decode_tc_kernel<true><<<grid, kThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kTcKernels[dp.policy != H2O_POLICY_H2O], grid, kThreads, kSmem, stream, &p);
 }
 
 }  // namespace h2o

@@ -78,6 +78,25 @@ struct SelectParams {
 
 // ---- launchers (host) ---------------------------------------------------------------------
 
+// Launch `kernel(*params)` with programmatic stream serialization allowed (the kernel calls
+// pdl_launch_dependents / pdl_wait), so consecutive decode steps overlap launch and prologue.
+template <typename Params>
+inline cudaError_t launch_pdl(const void* kernel, int grid, int threads, int smem, cudaStream_t stream,
+                              Params* params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {params};
+  return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int dtype, cudaStream_t s);
 cudaError_t launch_prefill_scores_simt(const PrefillParams& p, int head_dim, int dtype, cudaStream_t s);
 cudaError_t launch_prefill_scores_tc(const PrefillParams& p, int head_dim, cudaStream_t s);  // bf16
@@ -195,6 +214,12 @@ __device__ __forceinline__ unsigned long long policy_key(int32_t policy, float s
     }
   }
 }
+
+// Programmatic dependent launch: the next kernel in the stream may start its prologue once every
+// CTA of this one has signalled; it waits for this grid's completion (and memory) before touching
+// the data this grid writes.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
