@@ -240,3 +240,26 @@ def test_streaming_full_length_properties_and_prefix_parity():
                      property_checks=props, state_every=0)
     assert not rep.notes, rep.notes
     torch.cuda.synchronize()
+
+
+def test_long_prompt_column_sums_and_selection():
+    """A 4096-token prompt (32 tiles of 128 rows per unit) on the tensor-core passes: every column sum
+    against the oracle, the kept slot map, and a few decode steps."""
+    w = W["llama-7b"].with_(batch=1, heads=2, prompt_len=4096, decode_steps=4, budget=1024,
+                            k_heavy=512, k_local=512)
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    inp = synth.generate(w, steps=0)
+    dims = parity.dims_of(w)
+    q, k = parity.to_device(inp.q_prompt, w.dtype), parity.to_device(inp.k_prompt, w.dtype)
+    colsum = torch.empty((w.units, w.prompt_len), dtype=torch.float32, device="cuda")
+    ws = torch.empty(h2o.h2o_prefill_workspace_bytes(dims, w.prompt_len), dtype=torch.uint8, device="cuda")
+    h2o.h2o_prefill_scores(dims, w.prompt_len, q, k, colsum, ws)
+    got = colsum.cpu().numpy().astype(np.float64)
+    orc = oracle.Oracle(w.budget, w.k_heavy, w.k_local)
+    st = orc.new_state(w.units, w.head_dim, synth.storage_dtype(w))
+    ref, _ = orc.prefill_select(inp.q_prompt, inp.k_prompt, inp.v_prompt, st, want_colsum=True)
+    rel = np.abs(got - ref) / np.maximum(ref, 1e-3)
+    assert rel.max() < 2e-5, rel.max()
+    _assert(parity.run(w, state_every=2))
