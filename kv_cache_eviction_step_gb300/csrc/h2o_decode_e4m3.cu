@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
   // starves the producer's lookahead (measured: a lag of 2 with four groups took 106 us instead of
   // 80.5 us per OPT-6.7B step).
   constexpr int kLag = 1;
+  constexpr bool kInOrder = kGroups == 2;  // see the producer and MMA warps
   constexpr int kStages = L::kStages, kEpiWarps = L::kEpiWarps, kThreads = L::kThreads;
   constexpr int kTmaWarp = L::kTmaWarp, kMmaWarp = L::kMmaWarp;
   constexpr uint32_t kTmemCols = L::kTmemCols;
@@ -261,6 +262,15 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
     uint32_t g = 0;
     int k = 0;
     bool ok = true;
+    int prev_u = -1;  // the unit whose V tiles follow this unit's K tiles
+    auto stream = [&](const CUtensorMap* map, int t, int unit) {
+      const int s = static_cast<int>(g % kStages);
+      if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) return false;
+      mbar_expect_tx(&full[s], kTileBytes);
+      tma_load_3d(ring + s * kTileBytes, map, 0, t * kTileRows, unit, &full[s]);
+      ++g;
+      return true;
+    };
     uint2 qn = make_uint2(0, 0);  // the next unit's four bf16 query elements
     auto qload = [&](int u) {
       if (u < p.units) qn = *reinterpret_cast<const uint2*>(p.q + static_cast<size_t>(u) * kD + 4 * lane);
@@ -302,29 +312,43 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&q_full[r]);
-        for (int i = 0; i < 2 * T; ++i, ++g) {
-          const int s = static_cast<int>(g % kStages);
-          if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
-            ok = false;
-            break;
+        if constexpr (kInOrder) {
+          // The order the tensor core consumes: this unit's K tiles, then the previous unit's V.
+          for (int t = 0; t < T && ok; ++t) ok = stream(&p.tm_k, t, u);
+          for (int t = 0; t < T && ok && prev_u >= 0; ++t) ok = stream(&p.tm_v, t, prev_u);
+          prev_u = u;
+        } else {
+          // V right behind K: the product of this unit follows soon after its logits.
+          for (int i = 0; i < 2 * T; ++i, ++g) {
+            const int s = static_cast<int>(g % kStages);
+            if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
+              ok = false;
+              break;
+            }
+            const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
+            const int row0 = (i < T ? i : i - T) * kTileRows;
+            mbar_expect_tx(&full[s], kTileBytes);
+            tma_load_3d(ring + s * kTileBytes, map, 0, row0, u, &full[s]);
           }
-          const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
-          const int row0 = (i < T ? i : i - T) * kTileRows;
-          mbar_expect_tx(&full[s], kTileBytes);
-          tma_load_3d(ring + s * kTileBytes, map, 0, row0, u, &full[s]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
+    if (kInOrder && lane == 0)
+      for (int t = 0; t < T && ok && prev_u >= 0; ++t) ok = stream(&p.tm_v, t, prev_u);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      // Ring positions: unit k's K tiles are 2 T k .. 2 T k + T - 1, its V tiles the next T. The
-      // logits of unit k are issued before the product of unit k - kLag, so the epilogue finds the
-      // next unit's logits ready while the tensor core works on the previous unit's output; the ring
-      // (>= 2 T (kLag + 1) tiles) holds the K tiles of unit k while the V tiles of units k - kLag ..
-      // k - 1 wait for their weights.
+      // The logits of unit k are issued before the product of unit k - kLag, so the epilogue finds
+      // the next unit's logits ready while the tensor core works on the previous unit's output.
+      // With two groups (long caches) the producer loads the tiles in exactly this order, so ring
+      // slots free in order and V tiles do not wait in the ring; with four groups (short caches) it
+      // loads each unit's V right behind its K, so the product never waits for its tiles.
       bool ok = true;
+      uint32_t g = 0;  // ring tiles consumed (in-order loads)
+      // Ring position of tile t of unit k's K (V) tiles when V follows K within each unit.
+      auto pos_k = [&](int k, int t) { return static_cast<uint32_t>(2 * T * k + t); };
+      auto pos_v = [&](int k, int t) { return static_cast<uint32_t>(2 * T * k + T + t); };
       auto wait_tile = [&](uint32_t pos) {
         return mbar_wait(&full[pos % kStages], (pos / kStages) & 1u, p.err);
       };
@@ -336,7 +360,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         tc_fence_after();
         const uint32_t w_base = smem_u32(wbuf + r * kWBytes);
         for (int t = 0; t < T; ++t) {
-          const uint32_t pos = static_cast<uint32_t>(2 * T * k + T + t);
+          const uint32_t pos = kInOrder ? g++ : pos_v(k, t);
           if (!wait_tile(pos)) return false;
           tc_fence_after();
           const uint32_t v_base = smem_u32(ring + (pos % kStages) * kTileBytes);
@@ -363,7 +387,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         const uint32_t q_base = smem_u32(qbuf + r * kSmallBox);
         // D2: logits of each 128-row K tile into columns 16 t, 16 t + 1 of this unit's slot.
         for (int t = 0; t < T; ++t) {
-          const uint32_t pos = static_cast<uint32_t>(2 * T * k + t);
+          const uint32_t pos = kInOrder ? g++ : pos_k(k, t);
           if (!wait_tile(pos)) {
             ok = false;
             break;
