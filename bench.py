@@ -108,16 +108,17 @@ def decode_kernel(w: synth.Workload, sms: int, e4m3: bool = False) -> tuple[str,
 
 
 def recorded_traffic(workload: str, kernel: str, src: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the current
+    """DRAM bytes per decode launch from the committed ncu records, if one was taken on the current
     source of this kernel and on this workload; otherwise None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
-        rec = json.load(f)
-    if (rec.get("kernel") != kernel or rec.get("kernel_sha") != source_sha(src)
-            or rec.get("workload") != workload):
-        return None
-    return rec.get("dram_bytes_per_launch")
+        recs = json.load(f)
+    for rec in recs.get("records", [recs]):
+        if (rec.get("kernel") == kernel and rec.get("kernel_sha") == source_sha(src)
+                and rec.get("workload") == workload):
+            return rec.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
