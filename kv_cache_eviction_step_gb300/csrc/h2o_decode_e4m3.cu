@@ -24,10 +24,11 @@
 // slots, 2 beyond) that take units in turn, each with its own tensor-memory unit slot: with half the
 // bytes per unit, one group's serial chain of reductions and barriers per unit would be slower than
 // the memory system, and more warps hide more latency. The next warp is the producer (all lanes
-// prepare the split query of each unit, lane 0 streams the unit's K then V code tiles through a ring
-// of 16 KB tiles), the last allocates tensor memory and issues the MMAs, the logits of unit k before
-// the product of unit k - 1. Each group loads its units' tokens and state a unit
-// ahead. All waits are bounded (mbar_wait); tensor memory is always freed.
+// prepare the split query of each unit, lane 0 streams code tiles through a ring of 16 KB tiles in
+// the order the tensor core consumes them), the last allocates tensor memory and issues the MMAs, the
+// logits of unit k before the product of unit k - 2 (four groups) or k - 1 (two). Each group loads
+// its units' tokens and state a unit ahead. All waits are bounded (mbar_wait); tensor memory is
+// always freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -49,7 +50,6 @@ constexpr int kTileBytes = kTileRows * kD; // [128 rows x 128 codes]: 16 KB, 128
 constexpr int kMaxTiles = 4;               // budgets up to 512 slots
 constexpr int kNRows = 16;                 // rows of the small operand (q split, or w split): MMA N
 constexpr int kSmallBox = kNRows * 128;    // [16 rows x 128 codes]: 2 KB
-constexpr int kWBytes = kMaxTiles * kSmallBox;  // w operand: 128 slots per 2 KB box
 constexpr int kGroupWarps = 4;             // one epilogue group: a warp per TMEM lane quarter
 constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
@@ -60,7 +60,9 @@ constexpr int kAlign = 1024;
 // four groups' units would not fit in the ring. Shared-memory offsets are from a 1024-aligned base.
 template <int G>
 struct Layout {
-  static constexpr int kStages = G == 4 ? 10 : 12;   // streamed 16 KB tiles
+  static constexpr int kTiles = G == 4 ? 2 : kMaxTiles;  // largest cache this instantiation serves
+  static constexpr int kWBytes = kTiles * kSmallBox;     // w operand: 128 slots per 2 KB box
+  static constexpr int kStages = G == 4 ? 10 : 12;       // streamed 16 KB tiles
   static constexpr int kEpiWarps = G * kGroupWarps;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static constexpr int kTmaWarp = kEpiWarps;
@@ -194,12 +196,14 @@ template <bool kAnyPolicy, int kGroups>
 __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
     h2o_decode_e4m3_kernel(const __grid_constant__ Q8Params p) {
   using L = Layout<kGroups>;
-  // Products issued one unit behind the logits: a longer lag holds more V tiles in the ring and
-  // starves the producer's lookahead (measured: a lag of 2 with four groups took 106 us instead of
-  // 80.5 us per OPT-6.7B step).
-  constexpr int kLag = 1;
-  constexpr bool kInOrder = kGroups == 2;  // see the producer and MMA warps
+  // Products issued kLag units behind the logits, so kLag + 1 epilogue groups run their softmax at
+  // once; unit k's slot of tensor memory is reused by unit k + kGroups, whose logits follow product
+  // k only if kLag < kGroups. The producer loads tiles in the order the tensor core consumes them
+  // (unit k's K tiles, then unit k - kLag's V tiles), so ring slots free in order.
+  constexpr int kLag = kGroups == 4 ? 2 : 1;
+  static_assert(kLag < kGroups, "a unit's tensor-memory slot must be free before its logits");
   constexpr int kStages = L::kStages, kEpiWarps = L::kEpiWarps, kThreads = L::kThreads;
+  constexpr int kTiles = L::kTiles, kWBytes = L::kWBytes;
   constexpr int kTmaWarp = L::kTmaWarp, kMmaWarp = L::kMmaWarp;
   constexpr uint32_t kTmemCols = L::kTmemCols;
   constexpr int kRingOff = 0, kQOff = L::kQOff, kWOff = L::kWOff, kCtrlOff = L::kCtrlOff;
@@ -259,18 +263,9 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
 
   if (warp == kTmaWarp) {
     // Producer: every lane splits four query elements (d = 4 lane .. 4 lane + 3); lane 0 streams.
-    uint32_t g = 0;
+    uint32_t g = 0;  // ring tiles issued
     int k = 0;
     bool ok = true;
-    int prev_u = -1;  // the unit whose V tiles follow this unit's K tiles
-    auto stream = [&](const CUtensorMap* map, int t, int unit) {
-      const int s = static_cast<int>(g % kStages);
-      if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) return false;
-      mbar_expect_tx(&full[s], kTileBytes);
-      tma_load_3d(ring + s * kTileBytes, map, 0, t * kTileRows, unit, &full[s]);
-      ++g;
-      return true;
-    };
     uint2 qn = make_uint2(0, 0);  // the next unit's four bf16 query elements
     auto qload = [&](int u) {
       if (u < p.units) qn = *reinterpret_cast<const uint2*>(p.q + static_cast<size_t>(u) * kD + 4 * lane);
@@ -312,43 +307,44 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&q_full[r]);
-        if constexpr (kInOrder) {
-          // The order the tensor core consumes: this unit's K tiles, then the previous unit's V.
-          for (int t = 0; t < T && ok; ++t) ok = stream(&p.tm_k, t, u);
-          for (int t = 0; t < T && ok && prev_u >= 0; ++t) ok = stream(&p.tm_v, t, prev_u);
-          prev_u = u;
-        } else {
-          // V right behind K: the product of this unit follows soon after its logits.
-          for (int i = 0; i < 2 * T; ++i, ++g) {
-            const int s = static_cast<int>(g % kStages);
-            if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
-              ok = false;
-              break;
-            }
-            const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
-            const int row0 = (i < T ? i : i - T) * kTileRows;
-            mbar_expect_tx(&full[s], kTileBytes);
-            tma_load_3d(ring + s * kTileBytes, map, 0, row0, u, &full[s]);
+        // This unit's K tiles, then the V tiles of the unit kLag behind it (none for the first kLag).
+        const int vu = u - kLag * static_cast<int>(gridDim.x);
+        const int nt = k < kLag ? T : 2 * T;
+        for (int i = 0; i < nt; ++i, ++g) {
+          const int s = static_cast<int>(g % kStages);
+          if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
+            ok = false;
+            break;
           }
+          const bool is_k = i < T;
+          mbar_expect_tx(&full[s], kTileBytes);
+          tma_load_3d(ring + s * kTileBytes, is_k ? &p.tm_k : &p.tm_v, 0, (is_k ? i : i - T) * kTileRows,
+                      is_k ? u : vu, &full[s]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    if (kInOrder && lane == 0)
-      for (int t = 0; t < T && ok && prev_u >= 0; ++t) ok = stream(&p.tm_v, t, prev_u);
+    // The V tiles of the last kLag units.
+    for (int j = k - kLag < 0 ? 0 : k - kLag; lane == 0 && ok && j < k; ++j) {
+      const int vu = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+      for (int t = 0; t < T; ++t, ++g) {
+        const int s = static_cast<int>(g % kStages);
+        if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&full[s], kTileBytes);
+        tma_load_3d(ring + s * kTileBytes, &p.tm_v, 0, t * kTileRows, vu, &full[s]);
+      }
+    }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // The logits of unit k are issued before the product of unit k - kLag, so the epilogue finds
-      // the next unit's logits ready while the tensor core works on the previous unit's output.
-      // With two groups (long caches) the producer loads the tiles in exactly this order, so ring
-      // slots free in order and V tiles do not wait in the ring; with four groups (short caches) it
-      // loads each unit's V right behind its K, so the product never waits for its tiles.
+      // the next units' logits ready while the tensor core works on an earlier unit's output. Ring
+      // tiles are consumed in the order the producer loads them.
       bool ok = true;
-      uint32_t g = 0;  // ring tiles consumed (in-order loads)
-      // Ring position of tile t of unit k's K (V) tiles when V follows K within each unit.
-      auto pos_k = [&](int k, int t) { return static_cast<uint32_t>(2 * T * k + t); };
-      auto pos_v = [&](int k, int t) { return static_cast<uint32_t>(2 * T * k + T + t); };
+      uint32_t g = 0;  // ring tiles consumed
       auto wait_tile = [&](uint32_t pos) {
         return mbar_wait(&full[pos % kStages], (pos / kStages) & 1u, p.err);
       };
@@ -360,16 +356,17 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         tc_fence_after();
         const uint32_t w_base = smem_u32(wbuf + r * kWBytes);
         for (int t = 0; t < T; ++t) {
-          const uint32_t pos = kInOrder ? g++ : pos_v(k, t);
+          const uint32_t pos = g++;
           if (!wait_tile(pos)) return false;
           tc_fence_after();
-          const uint32_t v_base = smem_u32(ring + (pos % kStages) * kTileBytes);
+          const uint64_t a0 = sw128_desc(smem_u32(ring + (pos % kStages) * kTileBytes), kTileBytes, 1024);
+          const uint64_t b0 = sw128_desc(w_base + t * kSmallBox, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kTileRows / 32; ++kk) {
             // V8^T as MN-major A: the 128 codes of d form one MN group; 32 slots (four 8-row groups
             // of 1024 bytes) per instruction. w as K-major B: 128 slots per 2 KB box.
-            mma8(slot + kPvCol, sw128_desc(v_base + kk * 4096, kTileBytes, 1024),
-                 sw128_desc(w_base + t * kSmallBox + kk * 32, 16, 1024), kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            mma8(slot + kPvCol, a0 + static_cast<uint64_t>(kk * (4096 >> 4)), b0 + static_cast<uint64_t>(kk * (32 >> 4)),
+                 kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&empty[pos % kStages]);
         }
@@ -387,16 +384,17 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         const uint32_t q_base = smem_u32(qbuf + r * kSmallBox);
         // D2: logits of each 128-row K tile into columns 16 t, 16 t + 1 of this unit's slot.
         for (int t = 0; t < T; ++t) {
-          const uint32_t pos = kInOrder ? g++ : pos_k(k, t);
+          const uint32_t pos = g++;
           if (!wait_tile(pos)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(ring + (pos % kStages) * kTileBytes);
+          const uint64_t a0 = sw128_desc(smem_u32(ring + (pos % kStages) * kTileBytes), 16, 1024);
+          const uint64_t b0 = sw128_desc(q_base, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kD / 32; ++kk)  // 32 codes = 32 bytes of each row per instruction
-            mma8(slot + 16 * t, sw128_desc(a_base + kk * 32, 16, 1024), sw128_desc(q_base + kk * 32, 16, 1024),
+            mma8(slot + 16 * t, a0 + static_cast<uint64_t>(kk * (32 >> 4)), b0 + static_cast<uint64_t>(kk * (32 >> 4)),
                  kIdescQK, kk > 0 ? 1u : 0u);
           mma_commit(&empty[pos % kStages]);
         }
@@ -436,8 +434,8 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
     const int woff0 = sw_offset(0, gtid), woff1 = sw_offset(1, gtid), woff2 = sw_offset(2, gtid);
     // A unit's new token and state are loaded one unit (of this group) ahead.
     __nv_bfloat16 nq = __float2bfloat16_rn(0.f), nkn = nq, nvn = nq;
-    float nsc[kMaxTiles], nks[kMaxTiles], nvs[kMaxTiles];
-    int32_t nsp[kMaxTiles];
+    float nsc[kTiles], nks[kTiles], nvs[kTiles];
+    int32_t nsp[kTiles];
     auto prefetch = [&](int u) {
       if (u >= p.units) return;
       const size_t row0 = static_cast<size_t>(u) * p.budget;
@@ -446,7 +444,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       nkn = p.k_new[ud];
       nvn = p.v_new[ud];
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         const int j = t * kTileRows + gtid;
         const bool valid = t < T && j < n;
         nsc[t] = valid ? p.scores[row0 + j] : 0.f;
@@ -463,10 +461,10 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       const size_t ud = static_cast<size_t>(u) * kD + gtid;
       const float qd = __bfloat162float(nq);
       const float knf = __bfloat162float(nkn), vnf = __bfloat162float(nvn);
-      float sc[kMaxTiles], ks[kMaxTiles], vs[kMaxTiles];
-      int32_t sp[kMaxTiles];
+      float sc[kTiles], ks[kTiles], vs[kTiles];
+      int32_t sp[kTiles];
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         sc[t] = nsc[t];
         sp[t] = nsp[t];
         ks[t] = nks[t];
@@ -476,7 +474,9 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       // First reduction (one barrier): s_new partial, max |q| (the producer's split exponent), the largest
       // value scale, and the new row's max |k_new|, |v_new| for its quantisation.
       float part = qd * knf;
-      float qm = fabsf(qd), vsm = fmaxf(fmaxf(vs[0], vs[1]), fmaxf(vs[2], vs[3]));
+      float qm = fabsf(qd), vsm = vs[0];
+#pragma unroll
+      for (int t = 1; t < kTiles; ++t) vsm = fmaxf(vsm, vs[t]);
       float km = fabsf(knf), vm = fabsf(vnf);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -508,10 +508,10 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       // Logits in log2 units (the exponentials below are 2^x): ks_j 2^-kq (1/sqrt(D)) log2(e).
       const float qinv = ldexpf(1.f, -range_exp(qmax)) * p.scale * kLog2e;
       const float s_new2 = s_new * kLog2e;
-      float s[kMaxTiles];
+      float s[kTiles];
       float m = s_new2;
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         s[t] = -INFINITY;
         if (t < T) {
           float c0, c1;
@@ -527,11 +527,11 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       m = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
       // D3 + D4 weights: w_j = e_j vs_j 2^kc split into three E4M3 rows of the w operand.
       const float cw = ldexpf(1.f, range_exp(vsmax));
-      float e[kMaxTiles];
+      float e[kTiles];
       float lsum = 0.f;
       unsigned char* wb = wbuf + r * kWBytes;
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         if (t < T) {
           e[t] = ex2(s[t] - m);  // 0 for -inf (slots past n)
           lsum += e[t];
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
       unsigned long long best = ~0ull;
       int32_t best_slot = -1;
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         if (t < T && t * kTileRows + gtid < n) {
           const float pr = e[t] / l;
           sc[t] = policy == H2O_POLICY_TOPK ? pr : sc[t] + pr;  // Top-K: this step's weight
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
 
       // D7: scores back, the new token quantised into its slot, eviction indices.
 #pragma unroll
-      for (int t = 0; t < kMaxTiles; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         const int j = t * kTileRows + gtid;
         if (t < T && j < n) p.scores[row0 + j] = (j == victim) ? p_new : sc[t];
       }
