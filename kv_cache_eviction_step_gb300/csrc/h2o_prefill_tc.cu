@@ -274,15 +274,45 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Two-lane fp32 fma and add (packed instructions of this GPU generation): each lane rounds exactly
+// like the scalar fmaf / + it stands for, so results do not change, at half the instructions.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+
+// The largest of three values in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float max32(const float* v) {
-  float m[16];
+  float m[11];
 #pragma unroll
-  for (int x = 0; x < 16; ++x) m[x] = fmaxf(v[x], v[x + 16]);
+  for (int x = 0; x < 10; ++x) m[x] = max3(v[3 * x], v[3 * x + 1], v[3 * x + 2]);
+  m[10] = fmaxf(v[30], v[31]);
+  const float a = max3(m[0], m[1], m[2]), b = max3(m[3], m[4], m[5]), c = max3(m[6], m[7], m[8]);
+  return fmaxf(max3(a, b, c), fmaxf(m[9], m[10]));
+}
+
+// sum_x 2^(v[x] sl + nb[x]) over 32 values in four interleaved partial sums (x mod 4), combined as
+// (s0 + s1) + (s2 + s3); lanes x < lo contribute nothing.
+template <bool kMask>
+__device__ __forceinline__ float exp2_sum32(const float* v, float2 sl2, const float* nb, int lo) {
+  float2 s01 = make_float2(0.f, 0.f), s23 = s01;
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int x = 0; x < w; ++x) m[x] = fmaxf(m[x], m[x + w]);
-  return m[0];
+  for (int x = 0; x < 32; x += 4) {
+    const float2 e01 = fma2(make_float2(v[x], v[x + 1]), sl2, make_float2(nb[x], nb[x + 1]));
+    const float2 e23 = fma2(make_float2(v[x + 2], v[x + 3]), sl2, make_float2(nb[x + 2], nb[x + 3]));
+    if constexpr (kMask) {
+      s01 = add2(s01, make_float2(x >= lo ? ex2(e01.x) : 0.f, x + 1 >= lo ? ex2(e01.y) : 0.f));
+      s23 = add2(s23, make_float2(x + 2 >= lo ? ex2(e23.x) : 0.f, x + 3 >= lo ? ex2(e23.y) : 0.f));
+    } else {
+      s01 = add2(s01, make_float2(ex2(e01.x), ex2(e01.y)));
+      s23 = add2(s23, make_float2(ex2(e23.x), ex2(e23.y)));
+    }
+  }
+  return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
 // Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
@@ -531,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int x0 = (it.t_begin + t) * kTile + h * kCols;  // key (query) of this warp's column 0
         if constexpr (kCol) {
           // this tile's query statistics for this warp's columns; prefetch the next tile's
-          xw[a * kCols + lane] = fmaf(qm, kLog2e, log2f(ql));
+          xw[a * kCols + lane] = -fmaf(qm, kLog2e, log2f(ql));
           if (t + 1 < it.nt) qload(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
           __syncwarp();
         }
@@ -554,42 +584,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             m2 = cm;
           }
           if (m2 != -INFINITY) {
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            float nm[kCols];
 #pragma unroll
-            for (int x = 0; x < kCols; ++x) s4[x & 3] += ex2(fmaf(v[x], sl, -m2));
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            for (int x = 0; x < kCols; ++x) nm[x] = -m2;
+            l += exp2_sum32<false>(v, make_float2(sl, sl), nm, 0);
           }
         } else if constexpr (kCol) {
           const float4* b4 = reinterpret_cast<const float4*>(xw + a * kCols);
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          float nb[kCols];  // this tile's negated query offsets for this warp's columns
+#pragma unroll
+          for (int x4 = 0; x4 < kCols / 4; ++x4) {
+            const float4 b = b4[x4];
+            nb[4 * x4 + 0] = b.x;
+            nb[4 * x4 + 1] = b.y;
+            nb[4 * x4 + 2] = b.z;
+            nb[4 * x4 + 3] = b.w;
+          }
+          const float2 sl2 = make_float2(sl, sl);
           if (p.last_row_only) {
             const int xl = P - 1 - x0;  // the last query's column, if this warp holds it
             if (xl >= 0 && xl < kCols) {
+              float s0 = 0.f;
 #pragma unroll
               for (int x = 0; x < kCols; ++x)
-                if (x == xl && row <= P - 1) s4[0] += ex2(fmaf(v[x], sl, -xw[a * kCols + x]));
+                if (x == xl && row <= P - 1) s0 += ex2(fmaf(v[x], sl, nb[x]));
+              c += s0;
             }
           } else if (it.t_begin + t > it.at) {  // queries all after the keys
-#pragma unroll
-            for (int x4 = 0; x4 < kCols / 4; ++x4) {
-              const float4 b = b4[x4];
-              s4[0] += ex2(fmaf(v[4 * x4 + 0], sl, -b.x));
-              s4[1] += ex2(fmaf(v[4 * x4 + 1], sl, -b.y));
-              s4[2] += ex2(fmaf(v[4 * x4 + 2], sl, -b.z));
-              s4[3] += ex2(fmaf(v[4 * x4 + 3], sl, -b.w));
-            }
+            c += exp2_sum32<false>(v, sl2, nb, 0);
           } else {  // the diagonal tile: queries i >= row
-            const int lo = row - x0;
-#pragma unroll
-            for (int x4 = 0; x4 < kCols / 4; ++x4) {
-              const float4 b = b4[x4];
-              s4[0] += 4 * x4 + 0 >= lo ? ex2(fmaf(v[4 * x4 + 0], sl, -b.x)) : 0.f;
-              s4[1] += 4 * x4 + 1 >= lo ? ex2(fmaf(v[4 * x4 + 1], sl, -b.y)) : 0.f;
-              s4[2] += 4 * x4 + 2 >= lo ? ex2(fmaf(v[4 * x4 + 2], sl, -b.z)) : 0.f;
-              s4[3] += 4 * x4 + 3 >= lo ? ex2(fmaf(v[4 * x4 + 3], sl, -b.w)) : 0.f;
-            }
+            c += exp2_sum32<true>(v, sl2, nb, row - x0);
           }
-          c += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         } else {
           // Output pass. Probability tile a was last read by the product of logit tile g - 2.
           if (g >= 2 && ok) ok = mbar_wait(&p_free[a], (g / 2 - 1) & 1u, p.err);
@@ -622,13 +647,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
           // Probabilities against mu (masked logits give 0) into this warp's 32 keys of tile a:
           // 16-byte chunks (h & 1) * 4 .. + 3 of box h >> 1, row r.
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const float2 sl2 = make_float2(sl, sl), nmu = make_float2(-mu, -mu);
+            float2 s01 = make_float2(0.f, 0.f), s23 = s01;
 #pragma unroll
-          for (int x = 0; x < kCols; ++x) {
-            v[x] = ex2(fmaf(v[x], sl, -mu));
-            s4[x & 3] += v[x];
+            for (int x = 0; x < kCols; x += 4) {
+              const float2 e01 = fma2(make_float2(v[x], v[x + 1]), sl2, nmu);
+              const float2 e23 = fma2(make_float2(v[x + 2], v[x + 3]), sl2, nmu);
+              v[x] = ex2(e01.x);
+              v[x + 1] = ex2(e01.y);
+              v[x + 2] = ex2(e23.x);
+              v[x + 3] = ex2(e23.y);
+              s01 = add2(s01, make_float2(v[x], v[x + 1]));
+              s23 = add2(s23, make_float2(v[x + 2], v[x + 3]));
+            }
+            l += (s01.x + s01.y) + (s23.x + s23.y);
           }
-          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           unsigned char* rowp = ptile + a * kPBytes + (h >> 1) * kBoxBytes + r * 128;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
