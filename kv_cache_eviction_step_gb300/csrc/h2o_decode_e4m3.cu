@@ -219,8 +219,7 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
   uint64_t* full = bars;                     // [kStages]
   uint64_t* empty = full + kStages;          // [kStages]
   uint64_t* q_full = empty + kStages;        // [kGroups] split query written
-  uint64_t* q_empty = q_full + kGroups;      // [kGroups]
-  uint64_t* s_full = q_empty + kGroups;      // [kGroups] logits ready
+  uint64_t* s_full = q_full + kGroups;       // [kGroups] logits ready (and the q buffer free again)
   uint64_t* w_ready = s_full + kGroups;      // [kGroups] weights written
   uint64_t* o_full = w_ready + kGroups;      // [kGroups] output ready
   uint64_t* tm_free = o_full + kGroups;      // [kGroups] unit slot of tensor memory free again
@@ -237,7 +236,6 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
     }
     for (int r = 0; r < kGroups; ++r) {
       mbar_init(&q_full[r], 1);
-      mbar_init(&q_empty[r], 1);
       mbar_init(&s_full[r], 1);
       mbar_init(&w_ready[r], 1);
       mbar_init(&o_full[r], 1);
@@ -297,7 +295,8 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
         w2 |= static_cast<uint32_t>(c2) << (8 * i);
       }
       if (lane == 0 && k >= kGroups)
-        ok = mbar_wait(&q_empty[r], static_cast<uint32_t>(k / kGroups - 1) & 1u, p.err);
+        // the q buffer of this group is free once the logits of its previous unit are done
+        ok = mbar_wait(&s_full[r], static_cast<uint32_t>(k / kGroups - 1) & 1u, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       unsigned char* qb = qbuf + r * kSmallBox;
@@ -399,7 +398,6 @@ __global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
           mma_commit(&empty[pos % kStages]);
         }
         if (!ok) break;
-        mma_commit(&q_empty[r]);
         mma_commit(&s_full[r]);
         if (k >= kLag && !product(k - kLag)) {
           ok = false;
