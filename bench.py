@@ -298,6 +298,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill-forward", action="store_true")
+    ap.add_argument("--no-per-layer", action="store_true",
+                    help="skip the decode timing with one launch per layer and step")
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "e4m3"],
                     help="cache format: the workload's dtype, or E4M3 codes with per-row scales")
     args = ap.parse_args()
@@ -438,6 +440,11 @@ def main():
             "clocks": clocks.summary(),
             "input_generation_s": t_gen}
 
+    # The same decode steps launched per layer, as a model's forward pass has to launch them.
+    if not args.no_per_layer and w.layers > 1:
+        line["decode_per_layer"] = decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream,
+                                                           dev, g_pre, args.warmup, K, e4m3)
+
     # The prompt pass with the attention output (h2o_prefill_forward), timed on its own: not part of
     # the step above, which builds the cache only.
     if not args.no_prefill_forward and not e4m3:
@@ -454,6 +461,75 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream, dev, g_pre, warmup: int,
+                            reps: int, e4m3: bool) -> dict:
+    """The decode steps with one launch per layer and step (a model cannot batch its layers: layer
+    l + 1's query needs layer l's output), against the all-layers launch of the main timing. Layer l's
+    units are the contiguous slice [l B H, (l + 1) B H) of every array; the launches are captured in
+    CUDA graphs of at most GRAPH_STEPS launches, the cache is rebuilt by the prefill graph before
+    each replay (untimed), and CUDA events bracket the decode graphs."""
+    import torch
+    L, P, S, D = w.layers, w.prompt_len, w.decode_steps, w.head_dim
+    ul = w.units // L
+    dl = type(dims)(units_b=dims.units_b // L, heads=dims.heads, head_dim=dims.head_dim,
+                    budget=dims.budget, k_heavy=dims.k_heavy, k_local=dims.k_local, dtype=dims.dtype)
+    c, sp = calls.cache, stream.cuda_stream
+
+    def launch(s, l):
+        sl = slice(l * ul, (l + 1) * ul)
+        args = (dv["q_dec"][s][sl], dv["k_dec"][s][sl], dv["v_dec"][s][sl], c.k_cache[sl], c.v_cache[sl])
+        if e4m3:
+            h2o.h2o_decode_step_e4m3(dl, None, P + s, *args, c.k_scale[sl], c.v_scale[sl], c.scores[sl],
+                                     c.slot_pos[sl], out[s][sl], evs[s][sl], evp[s][sl], sp)
+        else:
+            h2o.h2o_decode_step(dl, P + s, *args, c.scores[sl], c.slot_pos[sl], out[s][sl], evs[s][sl],
+                                evp[s][sl], sp)
+
+    order = [(s, l) for s in range(S) for l in range(L)]
+    with torch.cuda.stream(stream):  # one direct pass sets up the per-shape launch plans
+        g_pre.replay()
+        for s, l in order:
+            launch(s, l)
+    torch.cuda.synchronize(dev)
+    graphs = []
+    for i0 in range(0, len(order), GRAPH_STEPS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s, l in order[i0:i0 + GRAPH_STEPS]:
+                launch(s, l)
+        graphs.append(g)
+    ms = []
+    for i in range(warmup + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g_pre.replay()
+            e0.record(stream)
+            for g in graphs:
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= warmup:
+            ms.append(e0.elapsed_time(e1))
+    if h2o.h2o_get_device_error(sp) != 0:
+        raise RuntimeError("device error word set during the per-layer decode timing")
+    eb = 2 if w.dtype == "bf16" else 4
+    step_bytes = float(np.mean([w.units * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
+                                           decode_bytes_per_unit(min(P + s, w.budget), D, eb))
+                                for s in range(S)]))
+    us = float(np.median(ms)) * 1000.0 / S
+    kname = decode_kernel(w.with_(layers=1), torch.cuda.get_device_properties(dev).multi_processor_count,
+                          e4m3)[0]
+    peak = measured_peaks()[0]["hbm_gbs"]
+    return {"launches_per_step": L, "units_per_launch": ul, "kernel": kname,
+            "us_per_step": us, "us_per_launch": us / L,
+            "decode_tokens_per_s": w.batch * S / (float(np.median(ms)) / 1000.0),
+            "kv_read_gbs": step_bytes / (us * 1e-6) / 1e9,
+            "frac": step_bytes / (us * 1e-6) / 1e9 / peak,
+            "how": "per step, one h2o_decode_step launch per layer over its batch x heads units, in CUDA "
+                   "graphs; median over the timed replays; cache rebuilt by the prefill between replays "
+                   "(untimed)"}
 
 
 def prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, warmup: int, reps: int) -> dict:
