@@ -20,13 +20,13 @@
 //       victim slot with its score p_new and position                      (H2O post §2.3)
 //
 // Persistent like the bf16 kernel: each CTA walks units blockIdx.x, +gridDim.x, ... The first warps
-// are the epilogue, G groups of four (one warp per TMEM lane quarter; G = 4 for caches up to 256
-// slots, 2 beyond) that take units in turn, each with its own tensor-memory unit slot: with half the
+// are the epilogue, four groups of four warps (one warp per TMEM lane quarter) that take units in
+// turn, each with its own tensor-memory unit slot: with half the
 // bytes per unit, one group's serial chain of reductions and barriers per unit would be slower than
 // the memory system, and more warps hide more latency. The next warp is the producer (all lanes
 // prepare the split query of each unit, lane 0 streams code tiles through a ring of 16 KB tiles in
 // the order the tensor core consumes them), the last allocates tensor memory and issues the MMAs, the
-// logits of unit k before the product of unit k - 2 (four groups) or k - 1 (two). Each group loads
+// logits of unit k before the product of unit k - 2. Each group loads
 // its units' tokens and state a unit ahead. All waits are bounded (mbar_wait); tensor memory is
 // always freed.
 #include <cuda.h>
@@ -55,14 +55,16 @@ constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr uint32_t kPvCol = 64;            // output accumulator column inside a unit slot
 constexpr int kAlign = 1024;
 
-// Per group count G: epilogue groups take units in turn (unit k -> group and tensor-memory slot
-// k % G); four groups for caches of up to two 128-slot tiles, two (with a deeper ring) beyond, where
-// four groups' units would not fit in the ring. Shared-memory offsets are from a 1024-aligned base.
-template <int G>
+// Epilogue groups take units in turn (unit k -> group and tensor-memory slot k % kGroups). One
+// instantiation per largest cache served, NT 128-slot tiles (2 or 4): the smaller one sizes its
+// buffers and register arrays for two tiles. Shared-memory offsets are from a 1024-aligned base.
+constexpr int kGroups = 4;
+template <int NT>
 struct Layout {
-  static constexpr int kTiles = G == 4 ? 2 : kMaxTiles;  // largest cache this instantiation serves
+  static constexpr int G = kGroups;
+  static constexpr int kTiles = NT;                      // largest cache this instantiation serves
   static constexpr int kWBytes = kTiles * kSmallBox;     // w operand: 128 slots per 2 KB box
-  static constexpr int kStages = G == 4 ? 10 : 12;       // streamed 16 KB tiles
+  static constexpr int kStages = 10;                     // streamed 16 KB tiles
   static constexpr int kEpiWarps = G * kGroupWarps;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static constexpr int kTmaWarp = kEpiWarps;
@@ -192,15 +194,15 @@ __device__ __forceinline__ int range_exp(float mx) { return mx > 0.f ? 7 - ilogb
 // Byte offset of code j (0..127 within its 128-byte row) of row `row` in a 128-byte-swizzled box.
 __device__ __forceinline__ int sw_offset(int row, int j) { return row * 128 + ((((j >> 4) ^ row) & 7) << 4) + (j & 15); }
 
-template <bool kAnyPolicy, int kGroups>
-__global__ void __launch_bounds__(Layout<kGroups>::kThreads, 1)
+template <bool kAnyPolicy, int kNT>
+__global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
     h2o_decode_e4m3_kernel(const __grid_constant__ Q8Params p) {
-  using L = Layout<kGroups>;
+  using L = Layout<kNT>;
   // Products issued kLag units behind the logits, so kLag + 1 epilogue groups run their softmax at
   // once; unit k's slot of tensor memory is reused by unit k + kGroups, whose logits follow product
   // k only if kLag < kGroups. The producer loads tiles in the order the tensor core consumes them
   // (unit k's K tiles, then unit k - kLag's V tiles), so ring slots free in order.
-  constexpr int kLag = kGroups == 4 ? 2 : 1;
+  constexpr int kLag = 2;
   static_assert(kLag < kGroups, "a unit's tensor-memory slot must be free before its logits");
   constexpr int kStages = L::kStages, kEpiWarps = L::kEpiWarps, kThreads = L::kThreads;
   constexpr int kTiles = L::kTiles, kWBytes = L::kWBytes;
@@ -749,10 +751,10 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
     for (auto& d : ready)
       if (d.first == dev) sms = d.second;
     if (sms == 0) {
-      for (int g4 = 0; g4 < 2; ++g4)
+      for (int t4 = 0; t4 < 2; ++t4)
         for (int any = 0; any < 2; ++any) {
-          e = cudaFuncSetAttribute(kKernels[g4][any], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   g4 ? Layout<4>::kSmem : Layout<2>::kSmem);
+          e = cudaFuncSetAttribute(kKernels[t4][any], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   t4 ? Layout<4>::kSmem : Layout<2>::kSmem);
           if (e != cudaSuccess) return e;
         }
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -762,8 +764,8 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
   }
   const int grid = dp.units < sms ? dp.units : sms;
   const bool any = dp.policy != H2O_POLICY_H2O;
-  if (p.tiles <= 2) return launch_pdl(kKernels[1][any], grid, Layout<4>::kThreads, Layout<4>::kSmem, stream, &p);
-  return launch_pdl(kKernels[0][any], grid, Layout<2>::kThreads, Layout<2>::kSmem, stream, &p);
+  if (p.tiles <= 2) return launch_pdl(kKernels[0][any], grid, Layout<2>::kThreads, Layout<2>::kSmem, stream, &p);
+  return launch_pdl(kKernels[1][any], grid, Layout<4>::kThreads, Layout<4>::kSmem, stream, &p);
 }
 
 }  // namespace h2o
