@@ -56,6 +56,23 @@ def test_e4m3_many_units_sampled():
     _assert(parity.run(w, check_units=units, state_every=16, e4m3=True))
 
 
+def test_e4m3_per_layer_launch_shape():
+    """One OPT-6.7B layer per launch (256 units: one or two per CTA); 16 sampled."""
+    w = W["opt-6.7b"].with_(layers=1, decode_steps=96)
+    units = np.linspace(0, w.units - 1, 16).astype(int)
+    _assert(parity.run(w, check_units=units, state_every=32, e4m3=True))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,check", [("opt-6.7b", 8), ("llama-7b", 4), ("opt-30b", 6)])
+def test_e4m3_full_size_workload_sampled_units(name, check):
+    """The full workload over the E4M3 cache in the launch shape the benchmark times (both kernel
+    instantiations: two tiles for OPT-6.7B, four for LLaMA-7B and OPT-30B); sampled units."""
+    w = W[name]
+    units = np.linspace(0, w.units - 1, check).astype(int)
+    _assert(parity.run(w, check_units=units, state_every=64, e4m3=True))
+
+
 @pytest.mark.parametrize("policy", [(oracle.POLICY_LOCAL, 0, 1), (oracle.POLICY_SINK_WINDOW, 4, 1),
                                     (oracle.POLICY_TOPK, 0, 1), (oracle.POLICY_STRIDED, 0, 3)])
 def test_e4m3_policies(policy):

@@ -201,6 +201,16 @@ def test_full_size_workload_sampled_units(name, check):
     _assert(parity.run(w, check_units=units, state_every=64))
 
 
+def test_per_layer_launch_shape():
+    """One OPT-6.7B layer per launch (batch 8 x 32 heads = 256 units, k = 204), the shape of the
+    benchmark's per-layer decode timing: fewer than four units per SM, so the cluster-split tcgen05
+    kernel runs; the oracle follows 16 sampled units through every step."""
+    w = W["opt-6.7b"].with_(layers=1, decode_steps=96)
+    assert w.units == 256
+    units = np.linspace(0, w.units - 1, 16).astype(int)
+    _assert(parity.run(w, check_units=units, state_every=32))
+
+
 @pytest.mark.slow
 def test_streaming_full_length_properties_and_prefix_parity():
     """512 + 262144 steps at budget 4096: invariants that hold at any length, checked every 4096
