@@ -122,7 +122,9 @@ def recorded_traffic(workload: str, kernel: str, src: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock / throttle samples every 50 ms while the timed region runs. The sampler is
+    started first and the region is entered only once its first sample is written, so every sample
+    kept falls inside the region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -132,6 +134,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.skip = 0  # samples written before the region
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -139,10 +142,19 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return self
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            with open(self.path) as f:
+                n = sum(1 for _ in f)
+            if n:
+                self.skip = n
+                break
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
@@ -157,9 +169,9 @@ class ClockSampler:
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        for line in open(self.path):
+        for i, line in enumerate(open(self.path)):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if i >= self.skip and len(parts) >= 9:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
