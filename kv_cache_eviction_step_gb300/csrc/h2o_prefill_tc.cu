@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   constexpr int kStages = S::kStages;
   constexpr bool kOut = kMode == kRowOut;
   constexpr bool kCol = kMode == kColSums;
+  constexpr uint32_t kNAcc = kOut ? 2u : 3u;  // logit accumulators (the output pass keeps O at 256..)
   extern __shared__ unsigned char smem_raw[];
   // head: mbarriers, TMEM slot, exchange areas; body (1024-aligned): resident x2, ring, P x2
   unsigned char* head = smem_raw;
@@ -380,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t* ring_full = res_empty + 2;
   uint64_t* ring_empty = ring_full + kStages;
   uint64_t* acc_full = ring_empty + kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* p_full = acc_empty + 2;   // output pass: the epilogue wrote probability tile b
+  uint64_t* acc_empty = acc_full + 3;
+  uint64_t* p_full = acc_empty + 3;   // output pass: the epilogue wrote probability tile b
   uint64_t* p_free = p_full + 2;      // output pass: the product reading probability tile b finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + 2);
   float2* xh = reinterpret_cast<float2*>(head + kCtrlBytes);  // row stats / column sums: [2][kSplit][128]
@@ -391,11 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int P = p.P;
 
   if (tid == 0) {
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&res_full[b], 1);
       mbar_init(&res_empty[b], 1);
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
       mbar_init(&p_full[b], kEpiWarps);
       mbar_init(&p_free[b], 1);
     }
@@ -493,9 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint32_t a_base = smem_u32(res + rb * S::kTileBytes);
         for (int t = 0; t < it.nt; ++t, ++g) {
           const int s = static_cast<int>(r % kStages);
-          const uint32_t a = g & 1u;
+          const uint32_t a = g % kNAcc;
           if (!mbar_wait(&ring_full[s], (r / kStages) & 1u, p.err) ||
-              (g >= 2 && !mbar_wait(&acc_empty[a], (g / 2 - 1) & 1u, p.err))) {
+              (g >= kNAcc && !mbar_wait(&acc_empty[a], (g / kNAcc - 1) & 1u, p.err))) {
             ok = false;
             break;
           }
@@ -557,15 +560,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       float mu = -INFINITY;  // output pass: the maximum the probabilities are taken against
       if constexpr (kCol) qload(it.unit, it.t_begin * kTile + h * kCols + lane);
       for (int t = 0; t < it.nt; ++t, ++g) {
-        const uint32_t a = g & 1u;
+        const uint32_t a = g % kNAcc;  // logit accumulator
+        const uint32_t xa = g & 1u;    // query-statistics buffer
         const int x0 = (it.t_begin + t) * kTile + h * kCols;  // key (query) of this warp's column 0
         if constexpr (kCol) {
           // this tile's query statistics for this warp's columns; prefetch the next tile's
-          xw[a * kCols + lane] = -fmaf(qm, kLog2e, log2f(ql));
+          xw[xa * kCols + lane] = -fmaf(qm, kLog2e, log2f(ql));
           if (t + 1 < it.nt) qload(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
           __syncwarp();
         }
-        if (ok) ok = mbar_wait(&acc_full[a], (g / 2) & 1u, p.err);
+        if (ok) ok = mbar_wait(&acc_full[a], (g / kNAcc) & 1u, p.err);
         tc_fence_after();
         float v[kCols];
         tmem_ld32(lane_addr + a * kTile + h * kCols, v);
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             l += exp2_sum32<false>(v, make_float2(sl, sl), nm, 0);
           }
         } else if constexpr (kCol) {
-          const float4* b4 = reinterpret_cast<const float4*>(xw + a * kCols);
+          const float4* b4 = reinterpret_cast<const float4*>(xw + xa * kCols);
           float nb[kCols];  // this tile's negated query offsets for this warp's columns
 #pragma unroll
           for (int x4 = 0; x4 < kCols / 4; ++x4) {
