@@ -252,6 +252,22 @@ def test_streaming_full_length_properties_and_prefix_parity():
     torch.cuda.synchronize()
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("budget,P,steps", [
+    (6000, 6100, 12),     # n > 4096: the tensor-core step split over 16-CTA clusters
+    (9000, 9100, 12),     # n > 8192: the CUDA-core step
+    (16384, 16384, 4),    # the largest prompt and budget the library takes (cache full from t = P)
+])
+def test_long_caches_and_largest_sizes(budget, P, steps):
+    """One unit (bf16, D = 128) with caches beyond 4096 and 8192 slots and at the size limits: the
+    prefill's selection over long prompts and evicting decode steps, every step checked."""
+    kh = budget // 2
+    w = W["streaming"].with_(heads=1, prompt_len=P, decode_steps=steps, budget=budget, k_heavy=kh,
+                             k_local=budget - kh)
+    assert w.units == 1
+    _assert(parity.run(w, state_every=4))
+
+
 def test_long_prompt_column_sums_and_selection():
     """A 4096-token prompt (32 tiles of 128 rows per unit) on the tensor-core passes: every column sum
     against the oracle, the kept slot map, and a few decode steps."""
