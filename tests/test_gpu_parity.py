@@ -252,6 +252,18 @@ def test_streaming_full_length_properties_and_prefix_parity():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("units,e4m3", [(151, False), (152, False), (153, False), (607, False), (608, False),
+                                         (609, False), (151, True), (152, True), (153, True)])
+def test_unit_counts_around_the_dispatch_and_grid_boundaries(units, e4m3):
+    """Unit counts on both sides of one unit per SM (152: the persistent kernels' grid) and of four
+    per SM (608: where the bf16 step moves from the cluster-split to the persistent kernel), with the
+    OPT-6.7B budget; the first, last and middle units checked through every step."""
+    w = W["opt-6.7b"].with_(layers=1, batch=units, heads=1, decode_steps=24)
+    assert w.units == units
+    check = [0, units // 2, units - 1]
+    _assert(parity.run(w, check_units=check, state_every=8, e4m3=e4m3))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("budget,P,steps", [
     (6000, 6100, 12),     # n > 4096: the tensor-core step split over 16-CTA clusters
