@@ -43,6 +43,14 @@
  * H2O_ERR_CUDA. Conditions detected on the device (a bounded wait that ran out) are recorded in the
  * device error word and reported by h2o_get_device_error. No C++ exception crosses this ABI.
  * Calls that overlap on the GPU and touch the same cache race; order them on one stream.
+ *
+ * Decode steps are launched with programmatic dependent launch: a step may start while the kernel
+ * before it on the stream finishes, and waits for it before reading anything that kernel may write.
+ * When the previous decode step launched on the same stream wrote none of this call's cache arrays
+ * (one launch per layer: consecutive launches belong to different layers), the step may load its
+ * cached K/V rows before that wait. Precondition for that case: a kernel of the caller's that sits
+ * between two decode calls on the stream and itself signals programmatic completion early must
+ * not write the second call's cache (ordinary kernels, which do not signal early, are always safe).
  */
 #ifndef H2O_H
 #define H2O_H

@@ -301,6 +301,46 @@ h2o_status h2o_prefill_forward(const h2o_dims* dims, const h2o_policy* policy, i
                              workspace, workspace_bytes, stream, out);
 }
 
+// The launch of one decode step on the kernel its shape calls for.
+static h2o_status dispatch_decode(DecodeParams& p, const h2o_dims* dims, void* stream) {
+  // E4M3 caches: the tensor-core kernel over 8-bit tiles (bf16, D = 128, budgets up to 512).
+  if (p.k_scale != nullptr) return from_cuda(launch_decode_e4m3(p, static_cast<cudaStream_t>(stream)));
+  // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
+  // over units. Other shapes (fp32, D = 64, caches beyond 8192 slots) use the CUDA-core kernel, each
+  // unit split over a CTA cluster when units are few.
+  if (decode_tc_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= 4 * sm_count())
+    return from_cuda(launch_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  // Fewer bf16 units of D = 128 (or longer caches): the tensor-core step split over a CTA cluster.
+  if (decode_tc_split_supported(dims->head_dim, dims->dtype, p.units, p.n))
+    return from_cuda(launch_decode_tc_split(p, static_cast<cudaStream_t>(stream)));
+  size_t smem = 0;
+  if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem,
+                   &p.grid))
+    return H2O_ERR_UNSUPPORTED;
+  return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+// Per (device, stream), the device memory the last decode launch on that stream writes. A decode
+// kernel may start its cache reads before waiting for the previous grid only if that grid writes
+// none of them; with every decode kernel signalling its dependents after its own wait, all earlier
+// launches have completed by then (launches that signal nothing let the next one start only when
+// they complete).
+struct Span {
+  uintptr_t lo, hi;
+};
+struct LastDecode {
+  int dev;
+  void* stream;
+  Span w[9];
+};
+std::mutex g_decode_mu;
+std::vector<LastDecode> g_last_decode;
+
+Span span_of(const void* ptr, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  return {a, ptr == nullptr ? a : a + bytes};
+}
+
 static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* policy,
                                    int32_t position, const void* q, const void* k_new,
                                    const void* v_new, void* k_cache, void* v_cache, float* scores,
@@ -345,21 +385,38 @@ static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* polic
   p.stride = pol.kind == H2O_POLICY_STRIDED ? pol.stride : 1;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  // E4M3 caches: the tensor-core kernel over 8-bit tiles (bf16, D = 128, budgets up to 512).
-  if (k_scale != nullptr) return from_cuda(launch_decode_e4m3(p, static_cast<cudaStream_t>(stream)));
-  // Many bf16 units of D = 128 with budgets up to 512 slots: both contractions on tcgen05, persistent
-  // over units. Other shapes (fp32, D = 64, caches beyond 8192 slots) use the CUDA-core kernel, each
-  // unit split over a CTA cluster when units are few.
-  if (decode_tc_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= 4 * sm_count())
-    return from_cuda(launch_decode_tc(p, static_cast<cudaStream_t>(stream)));
-  // Fewer bf16 units of D = 128 (or longer caches): the tensor-core step split over a CTA cluster.
-  if (decode_tc_split_supported(dims->head_dim, dims->dtype, p.units, p.n))
-    return from_cuda(launch_decode_tc_split(p, static_cast<cudaStream_t>(stream)));
-  size_t smem = 0;
-  if (!plan_decode(p.units, p.n, dims->head_dim, elem_bytes(dims), &p.splits, &p.chunk, &p.stages, &smem,
-                   &p.grid))
-    return H2O_ERR_UNSUPPORTED;
-  return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
+
+  // This call's cache arrays (read, and written in place) and its outputs.
+  const size_t slots = static_cast<size_t>(p.units) * static_cast<size_t>(dims->budget);
+  const size_t row_bytes = static_cast<size_t>(dims->head_dim) * (k_scale != nullptr ? 1 : elem_bytes(dims));
+  const size_t units = static_cast<size_t>(p.units);
+  LastDecode mine = {0, stream,
+                     {span_of(k_cache, slots * row_bytes), span_of(v_cache, slots * row_bytes),
+                      span_of(scores, slots * 4), span_of(slot_pos, slots * 4), span_of(k_scale, slots * 4),
+                      span_of(v_scale, slots * 4), span_of(out, units * dims->head_dim * elem_bytes(dims)),
+                      span_of(evicted_slot, units * 4), span_of(evicted_pos, units * 4)}};
+  if (cudaGetDevice(&mine.dev) != cudaSuccess) return from_cuda(cudaGetLastError());
+  std::lock_guard<std::mutex> lock(g_decode_mu);
+  LastDecode* prev = nullptr;
+  for (auto& l : g_last_decode)
+    if (l.dev == mine.dev && l.stream == stream) prev = &l;
+  p.early = 0;
+  if (prev != nullptr) {
+    bool disjoint = true;
+    for (int i = 0; i < 6; ++i)  // the cache arrays
+      for (const Span& w : prev->w)
+        if (mine.w[i].lo < w.hi && w.lo < mine.w[i].hi) disjoint = false;
+    p.early = disjoint ? 1 : 0;
+  }
+  const h2o_status st_launch = dispatch_decode(p, dims, stream);
+  if (st_launch == H2O_OK) {
+    if (prev != nullptr) *prev = mine;
+    else g_last_decode.push_back(mine);
+  } else if (prev != nullptr) {
+    *prev = LastDecode{mine.dev, stream, {}};  // unknown: treat every range as possibly written
+    for (Span& w : prev->w) w = Span{0, ~uintptr_t(0)};
+  }
+  return st_launch;
 }
 
 h2o_status h2o_decode_step(const h2o_dims* dims, int32_t position, const void* q,

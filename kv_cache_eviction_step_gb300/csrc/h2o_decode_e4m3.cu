@@ -96,6 +96,7 @@ struct Q8Params {
   int32_t units, budget, k_local, position, n, tiles;
   float scale;
   int32_t policy, n_sink, stride;
+  int32_t early;  // the previous decode launch wrote none of this cache: tiles may load before the wait
 };
 
 // ---- PTX wrappers --------------------------------------------------------------------------------
@@ -210,7 +211,6 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
   constexpr uint32_t kTmemCols = L::kTmemCols;
   constexpr int kRingOff = 0, kQOff = L::kQOff, kWOff = L::kWOff, kCtrlOff = L::kCtrlOff;
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
-  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
@@ -259,11 +259,28 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the previous step's cache, scales, scores and slot map are complete from here on
+  // With p.early the producer's lane 0 loads the first ring tiles before the wait (the previous
+  // launch on the stream writes none of this cache); everything else waits for the previous grid.
+  const bool early_tiles = p.early != 0 && warp == kTmaWarp && lane == 0;
+  if (!early_tiles) {
+    pdl_wait();  // the previous step's cache, scales, scores and slot map are complete from here on
+    pdl_launch_dependents();
+  }
 
   if (warp == kTmaWarp) {
     // Producer: every lane splits four query elements (d = 4 lane .. 4 lane + 3); lane 0 streams.
-    uint32_t g = 0;  // ring tiles issued
+    uint32_t g = 0;      // ring tiles issued (position in the consumption order)
+    uint32_t g_pre = 0;  // tiles loaded before the wait
+    if (early_tiles) {
+      // The first unit's K tiles, the head of the consumption order (loading more of it before the
+      // wait measured slower: it slows the previous launch's last units more than it saves).
+      for (int t = 0; t < T; ++t, ++g_pre) {
+        mbar_expect_tx(&full[g_pre], kTileBytes);
+        tma_load_3d(ring + g_pre * kTileBytes, &p.tm_k, 0, t * kTileRows, blockIdx.x, &full[g_pre]);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+    }
     int k = 0;
     bool ok = true;
     uint2 qn = make_uint2(0, 0);  // the next unit's four bf16 query elements
@@ -312,6 +329,7 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
         const int vu = u - kLag * static_cast<int>(gridDim.x);
         const int nt = k < kLag ? T : 2 * T;
         for (int i = 0; i < nt; ++i, ++g) {
+          if (g < g_pre) continue;  // loaded before the wait
           const int s = static_cast<int>(g % kStages);
           if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
             ok = false;
@@ -329,6 +347,7 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
     for (int j = k - kLag < 0 ? 0 : k - kLag; lane == 0 && ok && j < k; ++j) {
       const int vu = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
       for (int t = 0; t < T; ++t, ++g) {
+        if (g < g_pre) continue;  // loaded before the wait
         const int s = static_cast<int>(g % kStages);
         if (g >= kStages && !mbar_wait(&empty[s], (g / kStages - 1) & 1u, p.err)) {
           ok = false;
@@ -739,6 +758,7 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
   p.policy = dp.policy;
   p.n_sink = dp.n_sink;
   p.stride = dp.stride;
+  p.early = dp.early;
 
   static std::mutex mu;
   static std::vector<std::pair<int, int>> ready;  // (device, SM count)

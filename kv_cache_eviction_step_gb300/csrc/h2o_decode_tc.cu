@@ -78,6 +78,7 @@ struct TcDecodeParams {
   int32_t units, budget, k_local, position, n, tiles;
   float scale;
   int32_t policy, n_sink, stride;  // eviction policy (h2o_policy_kind)
+  int32_t early;                   // cache reads may start before griddepcontrol.wait (DecodeParams)
 };
 
 // ---- PTX wrappers (same encodings as the prefill's tcgen05 path) -------------------------------
@@ -171,7 +172,6 @@ __device__ __forceinline__ int w_offset(int j, int row) {
 template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid_constant__ TcDecodeParams p) {
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
-  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem + kRingOff;
@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
+  pdl_launch_dependents();
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
@@ -604,7 +605,6 @@ template <bool kAnyPolicy>
 __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const __grid_constant__ TcSplitParams sp_) {
   const TcDecodeParams& p = sp_.d;
   const int32_t policy = kAnyPolicy ? p.policy : static_cast<int32_t>(H2O_POLICY_H2O);
-  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   unsigned char* ring = smem;
@@ -655,22 +655,38 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
   cluster_sync_all();  // every CTA's exchange barriers exist before any peer arrives on them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
+  // With p.early the producer's first cache tiles go out before the wait (the previous launch on
+  // the stream writes none of this call's cache); everything else waits for the previous grid.
+  const bool early_tiles = p.early != 0 && warp == kTmaWarp && lane == 0;
+  if (!early_tiles) {
+    pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
+    pdl_launch_dependents();
+  }
   const size_t row0 = static_cast<size_t>(unit) * p.budget;
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      mbar_expect_tx(q_full, 2 * 128);
-      tma_load_2d(qbuf, &p.tm_q, 0, unit, q_full);
-      tma_load_2d(qbuf + kNarrowBox, &p.tm_q, 64, unit, q_full);
-      for (int i = 0; i < 2 * T; ++i) {
+      auto tile = [&](int i) {  // ring tile i: K tiles 0..T-1, then V tiles
         const int s = i % kSplitStages;
-        if (i >= kSplitStages && !mbar_wait(&empty[s], static_cast<uint32_t>(i / kSplitStages - 1) & 1u, p.err)) break;
         const CUtensorMap* map = i < T ? &p.tm_k : &p.tm_v;
         const int r0 = c0 + (i < T ? i : i - T) * kTileRows;
         mbar_expect_tx(&full[s], kTileBytes);
         tma_load_3d(ring + s * kTileBytes, map, 0, r0, unit, &full[s]);
         tma_load_3d(ring + s * kTileBytes + kBox, map, 64, r0, unit, &full[s]);
+      };
+      int i = 0;
+      if (early_tiles) {
+        for (; i < 2 * T && i < kSplitStages; ++i) tile(i);
+        pdl_wait();
+        pdl_launch_dependents();
+      }
+      mbar_expect_tx(q_full, 2 * 128);
+      tma_load_2d(qbuf, &p.tm_q, 0, unit, q_full);
+      tma_load_2d(qbuf + kNarrowBox, &p.tm_q, 64, unit, q_full);
+      for (; i < 2 * T; ++i) {
+        const int s = i % kSplitStages;
+        if (i >= kSplitStages && !mbar_wait(&empty[s], static_cast<uint32_t>(i / kSplitStages - 1) & 1u, p.err)) break;
+        tile(i);
       }
     }
     __syncwarp();
@@ -989,6 +1005,7 @@ cudaError_t fill_params(const DecodeParams& dp, TcDecodeParams& p) {
   p.policy = dp.policy;
   p.n_sink = dp.n_sink;
   p.stride = dp.stride;
+  p.early = dp.early;
   return cudaSuccess;
 }
 

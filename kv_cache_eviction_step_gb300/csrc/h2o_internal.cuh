@@ -39,6 +39,8 @@ struct DecodeParams {
   int32_t stride;       // strided
   float* k_scale;       // E4M3 caches: [units, budget] per-row scales
   float* v_scale;
+  int32_t early;        // the previous decode launch on this stream wrote none of this call's cache
+                        // arrays: their reads may start before griddepcontrol.wait
 };
 
 struct PrefillParams {
@@ -217,7 +219,9 @@ __device__ __forceinline__ unsigned long long policy_key(int32_t policy, float s
 
 // Programmatic dependent launch: the next kernel in the stream may start its prologue once every
 // CTA of this one has signalled; it waits for this grid's completion (and memory) before touching
-// the data this grid writes.
+// the data this grid writes. Every decode kernel signals only after its own wait has returned, so
+// while a launch runs, every launch before its predecessor has completed: data that the predecessor
+// does not write may be read before the wait.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -252,6 +252,52 @@ def test_streaming_full_length_properties_and_prefix_parity():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_layer_interleaved_steps_match_one_cache_at_a_time(e4m3):
+    """Per-layer decoding: two caches (two layers of 256 units, k = 204) stepped alternately on one
+    stream, so that every launch may load its cache before the previous launch (the other layer's)
+    has finished, give outputs, evictions and cache state bit-identical to stepping one cache at a
+    time (where consecutive launches share a cache and each waits for the last)."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    w = W["opt-6.7b"].with_(layers=1, decode_steps=40)
+    dims = parity.dims_of(w)
+    keys = ("q_prompt", "k_prompt", "v_prompt", "q_dec", "k_dec", "v_dec")
+    dev = []
+    for i in range(2):
+        inp = synth.generate(w, seed=synth.DEFAULT_SEED + 101 * i)
+        dev.append({k: parity.to_device(getattr(inp, k), w.dtype) for k in keys})
+    S, U, D = w.decode_steps, w.units, w.head_dim
+
+    def run(interleaved):
+        caches = [h2o.H2OCache(dims, w.prompt_len, e4m3=e4m3) for _ in range(2)]
+        outs = [torch.empty((S, U, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        evs = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(2)]
+        evp = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(2)]
+        for c, d in zip(caches, dev):
+            c.prefill(d["q_prompt"], d["k_prompt"], d["v_prompt"])
+        order = ([(s, l) for s in range(S) for l in range(2)] if interleaved else
+                 [(s, l) for l in range(2) for s in range(S)])
+        for s, l in order:
+            d = dev[l]
+            caches[l].step(d["q_dec"][s], d["k_dec"][s], d["v_dec"][s], out=outs[l][s],
+                           evicted_slot=evs[l][s], evicted_pos=evp[l][s])
+        torch.cuda.synchronize()
+        got = outs + evs + evp
+        for c in caches:
+            got += [c.k_cache, c.v_cache, c.scores, c.slot_pos]
+            if e4m3:
+                got += [c.k_scale, c.v_scale]
+        return got
+
+    a, b = run(True), run(False)
+    assert len(a) == len(b)
+    for i, (x, y) in enumerate(zip(a, b)):
+        assert torch.equal(x, y), i
+    assert h2o.h2o_get_device_error() == 0
+
+
 @pytest.mark.parametrize("units,e4m3", [(151, False), (152, False), (153, False), (607, False), (608, False),
                                          (609, False), (151, True), (152, True), (153, True)])
 def test_unit_counts_around_the_dispatch_and_grid_boundaries(units, e4m3):
