@@ -293,7 +293,11 @@ def config_of(w: synth.Workload, args) -> dict:
                          else w.dtype),
             "l2": "no flush: KV cache and per-step inputs exceed the 129 MB L2",
             "timing": "CUDA events between replays of two CUDA graphs per job (3 prefill launches, "
-                      "then the decode launches)"}
+                      "then the decode launches)",
+            "decode_launch": (f"one launch per step over all {w.units} units ({w.layers} layers x "
+                              f"{w.batch} x {w.heads} heads); one launch per layer per step is timed "
+                              f"separately as decode_per_layer" if w.layers > 1 else
+                              f"one launch per step over all {w.units} units")}
 
 
 def main():
