@@ -46,11 +46,13 @@
  *
  * Decode steps are launched with programmatic dependent launch: a step may start while the kernel
  * before it on the stream finishes, and waits for it before reading anything that kernel may write.
- * When the previous decode step launched on the same stream wrote none of this call's cache arrays
- * (one launch per layer: consecutive launches belong to different layers), the step may load its
- * cached K/V rows before that wait. Precondition for that case: a kernel of the caller's that sits
- * between two decode calls on the stream and itself signals programmatic completion early must
- * not write the second call's cache (ordinary kernels, which do not signal early, are always safe).
+ * When the library's previous launch on the same stream was a decode step that wrote none of this
+ * call's cache arrays (one launch per layer: consecutive launches belong to different layers), the
+ * step may load its cached K/V rows before that wait. Any other launch of the library on the stream
+ * (a prefill call, the self-test) cancels this for the next decode step, which then waits before
+ * its first read. Precondition for the early case: a kernel of the caller's that sits between two
+ * decode calls on the stream and itself signals programmatic completion early must not write the
+ * second call's cache (ordinary kernels, which do not signal early, are always safe).
  */
 #ifndef H2O_H
 #define H2O_H
@@ -158,14 +160,23 @@ H2O_API h2o_status h2o_prefill_select(const h2o_dims* dims, int32_t prompt_len, 
  * (for example a serving engine that reserved all device memory for its own pool at start-up, or a
  * plugin running inside a host framework that owns the allocator and hands it only the tensors it
  * declared). The H2O pages have no counterpart: this is a deployment convenience. The scratch lives
- * in one device array of H2O_STATIC_SCRATCH_BYTES inside this library, which every GPU that loads the
- * library holds until the process exits; nothing is allocated or freed by the call.
+ * in one device array of H2O_STATIC_SCRATCH_BYTES inside this library, which a GPU holds from the
+ * moment the library's device code is loaded on it (see below) until the process exits; nothing is
+ * allocated or freed by the call.
  *   - Same arguments, results and errors as h2o_prefill_select, minus the workspace.
  *   - Limit: h2o_prefill_workspace_bytes(dims, prompt_len) <= H2O_STATIC_SCRATCH_BYTES, i.e.
  *     units * prompt_len <= 1,398,080 (e.g. 2048 units with 512-token prompts); larger calls return
  *     H2O_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *     that device current); make that first call before any stream capture.
+ *   - When its memory is taken: the array sits in the library's device code, which the CUDA runtime
+ *     loads into a device's memory when that code is first needed there. Under the default lazy
+ *     module loading that is the first h2o_prefill_select_static call on the device (the address
+ *     lookup loads it), not the moment the library is loaded. A caller that is about to reserve
+ *     all device memory for its own pool should therefore make one call (any valid shape) before
+ *     reserving, or run with CUDA_MODULE_LOADING=EAGER so the array is placed when the CUDA context
+ *     is created; otherwise that first call can fail with H2O_ERR_CUDA (out of memory, see
+ *     h2o_last_cuda_error).
  *   - Every call on a device shares the one array, which keeps the last call's contents (no array
  *     has to start at zero: each is fully written before it is read). Calls that overlap on the
  *     GPU, on different streams or from different threads, race on it: order them on one stream.

@@ -140,6 +140,42 @@ size_t h2o_prefill_workspace_bytes(const h2o_dims* dims, int32_t prompt_len) {
   return 3 * round256(units * static_cast<size_t>(prompt_len) * 4);
 }
 
+// Per (device, stream), the device memory the last launch of this library on that stream may
+// write. A decode kernel may start its cache reads before waiting for the previous grid only if
+// that grid writes none of them; with every decode kernel signalling its dependents after its own
+// wait, all earlier launches have completed by then (launches that signal nothing let the next one
+// start only when they complete). Any other launch of the library (a prefill, the self-test) marks
+// all memory as possibly written, so the decode launch after it always waits before its first read.
+struct Span {
+  uintptr_t lo, hi;
+};
+struct LastDecode {
+  int dev;
+  void* stream;
+  Span w[9];
+};
+static std::mutex g_decode_mu;
+static std::vector<LastDecode> g_last_decode;
+
+static Span span_of(const void* ptr, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  return {a, ptr == nullptr ? a : a + bytes};
+}
+
+// Records that a launch other than a decode step was enqueued on `stream` of the current device.
+static void note_other_launch(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    dev = -1;
+  }
+  std::lock_guard<std::mutex> lock(g_decode_mu);
+  for (auto& l : g_last_decode) {
+    if (l.stream != stream || (dev >= 0 && l.dev != dev)) continue;
+    for (Span& w : l.w) w = Span{0, ~uintptr_t(0)};
+  }
+}
+
 static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, const void* q,
                                       const void* k, float* colsum, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream,
@@ -162,6 +198,7 @@ static h2o_status prefill_scores_impl(const h2o_dims* dims, int32_t prompt_len, 
   p.v = v;
   p.out = out;
   (void)workspace_bytes;
+  note_other_launch(stream);
   // bf16: tcgen05 tensor cores (bf16 x bf16 products are exact in the fp32 accumulator); fp32 stays
   // on the CUDA cores, where the products are not rounded to tf32.
   if (dims->dtype == H2O_BF16) return from_cuda(launch_prefill_scores_tc(p, dims->head_dim, stream));
@@ -320,27 +357,6 @@ static h2o_status dispatch_decode(DecodeParams& p, const h2o_dims* dims, void* s
   return from_cuda(launch_decode(p, dims->head_dim, dims->dtype, static_cast<cudaStream_t>(stream)));
 }
 
-// Per (device, stream), the device memory the last decode launch on that stream writes. A decode
-// kernel may start its cache reads before waiting for the previous grid only if that grid writes
-// none of them; with every decode kernel signalling its dependents after its own wait, all earlier
-// launches have completed by then (launches that signal nothing let the next one start only when
-// they complete).
-struct Span {
-  uintptr_t lo, hi;
-};
-struct LastDecode {
-  int dev;
-  void* stream;
-  Span w[9];
-};
-std::mutex g_decode_mu;
-std::vector<LastDecode> g_last_decode;
-
-Span span_of(const void* ptr, size_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
-  return {a, ptr == nullptr ? a : a + bytes};
-}
-
 static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* policy,
                                    int32_t position, const void* q, const void* k_new,
                                    const void* v_new, void* k_cache, void* v_cache, float* scores,
@@ -450,6 +466,7 @@ h2o_status h2o_decode_step_e4m3(const h2o_dims* dims, const h2o_policy* policy, 
 h2o_status h2o_selftest_wait_timeout(void* stream) {
   int32_t* word = error_word();
   if (word == nullptr) return from_cuda(cudaGetLastError());
+  note_other_launch(stream);
   wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word, 50000000ull);
   return from_cuda(cudaGetLastError());
 }

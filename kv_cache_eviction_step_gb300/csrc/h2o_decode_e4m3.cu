@@ -180,15 +180,6 @@ __device__ __forceinline__ float e4m3_value(uint8_t c) {
   return __half2float(__half(h));
 }
 
-constexpr float kLog2e = 1.4426950408889634f;
-
-// 2^x by the special-function unit (ex2.approx, relative error ~2^-22; 2^-inf = 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Power-of-two exponent that brings a positive maximum into [128, 256) (0 for an all-zero vector).
 __device__ __forceinline__ int range_exp(float mx) { return mx > 0.f ? 7 - ilogbf(mx) : 0; }
 
@@ -524,11 +515,10 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
       const float vsmax = fmaxf(fmaxf(r1[4], r1[5]), fmaxf(r1[6], r1[7]));
       const float kamax = fmaxf(fmaxf(r1[8], r1[9]), fmaxf(r1[10], r1[11]));
       const float vamax = fmaxf(fmaxf(r1[12], r1[13]), fmaxf(r1[14], r1[15]));
-      // Logits in log2 units (the exponentials below are 2^x): ks_j 2^-kq (1/sqrt(D)) log2(e).
-      const float qinv = ldexpf(1.f, -range_exp(qmax)) * p.scale * kLog2e;
-      const float s_new2 = s_new * kLog2e;
+      // Logits: the tensor core's sum times ks_j 2^-kq (1/sqrt(D)).
+      const float qinv = ldexpf(1.f, -range_exp(qmax)) * p.scale;
       float s[kTiles];
-      float m = s_new2;
+      float m = s_new;
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
         s[t] = -INFINITY;
@@ -552,7 +542,7 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
         if (t < T) {
-          e[t] = ex2(s[t] - m);  // 0 for -inf (slots past n)
+          e[t] = expf(s[t] - m);  // accurate exp (the score increments); 0 for slots past n
           lsum += e[t];
           const float w = e[t] * vs[t] * cw;
           const uint8_t c1 = e4m3(w);
@@ -568,7 +558,7 @@ __global__ void __launch_bounds__(Layout<kNT>::kThreads, 1)
         }
       }
       fence_async_smem();
-      const float w_new = ex2(s_new2 - m);
+      const float w_new = expf(s_new - m);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
       if (lane == 0) rl[gwarp] = lsum;

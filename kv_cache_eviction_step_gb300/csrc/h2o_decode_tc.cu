@@ -573,7 +573,8 @@ __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cl
 
 // Bounded wait with cluster-scope acquire: data that peers stored before their release-arrive on
 // this barrier is visible afterwards.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                  uint64_t limit_ns = 2000000000ull) {
   const uint32_t addr = smem_u32(bar);
   uint64_t start = 0;
   for (uint32_t it = 0;; ++it) {
@@ -588,7 +589,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if ((it & 3u) == 0) {
       const uint64_t now = global_timer_ns();
       if (it == 0) start = now;
-      else if (now - start > 2000000000ull) {
+      else if (now - start > limit_ns) {
         atomicCAS(err, H2O_DEVERR_NONE, H2O_DEVERR_WAIT_TIMEOUT);
         return false;
       }
@@ -909,6 +910,12 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
       p.evicted_slot[unit] = cache_full ? victim : -1;
       p.evicted_pos[unit] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
     }
+    // Every peer stores into this CTA's exchange buffers before it arrives on xbar[1], and every
+    // peer always reaches that arrival (its own waits are bounded). If a wait above gave up, a late
+    // peer may still be on its way, so this CTA must not exit yet: thread 0 waits for all arrivals
+    // on xbar[1] (a second, longer bounded window; an immediate return on the normal path), and
+    // the block barrier below holds the whole CTA until then.
+    if (tid == 0) (void)mbar_wait_cluster(&xbar[1], 0, p.err, 8000000000ull);
   }
 
   tc_fence_before();

@@ -15,13 +15,7 @@ W = synth.WORKLOADS
 
 
 def _assert(rep: parity.Report):
-    msg = (f"{rep.workload}: {rep.mismatches} mismatches / {rep.decisions} decisions, "
-           f"near ties {rep.near_ties}, error-bound ties {rep.error_bound_ties}, prefill "
-           f"mismatches {rep.prefill_mismatches}, max out err {rep.max_out_err:.2e}, max score rel "
-           f"err {rep.max_score_rel_err:.2e}, notes {rep.notes}")
-    print(msg)
-    assert rep.ok(), msg
-    assert rep.error_bound_ties <= max(2, rep.decisions // 1000), msg
+    parity.check(rep)
 
 
 @pytest.fixture(scope="module", autouse=True)

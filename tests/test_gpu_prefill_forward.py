@@ -15,12 +15,7 @@ W = synth.WORKLOADS
 
 
 def _assert(rep: parity.Report):
-    msg = (f"{rep.workload}: prefill out err {rep.max_prefill_out_err:.2e}, {rep.mismatches} mismatches / "
-           f"{rep.decisions} decisions, prefill mismatches {rep.prefill_mismatches}, max out err "
-           f"{rep.max_out_err:.2e}, notes {rep.notes}")
-    print(msg)
-    assert rep.ok(), msg
-    assert rep.error_bound_ties <= max(2, rep.decisions // 1000), msg
+    parity.check(rep)
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -54,9 +54,38 @@ def test_static_scratch_prefill_matches_workspace_entry_point():
         got = _state(w)
         h2o.h2o_prefill_select_static(dims, w.prompt_len, q, k, v, *got)
         torch.cuda.synchronize()
+        # The first call on the device looks the array up (and so loads the module that holds it):
+        # it must leave no CUDA error behind.
+        assert h2o.last_cuda_error() == "cudaSuccess"
         for a, b in zip(ref, got):
             assert torch.equal(a, b), w.name
         assert h2o.h2o_get_device_error() == 0
+
+
+def test_static_scratch_call_allocates_no_device_memory():
+    """Once every shape below has run once (its kernels are loaded), further calls of all of them
+    leave the device's free memory exactly where it was: the entry point allocates nothing."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    calls = []
+    for w in (synth.WORKLOADS["opt-6.7b"].with_(layers=1, batch=2, heads=8),
+              synth.WORKLOADS["llama-7b"].with_(batch=1, heads=5),
+              synth.WORKLOADS["opt-30b"].with_(batch=1, heads=7, prompt_len=333),
+              synth.WORKLOADS["tiny"]):
+        inp = synth.generate(w, steps=0)
+        calls.append((_dims(h2o, w), w.prompt_len, _dev(inp.q_prompt), _dev(inp.k_prompt),
+                      _dev(inp.v_prompt), _state(w)))
+    for dims, P, q, k, v, st in calls:  # warm-up: every kernel these shapes use is loaded
+        h2o.h2o_prefill_select_static(dims, P, q, k, v, *st)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        for dims, P, q, k, v, st in calls:
+            h2o.h2o_prefill_select_static(dims, P, q, k, v, *st)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert h2o.h2o_get_device_error() == 0
 
 
 def test_static_scratch_rejects_oversized_calls():
