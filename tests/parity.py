@@ -154,16 +154,7 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
         _, pinfo = orc.prefill_select(prompt.q_prompt[check_units], prompt.k_prompt[check_units],
                                       prompt.v_prompt[check_units], st, prefer_pos=gpu_pos,
                                       tie_rel=TIE_REL, err_rel=ERR_REL)
-        for j, i in enumerate(pinfo):
-            rep.prefill_near_ties += i.kind == oracle.NEAR_TIE
-            rep.prefill_error_bound += i.kind == oracle.ERROR_BOUND
-            rep.prefill_mismatches += i.kind == oracle.REJECTED
-            if i.kind == oracle.NEAR_TIE or (i.kind == oracle.RULE and 0 < i.gap_rel < TIE_REL):
-                rep.near_tie_log.append(("prefill", int(check_units[j]), float(i.gap_rel),
-                                         i.kind == oracle.NEAR_TIE))
-            if i.kind == oracle.REJECTED and len(rep.notes) < 10:
-                rep.notes.append(f"prefill unit {check_units[j]}: kept set differs "
-                                 f"(boundary gap {i.gap_rel:.2e})")
+        compare_prefill(rep, pinfo, check_units)
         compare_state(rep, w, cache, st, check_units, 0)
     del prompt
 
@@ -193,30 +184,8 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
                 t, chunk.q_dec[s][check_units], chunk.k_dec[s][check_units],
                 chunk.v_dec[s][check_units], st, prefer_victim=evs_h[s][check_units],
                 tie_rel=TIE_REL, err_rel=ERR_REL)
-            e = float(np.max(np.abs(outs_h[s] - o_out)))
-            rep.max_out_err = max(rep.max_out_err, e)
-            if e > OUT_TOL[w.dtype] and len(rep.notes) < 10:
-                rep.notes.append(f"t={t}: output error {e:.3e}")
-            for j, inf in enumerate(infos):
-                if inf.kind == oracle.NO_EVICTION:
-                    if evs_h[s][check_units[j]] != -1 or evp_h[s][check_units[j]] != -1:
-                        rep.mismatches += 1
-                    continue
-                rep.decisions += 1
-                rep.near_ties += inf.kind == oracle.NEAR_TIE
-                rep.error_bound_ties += inf.kind == oracle.ERROR_BOUND
-                if inf.kind == oracle.NEAR_TIE or (inf.kind == oracle.RULE and 0 < inf.gap_rel < TIE_REL):
-                    rep.near_tie_log.append((t, int(check_units[j]), float(inf.gap_rel),
-                                             inf.kind == oracle.NEAR_TIE))
-                elif inf.kind == oracle.RULE and inf.gap_rel > 0:
-                    rep.min_decision_gap = min(rep.min_decision_gap, float(inf.gap_rel))
-                if inf.kind == oracle.REJECTED or o_ep[j] != evp_h[s][check_units[j]] \
-                        or o_es[j] != evs_h[s][check_units[j]]:
-                    rep.mismatches += 1
-                    if len(rep.notes) < 10:
-                        rep.notes.append(f"t={t} unit {check_units[j]}: gpu victim "
-                                         f"{evs_h[s][check_units[j]]}, oracle {o_es[j]} "
-                                         f"(kind {oracle.KIND_NAMES[inf.kind]}, gap {inf.gap_rel:.2e})")
+            compare_step(rep, w.dtype, t, check_units, outs_h[s], evs_h[s][check_units],
+                         evp_h[s][check_units], o_out, o_es, o_ep, infos)
         if follow and state_every:
             compare_state(rep, w, cache, st, check_units, s0 + ns)
         if property_checks is not None:
@@ -228,27 +197,203 @@ def run(w: synth.Workload, check_units=None, steps: int | None = None, seed: int
     return rep
 
 
+def compare_prefill(rep: Report, pinfo, units) -> None:
+    """The prefill's kept sets: exact, except at a logged near tie (< TIE_REL) at the boundary."""
+    for j, i in enumerate(pinfo):
+        rep.prefill_near_ties += i.kind == oracle.NEAR_TIE
+        rep.prefill_error_bound += i.kind == oracle.ERROR_BOUND
+        rep.prefill_mismatches += i.kind == oracle.REJECTED
+        if i.kind == oracle.NEAR_TIE or (i.kind == oracle.RULE and 0 < i.gap_rel < TIE_REL):
+            rep.near_tie_log.append(("prefill", int(units[j]), float(i.gap_rel),
+                                     i.kind == oracle.NEAR_TIE))
+        if i.kind == oracle.REJECTED and len(rep.notes) < 10:
+            rep.notes.append(f"prefill unit {units[j]}: kept set differs (boundary gap {i.gap_rel:.2e})")
+
+
+def run_segments(w: synth.Workload, check_units, seg_len: int, seed: int = synth.DEFAULT_SEED,
+                 chunk_steps: int = 4096, property_checks=None, threads: int | None = None) -> Report:
+    """Every decode step of a long run checked against the oracle, with the oracle's work spread over
+    the host's cores. The GPU runs the whole workload (every unit, every step) in the launch shape of
+    ``run``, recording the checked units' outputs and evictions at every step and their cache state
+    every ``seg_len`` steps. The oracle then follows each checked unit through consecutive segments of
+    ``seg_len`` steps, in parallel: the first starts from the oracle's own prefill; every later one
+    from the GPU's state at its first step, which the previous segment's oracle state must match
+    (slot map and K/V rows exactly, scores within the float32 tolerance of that segment's additions).
+    Within a segment, evictions and outputs are compared at every step as in ``run``. The only
+    difference from one unbroken oracle trajectory: at each segment boundary the oracle continues
+    from the GPU's float32 scores rather than its own (after checking that the two agree)."""
+    import concurrent.futures as cf
+    import os
+
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+
+    steps = w.decode_steps
+    assert seg_len % chunk_steps == 0 or chunk_steps % seg_len == 0
+    chunk_steps = min(chunk_steps, seg_len)  # snapshots are taken at chunk ends
+    U, D, P, k = w.units, w.head_dim, w.prompt_len, w.budget
+    check_units = np.asarray(check_units)
+    nc = len(check_units)
+    dims = dims_of(w)
+    cache = h2o.H2OCache(dims, P)
+    gpu = Report(w.name, nc, steps)
+
+    prompt = synth.generate(w, seed, steps=0)
+    q, kk, v = (to_device(a, w.dtype) for a in (prompt.q_prompt, prompt.k_prompt, prompt.v_prompt))
+    cache.prefill(q, kk, v)
+    del q, kk, v
+    torch.cuda.synchronize()
+    assert h2o.h2o_get_device_error() == 0
+    snaps = {0: snapshot(w, cache, check_units)}
+    prompt_c = (prompt.q_prompt[check_units], prompt.k_prompt[check_units], prompt.v_prompt[check_units])
+    del prompt
+    out_h = np.empty((steps, nc, D), dtype=synth.storage_dtype(w))
+    es_h = np.empty((steps, nc), dtype=np.int32)
+    ep_h = np.empty((steps, nc), dtype=np.int32)
+    idx = torch.as_tensor(check_units, device="cuda", dtype=torch.long)
+    s0 = 0
+    while s0 < steps:
+        ns = min(chunk_steps, steps - s0)
+        chunk = synth.generate(w, seed, step0=s0, steps=ns, prompt=False)
+        dq, dk, dv = (to_device(a, w.dtype) for a in (chunk.q_dec, chunk.k_dec, chunk.v_dec))
+        del chunk
+        outs = torch.empty((ns, nc, D), dtype=cache.dtype, device="cuda")
+        evs = torch.empty((ns, U), dtype=torch.int32, device="cuda")
+        evp = torch.empty((ns, U), dtype=torch.int32, device="cuda")
+        for s in range(ns):
+            cache.step(dq[s], dk[s], dv[s], evicted_slot=evs[s], evicted_pos=evp[s])
+            outs[s] = cache.out.index_select(0, idx)
+        torch.cuda.synchronize()
+        err = h2o.h2o_get_device_error()
+        if err:
+            gpu.notes.append(f"device error word {err}")
+            return gpu
+        out_h[s0:s0 + ns] = to_host(outs, w.dtype)
+        es_h[s0:s0 + ns] = to_host(evs, "i32")[:, check_units]
+        ep_h[s0:s0 + ns] = to_host(evp, "i32")[:, check_units]
+        s0 += ns
+        if s0 % seg_len == 0 or s0 == steps:
+            snaps[s0] = snapshot(w, cache, check_units)
+        if property_checks is not None:
+            property_checks(cache, P + s0 - 1)
+        del dq, dk, dv, outs, evs, evp
+
+    orc = oracle.Oracle(k, w.k_heavy, w.k_local)
+    bounds = sorted(snaps)
+
+    def one(job):
+        j, a, b = job
+        u = check_units[j:j + 1]
+        rep = Report(w.name, 1, b - a)
+        st = orc.new_state(1, D, synth.storage_dtype(w))
+        if a == 0:
+            _, pinfo = orc.prefill_select(*(x[j:j + 1] for x in prompt_c), st,
+                                          prefer_pos=snaps[0]["slot_pos"][j:j + 1],
+                                          tie_rel=TIE_REL, err_rel=ERR_REL)
+            compare_prefill(rep, pinfo, u)
+            compare_snapshot(rep, {n: x[j:j + 1] for n, x in snaps[0].items()}, st, 0, 0)
+        else:
+            for n in ("slot_pos", "k_cache", "v_cache", "scores"):
+                getattr(st, n)[...] = snaps[a][n][j:j + 1]
+        x = synth.generate(w, seed, units=u, step0=a, steps=b - a, prompt=False, threads=1)
+        for s in range(a, b):
+            o_out, o_es, o_ep, _, infos = orc.decode_step(
+                P + s, x.q_dec[s - a], x.k_dec[s - a], x.v_dec[s - a], st,
+                prefer_victim=es_h[s, j:j + 1], tie_rel=TIE_REL, err_rel=ERR_REL)
+            compare_step(rep, w.dtype, P + s, u, widen(out_h[s, j:j + 1]), es_h[s, j:j + 1],
+                         ep_h[s, j:j + 1], o_out, o_es, o_ep, infos)
+        compare_snapshot(rep, {n: x[j:j + 1] for n, x in snaps[b].items()}, st, b, b - a)
+        return rep
+
+    jobs = [(j, a, b) for j in range(nc) for a, b in zip(bounds[:-1], bounds[1:])]
+    jobs.sort(key=lambda jb: -(jb[2] - jb[1]))
+    with cf.ThreadPoolExecutor(threads or os.cpu_count() or 1) as ex:
+        reports = list(ex.map(one, jobs))
+    rep = merge([gpu] + reports, w.name, nc, steps)
+    return rep
+
+
+def compare_step(rep: Report, dtype: str, t: int, units, gpu_out, gpu_es, gpu_ep, o_out, o_es, o_ep,
+                 infos) -> None:
+    """One decode step of the checked units: outputs within the dtype's tolerance; eviction slot and
+    position exact, except at a logged near tie (< TIE_REL) where the oracle took the GPU's choice.
+    gpu_out: float64 [units, D]; gpu_es / gpu_ep: [units]."""
+    e = float(np.max(np.abs(gpu_out - o_out)))
+    rep.max_out_err = max(rep.max_out_err, e)
+    if e > OUT_TOL[dtype] and len(rep.notes) < 10:
+        rep.notes.append(f"t={t}: output error {e:.3e}")
+    for j, inf in enumerate(infos):
+        if inf.kind == oracle.NO_EVICTION:
+            if gpu_es[j] != -1 or gpu_ep[j] != -1:
+                rep.mismatches += 1
+            continue
+        rep.decisions += 1
+        rep.near_ties += inf.kind == oracle.NEAR_TIE
+        rep.error_bound_ties += inf.kind == oracle.ERROR_BOUND
+        if inf.kind == oracle.NEAR_TIE or (inf.kind == oracle.RULE and 0 < inf.gap_rel < TIE_REL):
+            rep.near_tie_log.append((t, int(units[j]), float(inf.gap_rel), inf.kind == oracle.NEAR_TIE))
+        elif inf.kind == oracle.RULE and inf.gap_rel > 0:
+            rep.min_decision_gap = min(rep.min_decision_gap, float(inf.gap_rel))
+        if inf.kind == oracle.REJECTED or o_ep[j] != gpu_ep[j] or o_es[j] != gpu_es[j]:
+            rep.mismatches += 1
+            if len(rep.notes) < 10:
+                rep.notes.append(f"t={t} unit {units[j]}: gpu victim {gpu_es[j]}, oracle {o_es[j]} "
+                                 f"(kind {oracle.KIND_NAMES[inf.kind]}, gap {inf.gap_rel:.2e})")
+
+
+def merge(reports: list, workload: str, units_checked: int, steps: int) -> Report:
+    """One report from the reports of separate pieces of a run (counts added, extremes kept)."""
+    rep = Report(workload, units_checked, steps)
+    for r in reports:
+        for f in ("decisions", "near_ties", "error_bound_ties", "mismatches", "prefill_near_ties",
+                  "prefill_error_bound", "prefill_mismatches"):
+            setattr(rep, f, getattr(rep, f) + getattr(r, f))
+        for f in ("max_out_err", "max_score_rel_err", "max_prefill_out_err"):
+            setattr(rep, f, max(getattr(rep, f), getattr(r, f)))
+        rep.min_decision_gap = min(rep.min_decision_gap, r.min_decision_gap)
+        rep.notes += r.notes
+        rep.near_tie_log += r.near_tie_log
+    return rep
+
+
 def compare_state(rep: Report, w, cache, st: oracle.State, check_units, steps_done: int):
     """Slot map and K/V rows must be identical; scores within the accumulation tolerance."""
-    sp = to_host(cache.slot_pos, "i32")[check_units]
+    snap = snapshot(w, cache, check_units)
+    compare_snapshot(rep, snap, st, steps_done, 0 if rep.topk else steps_done)
+
+
+def snapshot(w, cache, units) -> dict:
+    """The GPU cache state of ``units`` on the host."""
+    snap = {"slot_pos": to_host(cache.slot_pos, "i32")[units],
+            "k_cache": to_host(cache.k_cache, w.dtype)[units],
+            "v_cache": to_host(cache.v_cache, w.dtype)[units],
+            "scores": to_host(cache.scores, "f32")[units]}
+    if cache.e4m3:
+        snap["k_scale"] = cache.k_scale.cpu().numpy()[units]
+        snap["v_scale"] = cache.v_scale.cpu().numpy()[units]
+    return snap
+
+
+def compare_snapshot(rep: Report, snap: dict, st: oracle.State, steps_done: int, acc_steps: int):
+    """GPU state ``snap`` against the oracle's ``st``: slot map, K/V rows (and E4M3 scales) exact;
+    scores within the tolerance of ``acc_steps`` float32 additions since both sides last agreed."""
+    sp = snap["slot_pos"]
     if not np.array_equal(sp, st.slot_pos):
         bad = np.argwhere(sp != st.slot_pos)
         rep.notes.append(f"after {steps_done} steps: slot map differs at {bad[:5].tolist()}")
         return
-    kc = to_host(cache.k_cache, w.dtype)[check_units]
-    vc = to_host(cache.v_cache, w.dtype)[check_units]
+    kc, vc = snap["k_cache"], snap["v_cache"]
     if not (np.array_equal(kc, st.k_cache) and np.array_equal(vc, st.v_cache)):
         bad = np.argwhere((kc != st.k_cache).any(axis=-1) | (vc != st.v_cache).any(axis=-1))
         rep.notes.append(f"after {steps_done} steps: K/V cache rows differ at {bad[:4].tolist()}")
     if st.e4m3:
-        ks = cache.k_scale.cpu().numpy()[check_units]
-        vs = cache.v_scale.cpu().numpy()[check_units]
-        if not (np.array_equal(ks, st.k_scale) and np.array_equal(vs, st.v_scale)):
+        if not (np.array_equal(snap["k_scale"], st.k_scale) and np.array_equal(snap["v_scale"], st.v_scale)):
             rep.notes.append(f"after {steps_done} steps: E4M3 row scales differ")
-    sc = to_host(cache.scores, "f32")[check_units].astype(np.float64)
+    sc = snap["scores"].astype(np.float64)
     ref = st.scores.astype(np.float64)
     rel = np.abs(sc - ref) / np.maximum(np.abs(ref), 1e-6)
     rep.max_score_rel_err = max(rep.max_score_rel_err, float(rel.max(initial=0.0)))
-    tol = score_rtol(0 if rep.topk else steps_done) + 1e-5
+    tol = score_rtol(acc_steps) + 1e-5
     if float(rel.max(initial=0.0)) > tol:
         rep.notes.append(f"after {steps_done} steps: score rel err {rel.max():.3e} > {tol:.3e}")
