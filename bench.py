@@ -316,6 +316,8 @@ def main():
     ap.add_argument("--no-prefill-forward", action="store_true")
     ap.add_argument("--no-per-layer", action="store_true",
                     help="skip the decode timing with one launch per layer and step")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' decode / prefill timings in the default line")
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "e4m3"],
                     help="cache format: the workload's dtype, or E4M3 codes with per-row scales")
     args = ap.parse_args()
@@ -466,6 +468,12 @@ def main():
     if not args.no_prefill_forward and not e4m3:
         line["prefill_forward"] = prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, args.warmup, K)
 
+    # The other workloads of the method's configurations, each timed on this GPU in the same run
+    # (decode kernel rate with its roofline, prefill time, clocks), and the E4M3 cache on this one.
+    if (not args.no_workloads and world == 1 and not e4m3 and args.layers is None
+            and args.decode_steps is None and w.name == "opt-6.7b"):
+        line["workloads"] = other_workloads(h2o, dv, dev, args.warmup, K)
+
     # End to end through the public API with host buffers: every job copies its prompt and decode
     # inputs host->device (pinned) and the outputs and eviction indices device->host.
     if not args.no_e2e:
@@ -477,6 +485,129 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def workload_timing(h2o, w: synth.Workload, dev, warmup: int, reps: int, e4m3: bool = False,
+                    dv=None, fill: int = 0, window: int | None = None) -> dict:
+    """One workload timed on its own: the prefill (h2o_prefill_select) and a window of ``window``
+    decode steps (default: all of them) after ``fill`` untimed steps, each launch over all of the
+    workload's units, captured in CUDA graphs. Every replay rebuilds the cache from the prompt and
+    replays the fill steps (untimed), then CUDA events on the launching stream bracket the prefill
+    and the window. ``dv``: device inputs to reuse (else generated here)."""
+    import torch
+    U, D, P = w.units, w.head_dim, w.prompt_len
+    window = w.decode_steps - fill if window is None else window
+    S = fill + window
+    assert S <= w.decode_steps
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    dims = h2o.Dims(units_b=w.units_b, heads=w.heads, head_dim=D, budget=w.budget,
+                    k_heavy=w.k_heavy, k_local=w.k_local, dtype=h2o.F32 if w.dtype == "f32" else h2o.BF16)
+    t_gen = 0.0
+    if dv is None:
+        t_gen = time.perf_counter()
+        inp = synth.generate(w, synth.DEFAULT_SEED, steps=S)
+
+        def to_dev(a):
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+            return (t.view(tdt) if a.dtype == np.uint16 else t).to(dev)
+
+        dv = {k: to_dev(getattr(inp, k)) for k in ("q_prompt", "k_prompt", "v_prompt", "q_dec", "k_dec", "v_dec")}
+        del inp
+        t_gen = time.perf_counter() - t_gen
+    cache = h2o.H2OCache(dims, P, device=dev, e4m3=e4m3)
+    calls = Calls(h2o, dims, cache, e4m3)
+    out = torch.empty((S, U, D), dtype=tdt, device=dev)
+    evs = torch.empty((S, U), dtype=torch.int32, device=dev)
+    evp = torch.empty((S, U), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def prefill():
+        calls.prefill(P, dv["q_prompt"], dv["k_prompt"], dv["v_prompt"], sp)
+
+    def decode_range(s0, s1):
+        for s in range(s0, s1):
+            calls.decode(P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s], out[s], evs[s], evp[s], sp)
+
+    with torch.cuda.stream(stream):  # one direct pass sets up the per-shape launch plans
+        prefill()
+        decode_range(0, S)
+    torch.cuda.synchronize(dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    g_pre = capture(prefill)
+    g_fill = [capture(lambda a=a: decode_range(a, min(fill, a + GRAPH_STEPS))) for a in range(0, fill, GRAPH_STEPS)]
+    g_win = [capture(lambda a=a: decode_range(a, min(S, a + GRAPH_STEPS))) for a in range(fill, S, GRAPH_STEPS)]
+    pre_ms, win_ms = [], []
+    with ClockSampler(dev.index or 0) as clocks:
+        for i in range(warmup + reps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            with torch.cuda.stream(stream):
+                ev[0].record(stream)
+                g_pre.replay()
+                ev[1].record(stream)
+                for g in g_fill:
+                    g.replay()
+                ev[2].record(stream)
+                for g in g_win:
+                    g.replay()
+                ev[3].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= warmup:
+                pre_ms.append(ev[0].elapsed_time(ev[1]))
+                win_ms.append(ev[2].elapsed_time(ev[3]))
+    if h2o.h2o_get_device_error(sp) != 0:
+        raise RuntimeError(f"device error word set during the {w.name} timing")
+    eb = w.elem_bytes
+    step_bytes = [U * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
+                       decode_bytes_per_unit(min(P + s, w.budget), D, eb)) for s in range(fill, S)]
+    avg_bytes = float(np.mean(step_bytes))
+    us = float(np.median(win_ms)) * 1000.0 / window
+    peaks, peak_kind = measured_peaks()
+    achieved = avg_bytes / (us * 1e-6) / 1e9
+    kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count, e4m3)
+    res = {"workload": f"{w.name}: {w.note}", "units_per_launch": U,
+           "kv_cache": "E4M3 codes + float32 row scales" if e4m3 else w.dtype,
+           "decode_steps_timed": window, "first_timed_position": P + fill,
+           "decode_us_per_step": us,
+           "decode_tokens_per_s": w.batch * window / (float(np.median(win_ms)) / 1000.0),
+           "prefill_ms": float(np.median(pre_ms)),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"],
+                        "traffic": recorded_traffic(w.name, kname, ksrc), "kernel": kname,
+                        "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                        "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": us},
+           "clocks": clocks.summary(), "gpu_launches_per_rep": 3 + S,
+           "how": "median over the timed replays; CUDA events around the prefill graph and around the "
+                  "window's decode graphs on the launching stream" +
+                  (f"; {fill} untimed decode steps before the window fill the cache" if fill else "")}
+    if t_gen:
+        res["input_generation_s"] = t_gen
+    del dv, cache, out, evs, evp
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def other_workloads(h2o, dv_main, dev, warmup: int, reps: int) -> dict:
+    """The method's other configurations, each on this GPU in the same run: the LLaMA-7B-shaped
+    decode (one layer of 2048 units per launch, the layer the configuration times), the OPT-30B-shaped
+    decode with its prefill (the configuration also times h2o_prefill_select), the streaming workload
+    over 2048 steps at its full 4096-slot cache, and the OPT-6.7B job with the E4M3 cache."""
+    W = synth.WORKLOADS
+    out = {}
+    out["llama-7b"] = workload_timing(h2o, W["llama-7b"], dev, warmup, reps)
+    out["opt-30b"] = workload_timing(h2o, W["opt-30b"], dev, warmup, reps)
+    st = W["streaming"]
+    fill = st.budget - st.prompt_len  # the cache is full from position 4096 on
+    out["streaming"] = workload_timing(h2o, st, dev, warmup, reps, fill=fill, window=2048)
+    out["opt-6.7b-e4m3"] = workload_timing(h2o, W["opt-6.7b"], dev, warmup, reps, e4m3=True, dv=dv_main)
+    return out
 
 
 def decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream, dev, g_pre, warmup: int,
