@@ -653,13 +653,15 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // every CTA's exchange barriers exist before any peer arrives on them
+  if (splits > 1) cluster_sync_all();  // every CTA's exchange barriers exist before any peer arrives
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // With p.early the producer's first cache tiles go out before the wait (the previous launch on
-  // the stream writes none of this call's cache); everything else waits for the previous grid.
+  // With p.early (the previous launch on the stream writes none of this call's cache) the producer's
+  // first cache tiles go out, and the epilogue warps read the unit's scores and slot map, before the
+  // wait; everything else waits for the previous grid.
   const bool early_tiles = p.early != 0 && warp == kTmaWarp && lane == 0;
-  if (!early_tiles) {
+  const bool early_epi = p.early != 0 && warp < kEpiWarps;
+  if (!early_tiles && !early_epi) {
     pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
     pdl_launch_dependents();
   }
@@ -737,12 +739,6 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     const bool cache_full = p.n == p.budget;
     const int32_t last_candidate = p.position - p.k_local;
     const size_t ud = static_cast<size_t>(unit) * kD + tid;
-    const float qd = __bfloat162float(p.q[ud]);
-    const __nv_bfloat16 kn = p.k_new[ud];
-    const __nv_bfloat16 vn = p.v_new[ud];
-    const int slice = kD / splits;
-    float vn_slice = 0.f;
-    if (tid < slice) vn_slice = __bfloat162float(p.v_new[static_cast<size_t>(unit) * kD + rank * slice + tid]);
     float sc[kMaxTiles];
     int32_t sp[kMaxTiles];
 #pragma unroll
@@ -752,6 +748,16 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
       sc[t] = valid ? p.scores[row0 + c0 + jl] : 0.f;
       sp[t] = valid ? p.slot_pos[row0 + c0 + jl] : 0;
     }
+    if (early_epi) {  // the new token's rows may be written by the previous grid: read after the wait
+      pdl_wait();
+      pdl_launch_dependents();
+    }
+    const float qd = __bfloat162float(p.q[ud]);
+    const __nv_bfloat16 kn = p.k_new[ud];
+    const __nv_bfloat16 vn = p.v_new[ud];
+    const int slice = kD / splits;
+    float vn_slice = 0.f;
+    if (tid < slice) vn_slice = __bfloat162float(p.v_new[static_cast<size_t>(unit) * kD + rank * slice + tid]);
     float part = qd * __bfloat162float(kn);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -803,19 +809,23 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     if (lane == 0) red[warp] = lsum;
     epi_sync();
     const float lc = red[0] + red[1] + red[2] + red[3];
-    // Exchange 1: (local max, local normaliser) -> cluster-wide max and normaliser.
-    if (tid == 0) {
-      for (int r = 0; r < splits; ++r) {
-        st_peer_f32(peer_smem(&xg->m_in[rank], r), mc);
-        st_peer_f32(peer_smem(&xg->l_in[rank], r), lc);
-        arrive_peer(peer_smem(&xbar[0], r));
+    // Exchange 1: (local max, local normaliser) -> cluster-wide max and normaliser. One CTA per unit
+    // (splits == 1) has both already: m = mc, l = lc (what the exchange would give: lc * exp(0)).
+    float mg = mc, l = lc;
+    if (splits > 1) {
+      if (tid == 0) {
+        for (int r = 0; r < splits; ++r) {
+          st_peer_f32(peer_smem(&xg->m_in[rank], r), mc);
+          st_peer_f32(peer_smem(&xg->l_in[rank], r), lc);
+          arrive_peer(peer_smem(&xbar[0], r));
+        }
       }
+      ok = mbar_wait_cluster(&xbar[0], 0, p.err) && ok;
+      mg = -INFINITY;
+      for (int r = 0; r < splits; ++r) mg = fmaxf(mg, xg->m_in[r]);
+      l = 0.f;
+      for (int r = 0; r < splits; ++r) l = fmaf(xg->l_in[r], expf(xg->m_in[r] - mg), l);
     }
-    ok = mbar_wait_cluster(&xbar[0], 0, p.err) && ok;
-    float mg = -INFINITY;
-    for (int r = 0; r < splits; ++r) mg = fmaxf(mg, xg->m_in[r]);
-    float l = 0.f;
-    for (int r = 0; r < splits; ++r) l = fmaf(xg->l_in[r], expf(xg->m_in[r] - mg), l);
     const float w_new = expf(s_new - mg);
 
     unsigned long long best = ~0ull;
@@ -856,39 +866,54 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     float oc0 = 0.f, oc1 = 0.f;
     tmem_ld2(lane_base + kPvCol, oc0, oc1);
     const float opart = T > 0 ? (oc0 + oc1) * expf(mc - mg) : 0.f;
-    st_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart);
-    fence_cluster();
-    epi_sync();
-    // Exchange 2: eviction keys and output slices.
-    if (tid == 0) {
-      unsigned long long kb = kred[0];
-      int32_t sb = sred[0];
-      for (int w = 1; w < kEpiWarps; ++w)
-        if (kred[w] < kb) {
-          kb = kred[w];
-          sb = sred[w];
-        }
-      for (int r = 0; r < splits; ++r) {
-        st_peer_u64(peer_smem(&xg->key_in[rank], r), kb);
-        st_peer_s32(peer_smem(&xg->slot_in[rank], r), sb);
-        arrive_peer(peer_smem(&xbar[1], r));
-      }
-    }
-    ok = mbar_wait_cluster(&xbar[1], 0, p.err) && ok;
     int32_t victim = -1;
     unsigned long long vkey = ~0ull;
-    if (cache_full) {
+    float o_sum = 0.f;  // this thread's output element (tid < slice) before the new token's share
+    if (splits == 1) {
+      // One CTA per unit: the block's own argmin and output, no exchange.
+      epi_sync();  // kred / sred complete
+      for (int w = 0; w < kEpiWarps; ++w)
+        if (kred[w] < vkey) {
+          vkey = kred[w];
+          victim = sred[w];
+        }
+      o_sum += opart;
+    } else {
+      st_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart);
+      fence_cluster();
+      epi_sync();
+      // Exchange 2: eviction keys and output slices.
+      if (tid == 0) {
+        unsigned long long kb = kred[0];
+        int32_t sb = sred[0];
+        for (int w = 1; w < kEpiWarps; ++w)
+          if (kred[w] < kb) {
+            kb = kred[w];
+            sb = sred[w];
+          }
+        for (int r = 0; r < splits; ++r) {
+          st_peer_u64(peer_smem(&xg->key_in[rank], r), kb);
+          st_peer_s32(peer_smem(&xg->slot_in[rank], r), sb);
+          arrive_peer(peer_smem(&xbar[1], r));
+        }
+      }
+      ok = mbar_wait_cluster(&xbar[1], 0, p.err) && ok;
       for (int r = 0; r < splits; ++r)
         if (xg->key_in[r] < vkey) {
           vkey = xg->key_in[r];
           victim = xg->slot_in[r];
         }
-      if (tid == 0 && rank == 0 && victim < 0) atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
+      if (tid < slice)
+        for (int r = 0; r < splits; ++r) o_sum += xg->o_in[r * slice + tid];
+    }
+    if (!cache_full) {
+      victim = -1;
+      vkey = ~0ull;
+    } else if (tid == 0 && rank == 0 && victim < 0) {
+      atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
     }
     if (tid < slice) {
-      float o = 0.f;
-      for (int r = 0; r < splits; ++r) o += xg->o_in[r * slice + tid];
-      o = fmaf(w_new, vn_slice, o);
+      const float o = fmaf(w_new, vn_slice, o_sum);
       p.out[static_cast<size_t>(unit) * kD + rank * slice + tid] = __float2bfloat16_rn(o / l);
     }
 #pragma unroll
@@ -915,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     // peer may still be on its way, so this CTA must not exit yet: thread 0 waits for all arrivals
     // on xbar[1] (a second, longer bounded window; an immediate return on the normal path), and
     // the block barrier below holds the whole CTA until then.
-    if (tid == 0) (void)mbar_wait_cluster(&xbar[1], 0, p.err, 8000000000ull);
+    if (tid == 0 && splits > 1) (void)mbar_wait_cluster(&xbar[1], 0, p.err, 8000000000ull);
   }
 
   tc_fence_before();
