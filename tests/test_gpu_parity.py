@@ -409,3 +409,34 @@ def test_prefill_between_decodes_of_different_caches(middle):
     for i, (p, q) in enumerate(zip(x, y)):
         assert torch.equal(p, q), i
     assert h2o.h2o_get_device_error() == 0
+
+
+@pytest.mark.parametrize("P", [100, 256, 300, 512])
+def test_prefill_with_many_units(P):
+    """At least 8 units per SM: CTAs take whole units, and with prompts of up to 4 tiles each unit's
+    streamed tiles stay in shared memory for all of its items. 1280 OPT-6.7B-shaped units with
+    prompts of 1 to 4 tiles: every column sum of 40 sampled units against the oracle's float64 sums,
+    then the kept slot maps and 8 decode steps."""
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    w = W["opt-6.7b"].with_(layers=1, batch=40, heads=32, decode_steps=8, prompt_len=P)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w.units >= 8 * sms
+    units = np.linspace(0, w.units - 1, 40).astype(int)
+    inp = synth.generate(w, steps=0)
+    dims = parity.dims_of(w)
+    q, k = parity.to_device(inp.q_prompt, w.dtype), parity.to_device(inp.k_prompt, w.dtype)
+    colsum = torch.empty((w.units, w.prompt_len), dtype=torch.float32, device="cuda")
+    ws = torch.empty(h2o.h2o_prefill_workspace_bytes(dims, w.prompt_len), dtype=torch.uint8, device="cuda")
+    h2o.h2o_prefill_scores(dims, w.prompt_len, q, k, colsum, ws)
+    got = colsum.cpu().numpy().astype(np.float64)
+    orc = oracle.Oracle(w.budget, w.k_heavy, w.k_local)
+    st = orc.new_state(len(units), w.head_dim, synth.storage_dtype(w))
+    ref, _ = orc.prefill_select(inp.q_prompt[units], inp.k_prompt[units], inp.v_prompt[units], st,
+                                want_colsum=True)
+    rel = np.abs(got[units] - ref) / np.maximum(ref, 1e-3)
+    print(f"P={P}: column sums max rel err {rel.max():.2e}")
+    assert rel.max() < 2e-5, rel.max()
+    assert np.allclose(got.sum(axis=1), w.prompt_len, rtol=1e-5)
+    _assert(parity.run(w, check_units=units, state_every=8))
