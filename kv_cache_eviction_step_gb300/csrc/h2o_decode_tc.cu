@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
 // arriving on the peers' exchange mbarriers with cluster-scope release. Only the epilogue warps take
 // part, so the TMA and MMA warps never wait on the cluster.
 // CTA r finishes output elements [r 128/splits, (r+1) 128/splits); the CTA holding the victim writes
-// the new token; rank 0 writes the eviction indices.
+// the new token; rank 0 writes the eviction indices. With splits == 1 (one CTA per unit, e.g. one
+// layer's 256 units per launch) there is nothing to exchange and the kernel skips both exchanges.
 
 constexpr int kSplitStages = 3;
 constexpr int kMaxSplitsTc = 16;
