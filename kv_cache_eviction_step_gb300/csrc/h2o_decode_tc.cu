@@ -1184,7 +1184,7 @@ cudaError_t launch_decode_tc(const DecodeParams& dp, cudaStream_t stream) {
       ready.emplace_back(dev, sms);
     }
   }
-  const int grid = dp.units < sms ? dp.units : sms;
+  const int grid = balanced_grid(dp.units, sms);
   return launch_pdl(kTcKernels[dp.policy != H2O_POLICY_H2O], grid, kThreads, kSmem, stream, &p);
 }
 
