@@ -772,7 +772,7 @@ cudaError_t launch_decode_e4m3(const DecodeParams& dp, cudaStream_t stream) {
       ready.emplace_back(dev, sms);
     }
   }
-  const int grid = dp.units < sms ? dp.units : sms;
+  const int grid = balanced_grid(dp.units, sms);
   const bool any = dp.policy != H2O_POLICY_H2O;
   if (p.tiles <= 2) return launch_pdl(kKernels[0][any], grid, Layout<2>::kThreads, Layout<2>::kSmem, stream, &p);
   return launch_pdl(kKernels[1][any], grid, Layout<4>::kThreads, Layout<4>::kSmem, stream, &p);
