@@ -99,16 +99,15 @@ inline cudaError_t launch_pdl(const void* kernel, int grid, int threads, int sme
   return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
-// Grid of the persistent decode kernels (bf16 and E4M3), whose CTAs take units u = blockIdx.x + k
-// gridDim.x.
-// A launch ends with its most loaded CTA; when every CTA runs many units (at least 8) the launch is
-// bandwidth-bound, so its time goes as ceil(units / G) unit times, each inversely proportional to the
-// bandwidth share of G SMs: proportional to ceil(units / G) * G. The G in [4/5 of the SMs, all of
-// them] that minimises that is taken when it saves at least 3 %. Measured: 2048 units of 460 slots
-// (128 CTAs of 16 units instead of 152 of 13-14) 77.4 -> 75.3 us (E4M3 cache: 43.3 -> 42.4 us);
-// 1792 units of 307 slots, where
-// 128 CTAs of 14 would save 1.75 % on paper, ran 5.8 % slower (fewer SMs, each with less in flight),
-// which is what the 3 % margin keeps out; 8192 units keep all 152 SMs (0.2 %).
+// Grid of the persistent decode kernels (bf16 and E4M3), whose CTAs take units
+// u = blockIdx.x + k gridDim.x. A launch ends with its most loaded CTA; when every CTA runs many
+// units (at least 8) the launch is bandwidth-bound, so its time goes as ceil(units / G) unit times,
+// each inversely proportional to the bandwidth share of G SMs: proportional to ceil(units / G) * G.
+// The G in [4/5 of the SMs, all of them] that minimises that is taken when it saves at least 3 %.
+// Measured: 2048 units of 460 slots run on 128 CTAs of 16 units instead of 152 of 13-14, 77.4 ->
+// 75.3 us (E4M3 cache: 43.3 -> 42.4 us); 1792 units of 307 slots, where 128 CTAs of 14 would save
+// 1.75 % on paper, ran 5.8 % slower (fewer SMs, each with less in flight), which is what the 3 %
+// margin keeps out; 8192 units keep all 152 SMs (0.2 %).
 inline int balanced_grid(int units, int sms) {
   if (units < 8 * sms) return units < sms ? units : sms;
   const long long full = static_cast<long long>((units + sms - 1) / sms) * sms;
