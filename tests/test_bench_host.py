@@ -1,0 +1,46 @@
+"""bench.py's host-side pieces on CPU: the algorithmic bytes per unit behind every roofline figure,
+the kernel each workload's decode step dispatches to, and the oracle baseline's record."""
+
+import argparse
+
+import bench
+import synth
+
+
+def test_decode_bytes_per_unit():
+    # n (2 D eb + 12) + 6 D eb + 16: K and V rows, score read + write and position read per slot;
+    # q / k_new / v_new in, the victim's K/V row and the output row out; score, position, indices
+    assert bench.decode_bytes_per_unit(204, 128, 2) == 204 * 524 + 1552 == 108_448
+    assert 8192 * bench.decode_bytes_per_unit(204, 128, 2) == 888_406_016  # one OPT-6.7B launch
+    assert bench.decode_bytes_per_unit(32, 64, 4) == 32 * 524 + 1552   # tiny: fp32, D = 64
+    # E4M3: codes (2 n D), row scales (8 n), scores and positions (12 n); bf16 q/k/v/out (8 D),
+    # the victim's codes (2 D) and scales (8); score, position, indices (16)
+    assert bench.decode_bytes_per_unit_e4m3(204, 128) == 204 * 276 + 1304
+    assert bench.decode_bytes_per_unit(0, 128, 2) == 6 * 128 * 2 + 16  # empty cache: the token only
+
+
+def test_decode_kernel_dispatch():
+    W = synth.WORKLOADS
+    k = lambda name, **kw: bench.decode_kernel(W[name].with_(**kw), 152)[0]
+    assert k("opt-6.7b") == "h2o_decode_tc_kernel"             # 8192 units, k = 204
+    assert k("llama-7b") == "h2o_decode_tc_kernel"             # 2048 units, k = 460
+    assert k("opt-30b") == "h2o_decode_tc_kernel"              # 1792 units, k = 307
+    assert k("opt-6.7b", layers=1) == "h2o_decode_tc_split_kernel"  # 256 units: one layer
+    assert k("streaming") == "h2o_decode_tc_split_kernel"      # 32 units, k = 4096
+    assert k("tiny") == "h2o_decode_step_kernel"               # fp32, D = 64
+    assert bench.decode_kernel(W["opt-6.7b"], 152, e4m3=True)[0] == "h2o_decode_e4m3_kernel"
+
+
+def test_oracle_baseline_record():
+    b = bench.cpu_oracle_baseline(synth.WORKLOADS["tiny"], synth.DEFAULT_SEED, target_s=0.2)
+    assert b["kind"] == "oracle" and b["unit"] == "tokens/s" and b["cores"] >= 1
+    assert b["value"] > 0 and "units" in b["sample"]
+
+
+def test_config_names_the_workload():
+    w = synth.WORKLOADS["opt-6.7b"]
+    args = argparse.Namespace(gpus=1, kv_cache="bf16")
+    c = bench.config_of(w, args)
+    assert c["workload"].startswith("opt-6.7b") and c["units"] == 8192 and c["budget"] == 204
+    assert (c["k_heavy"], c["k_local"], c["prompt_len"], c["decode_steps"]) == (102, 102, 512, 512)
+    assert "model" not in c
