@@ -95,13 +95,16 @@ def source_sha(path: str) -> str:
 
 def decode_kernel(w: synth.Workload, sms: int, e4m3: bool = False) -> tuple[str, str]:
     """Which decode kernel the library launches for this workload (the C ABI's dispatch rule:
-    persistent tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512, the cluster-split
+    persistent tcgen05 for >= 4 bf16 units of D = 128 per SM with budgets up to 512, the resident
+    one-CTA-per-unit kernel for 1 to 4 such units per SM with budgets up to 208, the cluster-split
     tcgen05 kernel for other bf16 D = 128 caches up to 8192 slots, the CUDA-core kernel otherwise;
     the E4M3 cache always runs its persistent tcgen05 kernel)."""
     if e4m3:
         return "h2o_decode_e4m3_kernel", os.path.join(CSRC, "h2o_decode_e4m3.cu")
     if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 512 and w.units >= 4 * sms:
         return "h2o_decode_tc_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
+    if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 208 and w.units >= sms:
+        return "h2o_decode_resident_kernel", os.path.join(CSRC, "h2o_decode_resident.cu")
     if w.dtype == "bf16" and w.head_dim == 128 and w.budget <= 8192:
         return "h2o_decode_tc_split_kernel", os.path.join(CSRC, "h2o_decode_tc.cu")
     return "h2o_decode_step_kernel", os.path.join(CSRC, "h2o_decode.cu")
@@ -624,59 +627,80 @@ def decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream, dev,
                     budget=dims.budget, k_heavy=dims.k_heavy, k_local=dims.k_local, dtype=dims.dtype)
     c, sp = calls.cache, stream.cuda_stream
 
-    def launch(s, l):
+    order = [(s, l) for s in range(S) for l in range(L)]
+
+    def launch(i, hint):
+        s, l = order[i]
         sl = slice(l * ul, (l + 1) * ul)
         args = (dv["q_dec"][s][sl], dv["k_dec"][s][sl], dv["v_dec"][s][sl], c.k_cache[sl], c.v_cache[sl])
         if e4m3:
             h2o.h2o_decode_step_e4m3(dl, None, P + s, *args, c.k_scale[sl], c.v_scale[sl], c.scores[sl],
                                      c.slot_pos[sl], out[s][sl], evs[s][sl], evp[s][sl], sp)
+        elif hint:  # the next launch's layer (the next step's layer 0 after the last layer)
+            nxt = None
+            if i + 1 < len(order):
+                nl = order[i + 1][1]
+                ns = slice(nl * ul, (nl + 1) * ul)
+                nxt = h2o.next_cache(c.k_cache[ns], c.v_cache[ns], c.scores[ns], c.slot_pos[ns])
+            h2o.h2o_decode_step_prefetch(dl, None, P + s, *args, c.scores[sl], c.slot_pos[sl], out[s][sl],
+                                         evs[s][sl], evp[s][sl], nxt, sp)
         else:
             h2o.h2o_decode_step(dl, P + s, *args, c.scores[sl], c.slot_pos[sl], out[s][sl], evs[s][sl],
                                 evp[s][sl], sp)
 
-    order = [(s, l) for s in range(S) for l in range(L)]
-    with torch.cuda.stream(stream):  # one direct pass sets up the per-shape launch plans
-        g_pre.replay()
-        for s, l in order:
-            launch(s, l)
-    torch.cuda.synchronize(dev)
-    graphs = []
-    for i0 in range(0, len(order), GRAPH_STEPS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for s, l in order[i0:i0 + GRAPH_STEPS]:
-                launch(s, l)
-        graphs.append(g)
-    ms = []
-    for i in range(warmup + reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
+    def timed(hint):
+        with torch.cuda.stream(stream):  # one direct pass sets up the per-shape launch plans
             g_pre.replay()
-            e0.record(stream)
-            for g in graphs:
-                g.replay()
-            e1.record(stream)
+            for i in range(len(order)):
+                launch(i, hint)
         torch.cuda.synchronize(dev)
-        if i >= warmup:
-            ms.append(e0.elapsed_time(e1))
-    if h2o.h2o_get_device_error(sp) != 0:
-        raise RuntimeError("device error word set during the per-layer decode timing")
+        graphs = []
+        for i0 in range(0, len(order), GRAPH_STEPS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(i0, min(i0 + GRAPH_STEPS, len(order))):
+                    launch(i, hint)
+            graphs.append(g)
+        ms = []
+        for i in range(warmup + reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g_pre.replay()
+                e0.record(stream)
+                for g in graphs:
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= warmup:
+                ms.append(e0.elapsed_time(e1))
+        if h2o.h2o_get_device_error(sp) != 0:
+            raise RuntimeError("device error word set during the per-layer decode timing")
+        return float(np.median(ms))
+
     eb = 2 if w.dtype == "bf16" else 4
     step_bytes = float(np.mean([w.units * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
                                            decode_bytes_per_unit(min(P + s, w.budget), D, eb))
                                 for s in range(S)]))
-    us = float(np.median(ms)) * 1000.0 / S
     kname = decode_kernel(w.with_(layers=1), torch.cuda.get_device_properties(dev).multi_processor_count,
                           e4m3)[0]
     peak = measured_peaks()[0]["hbm_gbs"]
-    return {"launches_per_step": L, "units_per_launch": ul, "kernel": kname,
-            "us_per_step": us, "us_per_launch": us / L,
-            "decode_tokens_per_s": w.batch * S / (float(np.median(ms)) / 1000.0),
-            "kv_read_gbs": step_bytes / (us * 1e-6) / 1e9,
-            "frac": step_bytes / (us * 1e-6) / 1e9 / peak,
-            "how": "per step, one h2o_decode_step launch per layer over its batch x heads units, in CUDA "
-                   "graphs; median over the timed replays; cache rebuilt by the prefill between replays "
-                   "(untimed)"}
+
+    def entry(ms, call):
+        us = ms * 1000.0 / S
+        return {"us_per_step": us, "us_per_launch": us / L,
+                "decode_tokens_per_s": w.batch * S / (ms / 1000.0),
+                "kv_read_gbs": step_bytes / (us * 1e-6) / 1e9,
+                "frac": step_bytes / (us * 1e-6) / 1e9 / peak, "call": call}
+
+    res = {"launches_per_step": L, "units_per_launch": ul, "kernel": kname}
+    if e4m3:
+        res.update(entry(timed(False), "h2o_decode_step_e4m3"))
+    else:  # the hinted call is how a model launches the step per layer; the plain call beside it
+        res.update(entry(timed(True), "h2o_decode_step_prefetch (next layer's cache named)"))
+        res["plain"] = entry(timed(False), "h2o_decode_step")
+    res["how"] = ("per step, one decode launch per layer over its batch x heads units, in CUDA graphs; "
+                  "median over the timed replays; cache rebuilt by the prefill between replays (untimed)")
+    return res
 
 
 def prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, warmup: int, reps: int) -> dict:

@@ -232,6 +232,34 @@ H2O_API h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy
                                           int32_t* evicted_slot, int32_t* evicted_pos, void* stream);
 
 /*
+ * The cache arrays of the decode call that will follow this one on the same stream: same dims and
+ * layouts as this call's k_cache, v_cache, scores and slot_pos (e.g. the next layer's cache when a
+ * model launches the step once per layer). All four non-NULL, k_cache and v_cache 16-byte aligned.
+ */
+typedef struct {
+  const void* k_cache;
+  const void* v_cache;
+  const float* scores;
+  const int32_t* slot_pos;
+} h2o_next_cache;
+
+/*
+ * h2o_decode_step_policy with a hint: while this step runs, the kernel asks L2 for `next`'s rows
+ * (prefetch only; nothing of `next` is read into a result or written), so that the next call's
+ * cache reads hit L2 instead of waiting for HBM. The step's results are identical with and without
+ * the hint, and next == NULL is the plain call. Honoured by the kernels that run one CTA per unit
+ * (few units per SM, bf16, D = 128: one layer's batch x heads per launch); ignored by the others.
+ * next's arrays must be device memory of the stated shape (an invalid address is undefined
+ * behaviour, as for every pointer here); H2O_ERR_INVALID_ARG for a NULL or misaligned member.
+ */
+H2O_API h2o_status h2o_decode_step_prefetch(const h2o_dims* dims, const h2o_policy* policy,
+                                            int32_t position, const void* q, const void* k_new,
+                                            const void* v_new, void* k_cache, void* v_cache,
+                                            float* scores, int32_t* slot_pos, void* out,
+                                            int32_t* evicted_slot, int32_t* evicted_pos,
+                                            const h2o_next_cache* next, void* stream);
+
+/*
  * The same two operations over a quantised cache (the H2O post §3.3 discusses combining H2O with
  * KV-cache quantisation): q, k, v, k_new, v_new and out stay as dims->dtype, which must be
  * H2O_BF16 with head_dim 128 and budget <= 512 (else H2O_ERR_UNSUPPORTED); the caches hold FP8

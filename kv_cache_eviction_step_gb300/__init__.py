@@ -28,7 +28,8 @@ STATIC_SCRATCH_BYTES = 16 << 20  # H2O_STATIC_SCRATCH_BYTES
 
 EXPORTS = ("h2o_prefill_workspace_bytes", "h2o_prefill_scores", "h2o_prefill_select",
            "h2o_prefill_select_static", "h2o_prefill_select_policy", "h2o_prefill_forward",
-           "h2o_decode_step", "h2o_decode_step_policy", "h2o_prefill_select_e4m3",
+           "h2o_decode_step", "h2o_decode_step_policy", "h2o_decode_step_prefetch",
+           "h2o_prefill_select_e4m3",
            "h2o_decode_step_e4m3", "h2o_get_device_error",
            "h2o_selftest_wait_timeout", "h2o_last_cuda_error", "h2o_status_string")
 
@@ -47,6 +48,14 @@ class Dims(ctypes.Structure):
 
     def __repr__(self):
         return ("Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
+
+
+class NextCache(ctypes.Structure):
+    """``h2o_next_cache``: the cache arrays of the next decode call on the stream (an L2 prefetch
+    hint for h2o_decode_step_prefetch)."""
+
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("scores", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p)]
 
 
 class Policy(ctypes.Structure):
@@ -100,6 +109,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.h2o_prefill_select_policy.restype = ctypes.c_int
     lib.h2o_decode_step_policy.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.h2o_decode_step_policy.restype = ctypes.c_int
+    lib.h2o_decode_step_prefetch.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             ctypes.POINTER(NextCache), vp]
+    lib.h2o_decode_step_prefetch.restype = ctypes.c_int
     lib.h2o_prefill_forward.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.h2o_prefill_forward.restype = ctypes.c_int
     lib.h2o_prefill_select_e4m3.argtypes = [dp, pp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -231,6 +243,21 @@ def h2o_decode_step_policy(dims: Dims, policy: Policy | None, position: int, q, 
         _ptr(evicted_pos), _stream(stream)))
 
 
+def next_cache(k_cache, v_cache, scores, slot_pos) -> NextCache:
+    """The ``h2o_next_cache`` of a cache's arrays (tensors or raw pointers)."""
+    return NextCache(_ptr(k_cache), _ptr(v_cache), _ptr(scores), _ptr(slot_pos))
+
+
+def h2o_decode_step_prefetch(dims: Dims, policy: Policy | None, position: int, q, k_new, v_new,
+                             k_cache, v_cache, scores, slot_pos, out, evicted_slot, evicted_pos,
+                             next: NextCache | None, stream=None):
+    """h2o_decode_step_policy, asking L2 for ``next``'s rows while it runs (None: no hint)."""
+    _check("h2o_decode_step_prefetch", load().h2o_decode_step_prefetch(
+        ctypes.byref(dims), _policy_ref(policy), position, _ptr(q), _ptr(k_new), _ptr(v_new),
+        _ptr(k_cache), _ptr(v_cache), _ptr(scores), _ptr(slot_pos), _ptr(out), _ptr(evicted_slot),
+        _ptr(evicted_pos), None if next is None else ctypes.byref(next), _stream(stream)))
+
+
 def h2o_prefill_select_e4m3(dims: Dims, policy: Policy | None, prompt_len: int, q, k, v, k_cache,
                             v_cache, k_scale, v_scale, scores, slot_pos, workspace, stream=None,
                             workspace_bytes: int | None = None):
@@ -312,11 +339,21 @@ class H2OCache:
                                 self.v_cache, self.scores, self.slot_pos, self.workspace, stream)
         self.position = self.prompt_len
 
-    def step(self, q, k_new, v_new, out=None, evicted_slot=None, evicted_pos=None, stream=None):
+    def step(self, q, k_new, v_new, out=None, evicted_slot=None, evicted_pos=None, stream=None,
+             prefetch: "H2OCache | None" = None):
+        """One decode step. ``prefetch``: the cache the next step on this stream will decode (same
+        dims), asked of L2 while this step runs (h2o_decode_step_prefetch; bf16 caches only)."""
         out = self.out if out is None else out
         es = self.evicted_slot if evicted_slot is None else evicted_slot
         ep = self.evicted_pos if evicted_pos is None else evicted_pos
-        if self.e4m3:
+        if prefetch is not None:
+            if self.e4m3 or prefetch.e4m3:
+                raise ValueError("the next-call prefetch hint is for bf16 / fp32 caches")
+            h2o_decode_step_prefetch(self.dims, self.policy, self.position, q, k_new, v_new,
+                                     self.k_cache, self.v_cache, self.scores, self.slot_pos, out, es,
+                                     ep, next_cache(prefetch.k_cache, prefetch.v_cache,
+                                                    prefetch.scores, prefetch.slot_pos), stream)
+        elif self.e4m3:
             h2o_decode_step_e4m3(self.dims, self.policy, self.position, q, k_new, v_new, self.k_cache,
                                  self.v_cache, self.k_scale, self.v_scale, self.scores, self.slot_pos,
                                  out, es, ep, stream)

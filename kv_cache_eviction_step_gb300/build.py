@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libh2o.so")
 SOURCES = ["h2o_abi.cu", "h2o_decode.cu", "h2o_prefill_simt.cu", "h2o_select.cu", "h2o_noalloc.cu",
-           "h2o_prefill_tc.cu", "h2o_decode_tc.cu", "h2o_decode_e4m3.cu"]
+           "h2o_prefill_tc.cu", "h2o_decode_tc.cu", "h2o_decode_e4m3.cu", "h2o_decode_resident.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]

@@ -347,6 +347,11 @@ static h2o_status dispatch_decode(DecodeParams& p, const h2o_dims* dims, void* s
   // unit split over a CTA cluster when units are few.
   if (decode_tc_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= 4 * sm_count())
     return from_cuda(launch_decode_tc(p, static_cast<cudaStream_t>(stream)));
+  // At least one unit per SM but fewer than four (e.g. one layer's batch x heads per launch), bf16,
+  // D = 128, caches of at most 208 slots: one CTA per unit with the unit's K and V resident in shared
+  // memory and both contractions on the CUDA cores.
+  if (decode_resident_supported(dims->head_dim, dims->dtype, dims->budget) && p.units >= sm_count())
+    return from_cuda(launch_decode_resident(p, static_cast<cudaStream_t>(stream)));
   // Fewer bf16 units of D = 128 (or longer caches): the tensor-core step split over a CTA cluster.
   if (decode_tc_split_supported(dims->head_dim, dims->dtype, p.units, p.n))
     return from_cuda(launch_decode_tc_split(p, static_cast<cudaStream_t>(stream)));
@@ -362,9 +367,13 @@ static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* polic
                                    const void* v_new, void* k_cache, void* v_cache, float* scores,
                                    int32_t* slot_pos, void* out, int32_t* evicted_slot,
                                    int32_t* evicted_pos, void* stream, float* k_scale = nullptr,
-                                   float* v_scale = nullptr) {
+                                   float* v_scale = nullptr, const h2o_next_cache* next = nullptr) {
   h2o_status st = check_dims(dims);
   if (st != H2O_OK) return st;
+  if (next != nullptr && (next->k_cache == nullptr || next->v_cache == nullptr || next->scores == nullptr ||
+                          next->slot_pos == nullptr || !aligned16(next->k_cache) ||
+                          !aligned16(next->v_cache) || !aligned4(next->scores) || !aligned4(next->slot_pos)))
+    return H2O_ERR_INVALID_ARG;
   const h2o_policy pol = policy ? *policy : h2o_policy{H2O_POLICY_H2O, 0, 1};
   st = check_policy(&pol, dims->budget);
   if (st != H2O_OK) return st;
@@ -401,6 +410,12 @@ static h2o_status decode_step_impl(const h2o_dims* dims, const h2o_policy* polic
   p.stride = pol.kind == H2O_POLICY_STRIDED ? pol.stride : 1;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  if (next != nullptr) {
+    p.next_k_cache = next->k_cache;
+    p.next_v_cache = next->v_cache;
+    p.next_scores = next->scores;
+    p.next_slot_pos = next->slot_pos;
+  }
 
   // This call's cache arrays (read, and written in place) and its outputs.
   const size_t slots = static_cast<size_t>(p.units) * static_cast<size_t>(dims->budget);
@@ -450,6 +465,15 @@ h2o_status h2o_decode_step_policy(const h2o_dims* dims, const h2o_policy* policy
                                   void* stream) {
   return decode_step_impl(dims, policy, position, q, k_new, v_new, k_cache, v_cache, scores,
                           slot_pos, out, evicted_slot, evicted_pos, stream);
+}
+
+h2o_status h2o_decode_step_prefetch(const h2o_dims* dims, const h2o_policy* policy, int32_t position,
+                                    const void* q, const void* k_new, const void* v_new,
+                                    void* k_cache, void* v_cache, float* scores, int32_t* slot_pos,
+                                    void* out, int32_t* evicted_slot, int32_t* evicted_pos,
+                                    const h2o_next_cache* next, void* stream) {
+  return decode_step_impl(dims, policy, position, q, k_new, v_new, k_cache, v_cache, scores,
+                          slot_pos, out, evicted_slot, evicted_pos, stream, nullptr, nullptr, next);
 }
 
 h2o_status h2o_decode_step_e4m3(const h2o_dims* dims, const h2o_policy* policy, int32_t position,

@@ -1,0 +1,375 @@
+// h2o_decode_resident.cu -- the decode step (D1-D7) for launches of few units with short caches,
+// e.g. one layer of a model's batch x heads per launch: one CTA per unit that holds the unit's whole
+// K and V in shared memory.
+//
+// Per unit and step (n = min(t, budget) cached slots; H2O post §2.1.1-§2.3, "H2O Heavy-Hitter
+// Oracle 分析" §3.2): logits s_j = (q . K_j) / sqrt(D) and s_new, softmax over the n + 1 keys,
+// out = sum_j p_j V_j + p_new v_new, scores[j] += p_j in fp32, victim = argmin over the slots with
+// position <= t - k_local of (score, position), and the new token written into the victim slot.
+//
+// Why a kernel of its own. A launch of 256 units of 204 slots carries 27.8 MB, ~4 us of HBM time,
+// so it is bound by what happens around the previous launch: when its CTAs can start, when their
+// data arrives, and the chain of dependent steps once the query is there. Here:
+//   - the unit's K and V (n rows each, <= 208 x 256 B) are fetched by bulk copies of 32 rows with one
+//     mbarrier each, issued at CTA start (before griddepcontrol.wait when the previous launch on the
+//     stream wrote none of this call's cache), and stay resident: no ring, no refill round trip;
+//   - both contractions are GEMVs (one query row) on the CUDA cores. Warp w owns slots
+//     [32 w, 32 w + 32) and waits only for their copies; lane l owns columns [4 l, 4 l + 4) of a
+//     row (one 8-byte shared load per row, conflict-free). The 32 partial dot products of a lane
+//     are reduced across the warp by a butterfly reduce-scatter (16 + 8 + 4 + 2 + 1 shuffles) that
+//     leaves lane l holding slot 32 w + l's logit, so thread j holds slot j for the softmax, the
+//     score update and the victim search without a trip through shared memory;
+//   - the softmax needs one block barrier: each warp publishes its (max, sum of exp) pair;
+//   - with a next-call hint (h2o_decode_step_prefetch) the CTA asks L2 for the next call's rows of
+//     its unit once its own critical reads are issued, so the next launch's copies hit L2.
+// Two CTAs fit on an SM (<= 108 KB each), so the next launch's CTAs start, and fetch their cache,
+// while this one runs.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "h2o_internal.cuh"
+
+namespace h2o {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kRowBytes = kD * 2;            // one bf16 K or V row
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBlockRows = 32;               // slots per warp, per bulk copy and per mbarrier
+constexpr int kMaxSlots = 208;
+constexpr int kMaxBlocks = (kMaxSlots + kBlockRows - 1) / kBlockRows;
+static_assert(kMaxBlocks <= kWarps, "one warp per block of slots");
+
+// Shared memory: K rows [budget], V rows [budget], per-warp output partials [kWarps][kD] (f32),
+// per-warp softmax pairs and eviction keys, the new token's rows, 2 x kWarps + 1 mbarriers.
+struct Layout {
+  int k, v, part, red, tok, bars, total;
+};
+
+__host__ __device__ inline Layout resident_layout(int budget) {
+  Layout L;
+  L.k = 0;
+  L.v = budget * kRowBytes;
+  L.part = 2 * budget * kRowBytes;
+  L.red = L.part + kWarps * kD * 4;   // m[kWarps], l[kWarps] (f32), key[kWarps] (u64), slot[kWarps]
+  L.tok = L.red + kWarps * 20;        // the new token's q, k_new and v_new rows
+  L.bars = L.tok + 3 * kRowBytes;
+  L.total = L.bars + (2 * kWarps + 1) * 8;
+  return L;
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_line_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+// Four bf16 (two 32-bit words) as floats.
+__device__ __forceinline__ void unpack4(const uint2& r, float* f) {
+  f[0] = bf16_lo(r.x);
+  f[1] = bf16_hi(r.x);
+  f[2] = bf16_lo(r.y);
+  f[3] = bf16_hi(r.y);
+}
+// q . k over 4 columns: bf16 inputs, f32 products and sums (fma.rn.f32.bf16 takes the bf16
+// operands exactly, so this is the fp32 dot product of the stored values, one rounding per fma).
+__device__ __forceinline__ float dot4_bf16(uint2 k, unsigned short q0, unsigned short q1, unsigned short q2,
+                                           unsigned short q3) {
+  float r;
+  asm("{\n .reg .b16 k0, k1, k2, k3;\n mov.b32 {k0, k1}, %1;\n mov.b32 {k2, k3}, %2;\n"
+      " fma.rn.f32.bf16 %0, %3, k0, 0f00000000;\n fma.rn.f32.bf16 %0, %4, k1, %0;\n"
+      " fma.rn.f32.bf16 %0, %5, k2, %0;\n fma.rn.f32.bf16 %0, %6, k3, %0;\n}"
+      : "=f"(r)
+      : "r"(k.x), "r"(k.y), "h"(q0), "h"(q1), "h"(q2), "h"(q3));
+  return r;
+}
+// Two fp32 fmas in one instruction (each lane of the pair rounded as fmaf).
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Butterfly reduce-scatter: on entry lane l holds v[i], its share of row i's sum (i < 32); on exit
+// v[0] of lane l is the warp-wide sum for row l. At step h each lane keeps the half of its rows
+// whose index has bit h equal to its own lane bit h and adds the partner's share of those rows.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) {
+    const bool upper = (lane & h) != 0;
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = upper ? v[j] : v[j + h];
+      const float keep = upper ? v[j + h] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int unit = static_cast<int>(blockIdx.x);
+  const int B = p.budget, n = p.n;
+  const int blocks = (n + kBlockRows - 1) / kBlockRows;
+  const Layout L = resident_layout(B);
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* red_m = reinterpret_cast<float*>(smem + L.red);
+  float* red_l = red_m + kWarps;
+  unsigned long long* red_key = reinterpret_cast<unsigned long long*>(red_l + kWarps);
+  int32_t* red_slot = reinterpret_cast<int32_t*>(red_key + kWarps);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* vbar = kbar + kWarps;
+  uint64_t* tbar = vbar + kWarps;  // the new token's rows
+  const uint32_t tok = smem_u32(smem + L.tok);
+  const size_t row0 = static_cast<size_t>(unit) * B;
+  const int j = tid;  // the slot this thread holds (valid if j < n)
+  const bool mine = warp < blocks;  // this warp's block of slots holds cached rows
+  const bool cache_full = n == B;
+
+  if (tid == 0) {
+    for (int b = 0; b < 2 * kWarps + 1; ++b) mbar_init(&kbar[b], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // The unit's K rows, then its V rows, 32 rows per copy; the scores and positions of slot j.
+  auto fetch = [&]() {
+    if (tid == 0) {
+      const unsigned char* ksrc = static_cast<const unsigned char*>(p.k_cache) + row0 * kRowBytes;
+      const unsigned char* vsrc = static_cast<const unsigned char*>(p.v_cache) + row0 * kRowBytes;
+      for (int b = 0; b < blocks; ++b) {
+        const uint32_t bytes = static_cast<uint32_t>(min(kBlockRows, n - b * kBlockRows) * kRowBytes);
+        mbar_expect_tx(&kbar[b], bytes);
+        bulk_g2s(smem + L.k + b * kBlockRows * kRowBytes, ksrc + b * kBlockRows * kRowBytes, bytes, &kbar[b]);
+      }
+      for (int b = 0; b < blocks; ++b) {
+        const uint32_t bytes = static_cast<uint32_t>(min(kBlockRows, n - b * kBlockRows) * kRowBytes);
+        mbar_expect_tx(&vbar[b], bytes);
+        bulk_g2s(smem + L.v + b * kBlockRows * kRowBytes, vsrc + b * kBlockRows * kRowBytes, bytes, &vbar[b]);
+      }
+    }
+  };
+  float sc = 0.f;
+  int32_t sp = 0;
+  if (p.early != 0) {  // the previous launch on the stream wrote none of this call's cache arrays
+    fetch();
+    if (j < n) {
+      sc = p.scores[row0 + j];
+      sp = p.slot_pos[row0 + j];
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
+    pdl_launch_dependents();
+    fetch();
+    if (j < n) {
+      sc = p.scores[row0 + j];
+      sp = p.slot_pos[row0 + j];
+    }
+  }
+
+  // D1: the new token's q, k_new and v_new rows, copied into shared memory (no warp waits on a
+  // register load); every warp forms s_new = q . k_new itself. Then the next call's rows of this
+  // unit are asked of L2 (a hint only: nothing here reads them), issued by the same thread after the
+  // new token's copies, which are on this step's critical path and so go to HBM first.
+  if (tid == 0) {
+    const size_t urow = static_cast<size_t>(unit) * kRowBytes;
+    mbar_expect_tx(tbar, 3 * kRowBytes);
+    bulk_g2s(smem + L.tok, static_cast<const unsigned char*>(p.q) + urow, kRowBytes, tbar);
+    bulk_g2s(smem + L.tok + kRowBytes, static_cast<const unsigned char*>(p.k_new) + urow, kRowBytes, tbar);
+    bulk_g2s(smem + L.tok + 2 * kRowBytes, static_cast<const unsigned char*>(p.v_new) + urow, kRowBytes, tbar);
+    if (p.next_k_cache != nullptr) {
+      const size_t off = row0 * kRowBytes;
+      bulk_prefetch_l2(static_cast<const unsigned char*>(p.next_k_cache) + off, static_cast<uint32_t>(B * kRowBytes));
+      bulk_prefetch_l2(static_cast<const unsigned char*>(p.next_v_cache) + off, static_cast<uint32_t>(B * kRowBytes));
+    }
+  }
+  if (warp == 1 && p.next_k_cache != nullptr) {
+    for (int o = lane * 128; o < B * 4; o += 32 * 128) {
+      prefetch_line_l2(reinterpret_cast<const unsigned char*>(p.next_scores + row0) + o);
+      prefetch_line_l2(reinterpret_cast<const unsigned char*>(p.next_slot_pos + row0) + o);
+    }
+  }
+  bool ok = mbar_wait(tbar, 0, p.err);
+  float qf[4], kf[4];
+  const uint2 q_raw = lds64(tok + lane * 8);
+  unpack4(q_raw, qf);
+  const unsigned short q16[4] = {static_cast<unsigned short>(q_raw.x & 0xffffu), static_cast<unsigned short>(q_raw.x >> 16),
+                                 static_cast<unsigned short>(q_raw.y & 0xffffu), static_cast<unsigned short>(q_raw.y >> 16)};
+  unpack4(lds64(tok + kRowBytes + lane * 8), kf);
+  const float s_new = warp_sum(qf[0] * kf[0] + qf[1] * kf[1] + qf[2] * kf[2] + qf[3] * kf[3]) * p.scale;
+
+  // D2: logits of this warp's 32 slots once their K rows have landed.
+  // Rows past the block's last cached slot re-read that slot (no branch per row, every load stays
+  // inside the copied rows); their logits are dropped and their weights are zero.
+  const int rows = min(kBlockRows, n - warp * kBlockRows);  // >= 1 for this warp's block
+  float s = -INFINITY;  // slot j's logit
+  if (mine) {
+    if (ok) ok = mbar_wait(&kbar[warp], 0, p.err);
+    const uint2* krow = reinterpret_cast<const uint2*>(smem + L.k + warp * kBlockRows * kRowBytes) + lane;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = dot4_bf16(krow[(i < rows ? i : rows - 1) * (kRowBytes / 8)], q16[0], q16[1], q16[2], q16[3]);
+    }
+    const float dot = reduce_scatter32(v, lane);
+    if (j < n) s = dot * p.scale;
+  }
+
+  // D3: softmax over the n slots and the new token. Each warp publishes (its max, its sum of
+  // exp(s - max)); every thread combines the pairs into the block's max m and normaliser l.
+  float mw = warp_max(warp == 0 ? fmaxf(s, s_new) : s);
+  float ew = (j < n) ? expf(s - mw) : 0.f;
+  if (warp == 0 && lane == 0) ew += expf(s_new - mw);
+  ew = warp_sum(ew);
+  if (lane == 0) {
+    red_m[warp] = mw;
+    red_l[warp] = ew;
+  }
+  __syncthreads();
+  float m = red_m[0];
+#pragma unroll
+  for (int w2 = 1; w2 < kWarps; ++w2) m = fmaxf(m, red_m[w2]);
+  float l = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < kWarps; ++w2) l = fmaf(red_l[w2], expf(red_m[w2] - m), l);
+  const float wj = (j < n) ? expf(s - m) : 0.f;  // slot j's unnormalised weight
+  const float w_new = expf(s_new - m);
+
+  // D4: this warp's share of sum_j w_j V_j: lane l accumulates columns [4 l, 4 l + 4).
+  if (mine) {
+    unsigned long long a01 = 0ull, a23 = 0ull;  // columns (4 l, 4 l + 1) and (4 l + 2, 4 l + 3)
+    if (ok) ok = mbar_wait(&vbar[warp], 0, p.err);
+    const uint2* vrow = reinterpret_cast<const uint2*>(smem + L.v + warp * kBlockRows * kRowBytes) + lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float wr = __shfl_sync(0xffffffffu, wj, i);  // 0 for rows past the last cached slot
+      const uint2 raw = vrow[(i < rows ? i : rows - 1) * (kRowBytes / 8)];
+      const unsigned long long w2 = pack2(wr, wr);
+      a01 = ffma2(w2, pack2(bf16_lo(raw.x), bf16_hi(raw.x)), a01);
+      a23 = ffma2(w2, pack2(bf16_lo(raw.y), bf16_hi(raw.y)), a23);
+    }
+    *reinterpret_cast<ulonglong2*>(part + warp * kD + lane * 4) = make_ulonglong2(a01, a23);
+  }
+
+  // D5 + D6: p_j, the updated score of slot j and the block's eviction key.
+  const int32_t last_candidate = p.position - p.k_local;
+  unsigned long long best = ~0ull;
+  float ns = 0.f;
+  if (j < n) {
+    const float pr = wj / l;
+    ns = p.policy == H2O_POLICY_TOPK ? pr : sc + pr;  // Top-K: this step's weight
+    bool cand = false;
+    const unsigned long long key = policy_key(p.policy, ns, sp, last_candidate, p.n_sink, p.stride, &cand);
+    if (cache_full && cand) best = key;
+  }
+  int32_t best_slot = best == ~0ull ? -1 : j;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
+    const int32_t os = __shfl_xor_sync(0xffffffffu, best_slot, off);
+    if (ob < best) {
+      best = ob;
+      best_slot = os;
+    }
+  }
+  if (lane == 0) {
+    red_key[warp] = best;
+    red_slot[warp] = best_slot;
+  }
+  __syncthreads();  // output partials and eviction keys complete
+  unsigned long long vkey = ~0ull;
+  int32_t victim = -1;
+#pragma unroll
+  for (int w2 = 0; w2 < kWarps; ++w2)
+    if (red_key[w2] < vkey) {
+      vkey = red_key[w2];
+      victim = red_slot[w2];
+    }
+  if (!cache_full) {
+    victim = -1;
+    vkey = ~0ull;
+  } else if (tid == 0 && victim < 0) {
+    atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
+  }
+  const float p_new = w_new / l;
+  if (j < kD) {
+    float o = 0.f;
+    for (int w2 = 0; w2 < blocks; ++w2) o += part[w2 * kD + j];
+    const float vn_j = bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(smem + L.tok + 2 * kRowBytes + 2 * j)));
+    o = fmaf(w_new, vn_j, o);
+    static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(unit) * kD + j] = __float2bfloat16_rn(o / l);
+  }
+
+  // D7: the score table written back, the new token in its slot (warp 0 writes K, warp 1 V).
+  if (j < n) p.scores[row0 + j] = (j == victim) ? p_new : ns;
+  const int32_t target = cache_full ? victim : n;
+  if (target >= 0 && ok) {
+    const size_t trow = row0 + static_cast<size_t>(target);
+    if (warp < 2)
+      *reinterpret_cast<uint2*>(static_cast<unsigned char*>(warp == 0 ? p.k_cache : p.v_cache) + trow * kRowBytes + lane * 8) =
+          lds64(tok + (1 + warp) * kRowBytes + lane * 8);
+    if (tid == 0) {
+      p.slot_pos[trow] = p.position;
+      if (!cache_full) p.scores[trow] = p_new;
+    }
+  }
+  if (tid == 0) {
+    p.evicted_slot[unit] = cache_full ? victim : -1;
+    p.evicted_pos[unit] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
+  }
+}
+
+}  // namespace
+
+bool decode_resident_supported(int head_dim, int dtype, int budget) {
+  return head_dim == kD && dtype == H2O_BF16 && budget >= 1 && budget <= kMaxSlots;
+}
+
+cudaError_t launch_decode_resident(const DecodeParams& p, cudaStream_t stream) {
+  const void* fn = reinterpret_cast<const void*>(h2o_decode_resident_kernel);
+  {  // opt in to more than 48 KB of dynamic shared memory, once per device
+    static std::mutex mu;
+    static std::vector<int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    bool found = false;
+    for (int d : done) found = found || d == dev;
+    if (!found) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, resident_layout(kMaxSlots).total);
+      if (e != cudaSuccess) return e;
+      done.push_back(dev);
+    }
+  }
+  DecodeParams q = p;
+  return launch_pdl(fn, p.units, kThreads, resident_layout(p.budget).total, stream, &q);
+}
+
+}  // namespace h2o

@@ -79,6 +79,8 @@ struct TcDecodeParams {
   float scale;
   int32_t policy, n_sink, stride;  // eviction policy (h2o_policy_kind)
   int32_t early;                   // cache reads may start before griddepcontrol.wait (DecodeParams)
+  const unsigned char* next_k;     // the next decode call's caches (an L2 prefetch hint), or null
+  const unsigned char* next_v;
 };
 
 // ---- PTX wrappers (same encodings as the prefill's tcgen05 path) -------------------------------
@@ -633,6 +635,14 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
   const int rows = max(0, min(p.n - c0, sp_.chunk));
   const int T = (rows + kTileRows - 1) / kTileRows;
   constexpr uint32_t kCols = 128;
+  // One CTA per unit with a next-call hint: the next call's rows of this unit are asked of L2 first
+  // (a prefetch only; nothing here reads them), so the next launch's tiles hit L2.
+  if (splits == 1 && p.next_k != nullptr && warp == kTmaWarp && lane == 0) {
+    const size_t off = static_cast<size_t>(unit) * p.budget * kD * 2;
+    const uint32_t bytes = static_cast<uint32_t>(p.budget) * kD * 2;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.next_k + off), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.next_v + off), "r"(bytes) : "memory");
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kSplitStages; ++s) {
@@ -1039,6 +1049,8 @@ cudaError_t fill_params(const DecodeParams& dp, TcDecodeParams& p) {
   p.n_sink = dp.n_sink;
   p.stride = dp.stride;
   p.early = dp.early;
+  p.next_k = static_cast<const unsigned char*>(dp.next_k_cache);
+  p.next_v = static_cast<const unsigned char*>(dp.next_v_cache);
   return cudaSuccess;
 }
 

@@ -41,6 +41,10 @@ struct DecodeParams {
   float* v_scale;
   int32_t early;        // the previous decode launch on this stream wrote none of this call's cache
                         // arrays: their reads may start before griddepcontrol.wait
+  const void* next_k_cache;      // the next decode call's cache arrays on this stream (same shape),
+  const void* next_v_cache;      // for an L2 prefetch while this step runs; null: no hint
+  const float* next_scores;
+  const int32_t* next_slot_pos;
 };
 
 struct PrefillParams {
@@ -133,6 +137,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
 // Tensor-core decode step with each unit split over a CTA cluster (bf16, D = 128, few units).
 bool decode_tc_split_supported(int head_dim, int dtype, int units, int n);
 cudaError_t launch_decode_tc_split(const DecodeParams& p, cudaStream_t s);
+// One CTA per unit with the unit's K and V resident in shared memory (bf16, D = 128, budget <= 208).
+bool decode_resident_supported(int head_dim, int dtype, int budget);
+cudaError_t launch_decode_resident(const DecodeParams& p, cudaStream_t s);
 bool decode_e4m3_supported(int head_dim, int dtype, int budget);
 cudaError_t launch_decode_e4m3(const DecodeParams& p, cudaStream_t s);  // E4M3 caches
 int select_max_prompt();

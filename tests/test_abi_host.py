@@ -90,6 +90,25 @@ def test_decode_rejects_null_misaligned_and_position(lib):
         assert lib.h2o_decode_step(ctypes.byref(d), 10, *p, None) == h2o.ERR_INVALID_ARG
 
 
+def test_prefetch_hint_rejects_null_and_misaligned_members(lib):
+    """h2o_decode_step_prefetch checks the next-call hint before any CUDA call: every member
+    non-NULL, the K/V caches 16-byte aligned, scores and positions 4-byte aligned. (A good hint with
+    position 0 still fails on the position, so nothing is launched.)"""
+    d = dims()
+    ptrs = [4096 * (i + 1) for i in range(10)]
+    good = [1 << 20, 2 << 20, 3 << 20, 4 << 20]
+    call = lambda nxt, pos: lib.h2o_decode_step_prefetch(ctypes.byref(d), None, pos, *ptrs,
+                                                         ctypes.byref(h2o.NextCache(*nxt)), None)
+    assert call(good, 0) == h2o.ERR_INVALID_ARG
+    for i in range(4):
+        bad = list(good)
+        bad[i] = None
+        assert call(bad, 10) == h2o.ERR_INVALID_ARG
+        bad[i] = good[i] + (8 if i < 2 else 2)
+        assert call(bad, 10) == h2o.ERR_INVALID_ARG
+    assert lib.h2o_decode_step_prefetch(ctypes.byref(d), None, 0, *ptrs, None, None) == h2o.ERR_INVALID_ARG
+
+
 def test_prefill_rejects_bad_arguments(lib):
     d = dims()
     ws = h2o.h2o_prefill_workspace_bytes(d, 64)

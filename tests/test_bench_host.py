@@ -25,7 +25,9 @@ def test_decode_kernel_dispatch():
     assert k("opt-6.7b") == "h2o_decode_tc_kernel"             # 8192 units, k = 204
     assert k("llama-7b") == "h2o_decode_tc_kernel"             # 2048 units, k = 460
     assert k("opt-30b") == "h2o_decode_tc_kernel"              # 1792 units, k = 307
-    assert k("opt-6.7b", layers=1) == "h2o_decode_tc_split_kernel"  # 256 units: one layer
+    assert k("opt-6.7b", layers=1) == "h2o_decode_resident_kernel"  # 256 units: one layer
+    assert k("opt-6.7b", layers=1, budget=209, k_heavy=105) == "h2o_decode_tc_split_kernel"
+    assert k("opt-6.7b", layers=1, batch=4) == "h2o_decode_tc_split_kernel"  # 128 units < one per SM
     assert k("streaming") == "h2o_decode_tc_split_kernel"      # 32 units, k = 4096
     assert k("tiny") == "h2o_decode_step_kernel"               # fp32, D = 64
     assert bench.decode_kernel(W["opt-6.7b"], 152, e4m3=True)[0] == "h2o_decode_e4m3_kernel"

@@ -197,8 +197,9 @@ def test_full_size_workload_sampled_units(name, check):
 
 def test_per_layer_launch_shape():
     """One OPT-6.7B layer per launch (batch 8 x 32 heads = 256 units, k = 204), the shape of the
-    benchmark's per-layer decode timing: fewer than four units per SM, so the cluster-split tcgen05
-    kernel runs; the oracle follows 16 sampled units through every step."""
+    benchmark's per-layer decode timing: between one and four units per SM with a budget of at most
+    208, so the resident one-CTA-per-unit kernel runs; the oracle follows 16 sampled units through
+    every step."""
     w = W["opt-6.7b"].with_(layers=1, decode_steps=96)
     assert w.units == 256
     units = np.linspace(0, w.units - 1, 16).astype(int)
