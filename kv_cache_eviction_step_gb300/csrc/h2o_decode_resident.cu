@@ -14,11 +14,13 @@
 //     mbarrier each, issued at CTA start (before griddepcontrol.wait when the previous launch on the
 //     stream wrote none of this call's cache), and stay resident: no ring, no refill round trip;
 //   - both contractions are GEMVs (one query row) on the CUDA cores. Warp w owns slots
-//     [32 w, 32 w + 32) and waits only for their copies; lane l owns columns [4 l, 4 l + 4) of a
-//     row (one 8-byte shared load per row, conflict-free). The 32 partial dot products of a lane
-//     are reduced across the warp by a butterfly reduce-scatter (16 + 8 + 4 + 2 + 1 shuffles) that
-//     leaves lane l holding slot 32 w + l's logit, so thread j holds slot j for the softmax, the
-//     score update and the victim search without a trip through shared memory;
+//     [32 w, 32 w + 32) and waits only for their copies; a half-warp covers a 256-byte row, lane
+//     (hl, li) = (lane / 16, lane % 16) reading columns [8 li, 8 li + 8) of the rows of parity hl
+//     with one 16-byte shared load per row (conflict-free). The logits use fma.rn.f32.bf16 (bf16
+//     operands, fp32 products and sums); the 16 partial dot products of a lane are reduced across
+//     its half-warp by a butterfly reduce-scatter (8 + 4 + 2 + 1 shuffles) that leaves lane (hl, li)
+//     holding slot 32 w + 2 li + hl's logit, the slot it keeps for the softmax, the score update and
+//     the victim search. V^T w accumulates column pairs with fma.rn.f32x2;
 //   - the softmax needs one block barrier: each warp publishes its (max, sum of exp) pair;
 //   - with a next-call hint (h2o_decode_step_prefetch) the CTA asks L2 for the next call's rows of
 //     its unit once its own critical reads are issued, so the next launch's copies hit L2.
@@ -73,15 +75,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
-// Four bf16 (two 32-bit words) as floats.
-__device__ __forceinline__ void unpack4(const uint2& r, float* f) {
-  f[0] = bf16_lo(r.x);
-  f[1] = bf16_hi(r.x);
-  f[2] = bf16_lo(r.y);
-  f[3] = bf16_hi(r.y);
-}
-// q . k over 4 columns: bf16 inputs, f32 products and sums (fma.rn.f32.bf16 takes the bf16
-// operands exactly, so this is the fp32 dot product of the stored values, one rounding per fma).
 __device__ __forceinline__ float dot4_bf16(uint2 k, unsigned short q0, unsigned short q1, unsigned short q2,
                                            unsigned short q3) {
   float r;
@@ -112,12 +105,18 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Butterfly reduce-scatter: on entry lane l holds v[i], its share of row i's sum (i < 32); on exit
-// v[0] of lane l is the warp-wide sum for row l. At step h each lane keeps the half of its rows
-// whose index has bit h equal to its own lane bit h and adds the partner's share of those rows.
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+__device__ __forceinline__ float dot8_bf16(uint4 k, const unsigned short (&q)[8]) {
+  return dot4_bf16(make_uint2(k.x, k.y), q[0], q[1], q[2], q[3]) + dot4_bf16(make_uint2(k.z, k.w), q[4], q[5], q[6], q[7]);
+}
+
+// Butterfly reduce-scatter over groups of N lanes (lane bits below N): on entry lane l holds v[i],
+// its share of row i's sum (i < N); on exit v[0] of lane l is the group's sum for row l mod N. At
+// step h each lane keeps the half of its rows whose index has bit h equal to its own lane bit h and
+// adds the partner's share of those rows.
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 #pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) {
+  for (int h = N / 2; h >= 1; h >>= 1) {
     const bool upper = (lane & h) != 0;
 #pragma unroll
     for (int j = 0; j < h; ++j) {
@@ -146,7 +145,10 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   uint64_t* tbar = vbar + kWarps;  // the new token's rows
   const uint32_t tok = smem_u32(smem + L.tok);
   const size_t row0 = static_cast<size_t>(unit) * B;
-  const int j = tid;  // the slot this thread holds (valid if j < n)
+  // Lane (hl, li) = (lane / 16, lane % 16) works on columns [8 li, 8 li + 8) of its warp's rows with
+  // parity hl, and holds slot j = 32 warp + 2 li + hl (valid if j < n).
+  const int hl = lane >> 4, li = lane & 15;
+  const int j = warp * kBlockRows + 2 * li + hl;
   const bool mine = warp < blocks;  // this warp's block of slots holds cached rows
   const bool cache_full = n == B;
 
@@ -216,13 +218,16 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     }
   }
   bool ok = mbar_wait(tbar, 0, p.err);
-  float qf[4], kf[4];
-  const uint2 q_raw = lds64(tok + lane * 8);
-  unpack4(q_raw, qf);
-  const unsigned short q16[4] = {static_cast<unsigned short>(q_raw.x & 0xffffu), static_cast<unsigned short>(q_raw.x >> 16),
-                                 static_cast<unsigned short>(q_raw.y & 0xffffu), static_cast<unsigned short>(q_raw.y >> 16)};
-  unpack4(lds64(tok + kRowBytes + lane * 8), kf);
-  const float s_new = warp_sum(qf[0] * kf[0] + qf[1] * kf[1] + qf[2] * kf[2] + qf[3] * kf[3]) * p.scale;
+  const uint4 q_raw = *reinterpret_cast<const uint4*>(smem + L.tok + li * 16);
+  const unsigned short q16[8] = {
+      static_cast<unsigned short>(q_raw.x & 0xffffu), static_cast<unsigned short>(q_raw.x >> 16),
+      static_cast<unsigned short>(q_raw.y & 0xffffu), static_cast<unsigned short>(q_raw.y >> 16),
+      static_cast<unsigned short>(q_raw.z & 0xffffu), static_cast<unsigned short>(q_raw.z >> 16),
+      static_cast<unsigned short>(q_raw.w & 0xffffu), static_cast<unsigned short>(q_raw.w >> 16)};
+  float sn = dot8_bf16(*reinterpret_cast<const uint4*>(smem + L.tok + kRowBytes + li * 16), q16);
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) sn += __shfl_xor_sync(0xffffffffu, sn, off);  // over the 16 lanes
+  const float s_new = sn * p.scale;
 
   // D2: logits of this warp's 32 slots once their K rows have landed.
   // Rows past the block's last cached slot re-read that slot (no branch per row, every load stays
@@ -231,13 +236,14 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   float s = -INFINITY;  // slot j's logit
   if (mine) {
     if (ok) ok = mbar_wait(&kbar[warp], 0, p.err);
-    const uint2* krow = reinterpret_cast<const uint2*>(smem + L.k + warp * kBlockRows * kRowBytes) + lane;
-    float v[32];
+    const uint4* krow = reinterpret_cast<const uint4*>(smem + L.k + warp * kBlockRows * kRowBytes) + li;
+    float v[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = dot4_bf16(krow[(i < rows ? i : rows - 1) * (kRowBytes / 8)], q16[0], q16[1], q16[2], q16[3]);
+    for (int i = 0; i < 16; ++i) {
+      const int r = 2 * i + hl;
+      v[i] = dot8_bf16(krow[(r < rows ? r : rows - 1) * (kRowBytes / 16)], q16);
     }
-    const float dot = reduce_scatter32(v, lane);
+    const float dot = reduce_scatter<16>(v, li);
     if (j < n) s = dot * p.scale;
   }
 
@@ -261,20 +267,36 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   const float wj = (j < n) ? expf(s - m) : 0.f;  // slot j's unnormalised weight
   const float w_new = expf(s_new - m);
 
-  // D4: this warp's share of sum_j w_j V_j: lane l accumulates columns [4 l, 4 l + 4).
+  // D4: this warp's share of sum_j w_j V_j: lane (hl, li) accumulates columns [8 li, 8 li + 8) over
+  // the rows of parity hl (row 2 i + hl's weight is held by lane 16 hl + i), then the two halves add.
   if (mine) {
-    unsigned long long a01 = 0ull, a23 = 0ull;  // columns (4 l, 4 l + 1) and (4 l + 2, 4 l + 3)
+    unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};  // column pairs (8 li + 2 e, 8 li + 2 e + 1)
     if (ok) ok = mbar_wait(&vbar[warp], 0, p.err);
-    const uint2* vrow = reinterpret_cast<const uint2*>(smem + L.v + warp * kBlockRows * kRowBytes) + lane;
+    const uint4* vrow = reinterpret_cast<const uint4*>(smem + L.v + warp * kBlockRows * kRowBytes) + li;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float wr = __shfl_sync(0xffffffffu, wj, i);  // 0 for rows past the last cached slot
-      const uint2 raw = vrow[(i < rows ? i : rows - 1) * (kRowBytes / 8)];
+    for (int i = 0; i < 16; ++i) {
+      const int r = 2 * i + hl;
+      const float wr = __shfl_sync(0xffffffffu, wj, 16 * hl + i);  // 0 for rows past the last cached slot
+      const uint4 raw = vrow[(r < rows ? r : rows - 1) * (kRowBytes / 16)];
       const unsigned long long w2 = pack2(wr, wr);
-      a01 = ffma2(w2, pack2(bf16_lo(raw.x), bf16_hi(raw.x)), a01);
-      a23 = ffma2(w2, pack2(bf16_lo(raw.y), bf16_hi(raw.y)), a23);
+      a[0] = ffma2(w2, pack2(bf16_lo(raw.x), bf16_hi(raw.x)), a[0]);
+      a[1] = ffma2(w2, pack2(bf16_lo(raw.y), bf16_hi(raw.y)), a[1]);
+      a[2] = ffma2(w2, pack2(bf16_lo(raw.z), bf16_hi(raw.z)), a[2]);
+      a[3] = ffma2(w2, pack2(bf16_lo(raw.w), bf16_hi(raw.w)), a[3]);
     }
-    *reinterpret_cast<ulonglong2*>(part + warp * kD + lane * 4) = make_ulonglong2(a01, a23);
+    float o8[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      o8[2 * e] = __uint_as_float(static_cast<uint32_t>(a[e]));
+      o8[2 * e + 1] = __uint_as_float(static_cast<uint32_t>(a[e] >> 32));
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o8[e] += __shfl_xor_sync(0xffffffffu, o8[e], 16);
+    if (hl == 0) {
+      float4* dst = reinterpret_cast<float4*>(part + warp * kD + li * 8);
+      dst[0] = make_float4(o8[0], o8[1], o8[2], o8[3]);
+      dst[1] = make_float4(o8[4], o8[5], o8[6], o8[7]);
+    }
   }
 
   // D5 + D6: p_j, the updated score of slot j and the block's eviction key.
@@ -318,12 +340,12 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
   }
   const float p_new = w_new / l;
-  if (j < kD) {
+  if (tid < kD) {  // output element tid
     float o = 0.f;
-    for (int w2 = 0; w2 < blocks; ++w2) o += part[w2 * kD + j];
-    const float vn_j = bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(smem + L.tok + 2 * kRowBytes + 2 * j)));
-    o = fmaf(w_new, vn_j, o);
-    static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(unit) * kD + j] = __float2bfloat16_rn(o / l);
+    for (int w2 = 0; w2 < blocks; ++w2) o += part[w2 * kD + tid];
+    const float vn = bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(smem + L.tok + 2 * kRowBytes + 2 * tid)));
+    o = fmaf(w_new, vn, o);
+    static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(unit) * kD + tid] = __float2bfloat16_rn(o / l);
   }
 
   // D7: the score table written back, the new token in its slot (warp 0 writes K, warp 1 V).
