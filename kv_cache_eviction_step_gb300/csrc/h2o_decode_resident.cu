@@ -264,9 +264,12 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   float m = red_m[0];
 #pragma unroll
   for (int w2 = 1; w2 < kWarps; ++w2) m = fmaxf(m, red_m[w2]);
-  float l = 0.f;
+  // l = sum over warps of (their sum) exp(their max - m): lane k of each group of kWarps lanes takes
+  // warp k's term and three shuffles add them, so each thread evaluates one exp instead of kWarps
+  // (the sum is the same in every lane: each step adds the same pairs).
+  float l = red_l[lane % kWarps] * expf(red_m[lane % kWarps] - m);
 #pragma unroll
-  for (int w2 = 0; w2 < kWarps; ++w2) l = fmaf(red_l[w2], expf(red_m[w2] - m), l);
+  for (int off = 1; off < kWarps; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   const float wj = (j < n) ? expf(s - m) : 0.f;  // slot j's unnormalised weight
   const float w_new = expf(s_new - m);
 
