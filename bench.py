@@ -56,10 +56,24 @@ def decode_bytes_per_unit_e4m3(n: int, head_dim: int) -> int:
 
 
 class Calls:
-    """The library calls of one job, for the bf16 or the E4M3 cache."""
+    """The library calls of one job, for the bf16 or the E4M3 cache. A decode step is launched once
+    per layer (a model's forward pass has to: layer l + 1's query needs layer l's output) over that
+    layer's B x H units, the slice [l B H, (l + 1) B H) of every array; with a bf16 cache each launch
+    names the next launch's layer (the next step's layer 0 after the last layer) as the L2 prefetch
+    hint of h2o_decode_step_prefetch. decode_all_layers is the same step as one launch over all
+    units."""
 
-    def __init__(self, h2o, dims, cache, e4m3: bool):
+    def __init__(self, h2o, dims, cache, e4m3: bool, layers: int = 1):
         self.h2o, self.dims, self.cache, self.e4m3 = h2o, dims, cache, e4m3
+        self.L = layers
+        self.ul = dims.units // layers
+        self.dl = type(dims)(units_b=dims.units_b // layers, heads=dims.heads, head_dim=dims.head_dim,
+                             budget=dims.budget, k_heavy=dims.k_heavy, k_local=dims.k_local, dtype=dims.dtype)
+        self.sl = [slice(l * self.ul, (l + 1) * self.ul) for l in range(layers)]
+        c = cache
+        self.nxt = [None if e4m3 else h2o.next_cache(c.k_cache[self.sl[(l + 1) % layers]], c.v_cache[self.sl[(l + 1) % layers]],
+                                                     c.scores[self.sl[(l + 1) % layers]], c.slot_pos[self.sl[(l + 1) % layers]])
+                    for l in range(layers)]
 
     def prefill(self, P, q, k, v, stream):
         c = self.cache
@@ -70,7 +84,26 @@ class Calls:
             self.h2o.h2o_prefill_select(self.dims, P, q, k, v, c.k_cache, c.v_cache, c.scores, c.slot_pos,
                                         c.workspace, stream)
 
-    def decode(self, t, q, k_new, v_new, out, evs, evp, stream):
+    def decode(self, t, q, k_new, v_new, out, evs, evp, stream, last: bool = False, hint: bool = True):
+        """One decode step at position t, one launch per layer; ``last``: no later step follows (the
+        last launch names no next cache); ``hint``: name the next launch's cache."""
+        if self.L == 1:
+            return self.decode_all_layers(t, q, k_new, v_new, out, evs, evp, stream)
+        c, h2o = self.cache, self.h2o
+        for l, sl in enumerate(self.sl):
+            args = (q[sl], k_new[sl], v_new[sl], c.k_cache[sl], c.v_cache[sl])
+            if self.e4m3:
+                h2o.h2o_decode_step_e4m3(self.dl, None, t, *args, c.k_scale[sl], c.v_scale[sl], c.scores[sl],
+                                         c.slot_pos[sl], out[sl], evs[sl], evp[sl], stream)
+            elif hint:
+                nxt = None if (last and l == self.L - 1) else self.nxt[l]
+                h2o.h2o_decode_step_prefetch(self.dl, None, t, *args, c.scores[sl], c.slot_pos[sl], out[sl], evs[sl],
+                                             evp[sl], nxt, stream)
+            else:
+                h2o.h2o_decode_step(self.dl, t, *args, c.scores[sl], c.slot_pos[sl], out[sl], evs[sl], evp[sl],
+                                    stream)
+
+    def decode_all_layers(self, t, q, k_new, v_new, out, evs, evp, stream):
         c = self.cache
         if self.e4m3:
             self.h2o.h2o_decode_step_e4m3(self.dims, None, t, q, k_new, v_new, c.k_cache, c.v_cache,
@@ -295,11 +328,15 @@ def config_of(w: synth.Workload, args) -> dict:
             "kv_cache": ("E4M3 codes + float32 row scales (bf16 q/k/v/out)" if args.kv_cache == "e4m3"
                          else w.dtype),
             "l2": "no flush: KV cache and per-step inputs exceed the 129 MB L2",
-            "timing": "CUDA events between replays of two CUDA graphs per job (3 prefill launches, "
-                      "then the decode launches)",
-            "decode_launch": (f"one launch per step over all {w.units} units ({w.layers} layers x "
-                              f"{w.batch} x {w.heads} heads); one launch per layer per step is timed "
-                              f"separately as decode_per_layer" if w.layers > 1 else
+            "timing": "CUDA events between replays of CUDA graphs per job (3 prefill launches, then the "
+                      "decode launches)",
+            "decode_launch": (f"one launch per layer and step ({w.layers} launches per step of {w.batch} x "
+                              f"{w.heads} = {w.units // w.layers} units each"
+                              + ("" if args.kv_cache == "e4m3" else
+                                 ", each naming the next launch's layer as the L2 prefetch hint of "
+                                 "h2o_decode_step_prefetch")
+                              + "); all layers in one launch per step is timed separately as "
+                                "decode_all_layers" if w.layers > 1 else
                               f"one launch per step over all {w.units} units")}
 
 
@@ -318,7 +355,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill-forward", action="store_true")
     ap.add_argument("--no-per-layer", action="store_true",
-                    help="skip the decode timing with one launch per layer and step")
+                    help="skip the decode timings in the other launch shapes (all layers in one launch "
+                         "per step; one launch per layer without the prefetch hint)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads' decode / prefill timings in the default line")
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "e4m3"],
@@ -365,7 +403,8 @@ def main():
     if e4m3 and (w.dtype != "bf16" or D != 128):
         raise SystemExit("--kv-cache e4m3 needs a bf16 workload with head_dim 128")
     cache = h2o.H2OCache(dims, P, device=dev, e4m3=e4m3)
-    calls = Calls(h2o, dims, cache, e4m3)
+    L = w.layers
+    calls = Calls(h2o, dims, cache, e4m3, layers=L)
     out = torch.empty((S, U, D), dtype=tdt, device=dev)
     evs = torch.empty((S, U), dtype=torch.int32, device=dev)
     evp = torch.empty((S, U), dtype=torch.int32, device=dev)
@@ -377,7 +416,8 @@ def main():
 
     def decode_range(s0, s1):
         for s in range(s0, s1):
-            calls.decode(P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s], out[s], evs[s], evp[s], sp_ptr)
+            calls.decode(P + s, dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s], out[s], evs[s], evp[s], sp_ptr,
+                         last=s == S - 1)
 
     # One direct run initialises the library's per-device state (kernel attributes, launch plans,
     # error word) outside any capture; then the job is captured as two CUDA graphs (the prefill
@@ -390,10 +430,11 @@ def main():
     with torch.cuda.graph(g_pre, stream=stream):
         prefill()
     g_dec = []  # decode launches in graphs of at most GRAPH_STEPS launches
-    for s0 in range(0, S, GRAPH_STEPS):
+    steps_per_graph = max(1, GRAPH_STEPS // L)
+    for s0 in range(0, S, steps_per_graph):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            decode_range(s0, min(S, s0 + GRAPH_STEPS))
+            decode_range(s0, min(S, s0 + steps_per_graph))
         g_dec.append(g)
 
     def job(marks=None):
@@ -428,26 +469,28 @@ def main():
     if h2o.h2o_get_device_error(sp_ptr) != 0:
         raise RuntimeError("device error word set during the timed region")
 
-    # Per decode launch: the decode graph's duration over its S launches (includes the short
-    # launch-to-launch gaps inside the graph, so it slightly understates the kernel's own rate).
+    # Per decode step: the decode graphs' duration over the S steps (L launches each; includes the
+    # short launch-to-launch gaps inside the graphs, so it slightly understates the kernel's own rate).
     decode_ms = [rec[i][1].elapsed_time(rec[i][2]) / S for i in range(K) for _ in range(S)]
     prefill_ms = [rec[i][0].elapsed_time(rec[i][1]) for i in range(K)]
     ms_per_step = total_ms / K
     tokens_per_job = w.batch * S
     value = world * tokens_per_job * K / (total_ms / 1000.0)
 
-    # Roofline of the decode kernel (the dominant kernel).
+    # Roofline of the decode kernel (the dominant kernel): one launch = one layer's B x H units.
     peaks, peak_kind = measured_peaks()
-    bytes_per_launch = [U * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
-                             decode_bytes_per_unit(min(P + s, w.budget), D, eb)) for s in range(S)]
+    bytes_per_launch = [U // L * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
+                                  decode_bytes_per_unit(min(P + s, w.budget), D, eb)) for s in range(S)]
     avg_bytes = float(np.mean(bytes_per_launch))
-    avg_decode_s = float(np.mean(decode_ms)) / 1000.0
+    avg_decode_s = float(np.mean(decode_ms)) / 1000.0 / L
     achieved = avg_bytes / avg_decode_s / 1e9
-    kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count, e4m3)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kname, ksrc = decode_kernel(w.with_(layers=1), sms, e4m3)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc),
                 "kernel": kname, "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-                "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_decode_s * 1e6}
+                "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_decode_s * 1e6,
+                "units_per_launch": U // L}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -457,14 +500,15 @@ def main():
             "decode_tokens_per_s": world * tokens_per_job / (sum(decode_ms) / K / 1000.0),
             "prefill_ms": float(np.mean(prefill_ms)),
             "decode_ms_per_token_step": float(np.mean(decode_ms)),
-            "gpu_launches": K * (3 + S),
+            "gpu_launches": K * (3 + S * L),
             "clocks": clocks.summary(),
             "input_generation_s": t_gen}
 
-    # The same decode steps launched per layer, as a model's forward pass has to launch them.
+    # The same decode steps in the other launch shapes: all layers in one launch per step, and one
+    # launch per layer without the prefetch hint.
     if not args.no_per_layer and w.layers > 1:
-        line["decode_per_layer"] = decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream,
-                                                           dev, g_pre, args.warmup, K, e4m3)
+        line.update(other_launch_shapes(h2o, w, dv, calls, out, evs, evp, stream, dev, g_pre, args.warmup, K,
+                                        e4m3))
 
     # The prompt pass with the attention output (h2o_prefill_forward), timed on its own: not part of
     # the step above, which builds the cache only.
@@ -613,53 +657,34 @@ def other_workloads(h2o, dv_main, dev, warmup: int, reps: int) -> dict:
     return out
 
 
-def decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream, dev, g_pre, warmup: int,
-                            reps: int, e4m3: bool) -> dict:
-    """The decode steps with one launch per layer and step (a model cannot batch its layers: layer
-    l + 1's query needs layer l's output), against the all-layers launch of the main timing. Layer l's
-    units are the contiguous slice [l B H, (l + 1) B H) of every array; the launches are captured in
-    CUDA graphs of at most GRAPH_STEPS launches, the cache is rebuilt by the prefill graph before
-    each replay (untimed), and CUDA events bracket the decode graphs."""
+def other_launch_shapes(h2o, w, dv, calls, out, evs, evp, stream, dev, g_pre, warmup: int, reps: int,
+                        e4m3: bool) -> dict:
+    """The main timing's decode steps in the other launch shapes, each captured in CUDA graphs of at
+    most GRAPH_STEPS launches and timed with CUDA events around the decode graphs (the cache rebuilt
+    by the prefill graph before each replay, untimed): all layers' units in one launch per step (the
+    multi-layer decode), and, for bf16 caches, one launch per layer without the prefetch hint."""
     import torch
-    L, P, S, D = w.layers, w.prompt_len, w.decode_steps, w.head_dim
-    ul = w.units // L
-    dl = type(dims)(units_b=dims.units_b // L, heads=dims.heads, head_dim=dims.head_dim,
-                    budget=dims.budget, k_heavy=dims.k_heavy, k_local=dims.k_local, dtype=dims.dtype)
-    c, sp = calls.cache, stream.cuda_stream
+    L, P, S, D, U = w.layers, w.prompt_len, w.decode_steps, w.head_dim, w.units
+    sp = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = measured_peaks()[0]["hbm_gbs"]
+    eb = 2 if w.dtype == "bf16" else 4
+    unit_bytes = float(np.mean([decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
+                                decode_bytes_per_unit(min(P + s, w.budget), D, eb) for s in range(S)]))
 
-    order = [(s, l) for s in range(S) for l in range(L)]
-
-    def launch(i, hint):
-        s, l = order[i]
-        sl = slice(l * ul, (l + 1) * ul)
-        args = (dv["q_dec"][s][sl], dv["k_dec"][s][sl], dv["v_dec"][s][sl], c.k_cache[sl], c.v_cache[sl])
-        if e4m3:
-            h2o.h2o_decode_step_e4m3(dl, None, P + s, *args, c.k_scale[sl], c.v_scale[sl], c.scores[sl],
-                                     c.slot_pos[sl], out[s][sl], evs[s][sl], evp[s][sl], sp)
-        elif hint:  # the next launch's layer (the next step's layer 0 after the last layer)
-            nxt = None
-            if i + 1 < len(order):
-                nl = order[i + 1][1]
-                ns = slice(nl * ul, (nl + 1) * ul)
-                nxt = h2o.next_cache(c.k_cache[ns], c.v_cache[ns], c.scores[ns], c.slot_pos[ns])
-            h2o.h2o_decode_step_prefetch(dl, None, P + s, *args, c.scores[sl], c.slot_pos[sl], out[s][sl],
-                                         evs[s][sl], evp[s][sl], nxt, sp)
-        else:
-            h2o.h2o_decode_step(dl, P + s, *args, c.scores[sl], c.slot_pos[sl], out[s][sl], evs[s][sl],
-                                evp[s][sl], sp)
-
-    def timed(hint):
+    def timed(step, launches_per_step):
         with torch.cuda.stream(stream):  # one direct pass sets up the per-shape launch plans
             g_pre.replay()
-            for i in range(len(order)):
-                launch(i, hint)
+            for s in range(S):
+                step(s)
         torch.cuda.synchronize(dev)
         graphs = []
-        for i0 in range(0, len(order), GRAPH_STEPS):
+        per_graph = max(1, GRAPH_STEPS // launches_per_step)
+        for s0 in range(0, S, per_graph):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for i in range(i0, min(i0 + GRAPH_STEPS, len(order))):
-                    launch(i, hint)
+                for s in range(s0, min(S, s0 + per_graph)):
+                    step(s)
             graphs.append(g)
         ms = []
         for i in range(warmup + reps):
@@ -674,32 +699,32 @@ def decode_per_layer_timing(h2o, dims, w, dv, calls, out, evs, evp, stream, dev,
             if i >= warmup:
                 ms.append(e0.elapsed_time(e1))
         if h2o.h2o_get_device_error(sp) != 0:
-            raise RuntimeError("device error word set during the per-layer decode timing")
+            raise RuntimeError("device error word set during the launch-shape timings")
         return float(np.median(ms))
 
-    eb = 2 if w.dtype == "bf16" else 4
-    step_bytes = float(np.mean([w.units * (decode_bytes_per_unit_e4m3(min(P + s, w.budget), D) if e4m3 else
-                                           decode_bytes_per_unit(min(P + s, w.budget), D, eb))
-                                for s in range(S)]))
-    kname = decode_kernel(w.with_(layers=1), torch.cuda.get_device_properties(dev).multi_processor_count,
-                          e4m3)[0]
-    peak = measured_peaks()[0]["hbm_gbs"]
+    def entry(ms, launches_per_step, kernel, call, traffic=None):
+        us_launch = ms * 1000.0 / S / launches_per_step
+        gbs = U / launches_per_step * unit_bytes / (us_launch * 1e-6) / 1e9
+        return {"kernel": kernel, "call": call, "launches_per_step": launches_per_step,
+                "units_per_launch": U // launches_per_step, "us_per_launch": us_launch,
+                "decode_tokens_per_s": w.batch * S / (ms / 1000.0), "kv_read_gbs": gbs, "frac": gbs / peak,
+                "traffic": traffic}
 
-    def entry(ms, call):
-        us = ms * 1000.0 / S
-        return {"us_per_step": us, "us_per_launch": us / L,
-                "decode_tokens_per_s": w.batch * S / (ms / 1000.0),
-                "kv_read_gbs": step_bytes / (us * 1e-6) / 1e9,
-                "frac": step_bytes / (us * 1e-6) / 1e9 / peak, "call": call}
+    def io(s):
+        return dv["q_dec"][s], dv["k_dec"][s], dv["v_dec"][s], out[s], evs[s], evp[s], sp
 
-    res = {"launches_per_step": L, "units_per_launch": ul, "kernel": kname}
-    if e4m3:
-        res.update(entry(timed(False), "h2o_decode_step_e4m3"))
-    else:  # the hinted call is how a model launches the step per layer; the plain call beside it
-        res.update(entry(timed(True), "h2o_decode_step_prefetch (next layer's cache named)"))
-        res["plain"] = entry(timed(False), "h2o_decode_step")
-    res["how"] = ("per step, one decode launch per layer over its batch x heads units, in CUDA graphs; "
-                  "median over the timed replays; cache rebuilt by the prefill between replays (untimed)")
+    res = {}
+    kname, ksrc = decode_kernel(w, sms, e4m3)
+    res["decode_all_layers"] = entry(
+        timed(lambda s: calls.decode_all_layers(P + s, *io(s)), 1), 1, kname,
+        "h2o_decode_step_e4m3" if e4m3 else "h2o_decode_step", recorded_traffic(w.name, kname, ksrc))
+    if not e4m3:
+        res["decode_per_layer_plain"] = entry(
+            timed(lambda s: calls.decode(P + s, *io(s), hint=False), L), L,
+            decode_kernel(w.with_(layers=1), sms)[0], "h2o_decode_step")
+    for v in res.values():
+        v["how"] = ("CUDA graphs of the decode launches, CUDA events around them; median over the timed "
+                    "replays; cache rebuilt by the prefill between replays (untimed)")
     return res
 
 
@@ -753,7 +778,10 @@ def e2e(args, w, calls, host, stream, dev, world, tokens_per_job):
     """The job end to end through the public API from pinned host buffers. Three streams: host->device
     copies, the library calls, device->host copies. Device inputs and outputs are double-buffered,
     so job j + 1's inputs are copied while job j decodes; each copy waits only for the launches that
-    last used its buffer (events), and each decode chunk waits only for its own inputs."""
+    last used its buffer (events), and each decode chunk waits only for its own inputs. The library
+    calls of each buffer set (the prefill, and each chunk's steps of one launch per layer) are
+    captured once into CUDA graphs, as a serving loop would, and replayed every job: the 16,384
+    per-layer calls of a job would otherwise be bound by the host."""
     import torch
     U, D, P, S = w.units, w.head_dim, w.prompt_len, w.decode_steps
     tdt = calls.cache.dtype
@@ -779,6 +807,35 @@ def e2e(args, w, calls, host, stream, dev, world, tokens_per_job):
         e.record(on)
         return e
 
+    def issue_prefill(b):
+        d = b["in"]
+        calls.prefill(P, d["q_prompt"], d["k_prompt"], d["v_prompt"], sp)
+
+    def issue_chunk(b, c0):
+        d = b["in"]
+        for s in range(c0, min(S, c0 + chunk)):
+            calls.decode(P + s, d["q_dec"][s], d["k_dec"][s], d["v_dec"][s], b["out"][s], b["evs"][s], b["evp"][s],
+                         sp, last=s == S - 1)
+
+    for b in sets:  # real inputs in both sets, one direct run each, then the graphs
+        for k in host:
+            b["in"][k].copy_(host[k])
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            issue_prefill(b)
+            for c0 in chunks:
+                issue_chunk(b, c0)
+        torch.cuda.synchronize(dev)
+        b["g_pre"] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(b["g_pre"], stream=stream):
+            issue_prefill(b)
+        b["g_chunks"] = []
+        for c0 in chunks:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue_chunk(b, c0)
+            b["g_chunks"].append(g)
+
     def job(j):
         b = sets[j % 2]
         d = b["in"]
@@ -796,12 +853,12 @@ def e2e(args, w, calls, host, stream, dev, world, tokens_per_job):
         stream.wait_event(prompt_ready)
         if b["outputs_free"] is not None:
             stream.wait_event(b["outputs_free"])
-        calls.prefill(P, d["q_prompt"], d["k_prompt"], d["v_prompt"], sp)
+        with torch.cuda.stream(stream):
+            b["g_pre"].replay()
         for ci, c0 in enumerate(chunks):
             stream.wait_event(ready[ci])
-            for s in range(c0, min(S, c0 + chunk)):
-                calls.decode(P + s, d["q_dec"][s], d["k_dec"][s], d["v_dec"][s], b["out"][s], b["evs"][s],
-                             b["evp"][s], sp)
+            with torch.cuda.stream(stream):
+                b["g_chunks"][ci].replay()
             done = event(stream)
             d2h_s.wait_event(done)
             with torch.cuda.stream(d2h_s):
@@ -828,7 +885,9 @@ def e2e(args, w, calls, host, stream, dev, world, tokens_per_job):
             "how": "pinned host inputs copied per job on a host-to-device stream in 64-step chunks, the "
                    "outputs and eviction indices back per chunk on a device-to-host stream; device "
                    "buffers double-buffered so the next job's inputs arrive during this job's decode; "
-                   "host wall clock around the jobs, synchronised at both ends"}
+                   "the library calls of each buffer set captured once into CUDA graphs (prefill, and "
+                   "per chunk the steps' per-layer launches) and replayed per job; host wall clock "
+                   "around the jobs, synchronised at both ends"}
 
 if __name__ == "__main__":
     main()
