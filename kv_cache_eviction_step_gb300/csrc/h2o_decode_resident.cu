@@ -21,11 +21,12 @@
 //     its half-warp by a butterfly reduce-scatter (8 + 4 + 2 + 1 shuffles) that leaves lane (hl, li)
 //     holding slot 32 w + 2 li + hl's logit, the slot it keeps for the softmax, the score update and
 //     the victim search. V^T w accumulates column pairs with fma.rn.f32x2;
-//   - the softmax needs one block barrier: each warp publishes its (max, sum of exp) pair;
+//   - the softmax needs one block barrier: each warp publishes its (max, sum of exp) pair, and every
+//     lane forms the normaliser from them with one exp and a 3-shuffle sum;
 //   - with a next-call hint (h2o_decode_step_prefetch) the CTA asks L2 for the next call's rows of
 //     its unit once its own critical reads have arrived, so the next launch's copies hit L2.
-// Two CTAs fit on an SM (<= 108 KB each), so the next launch's CTAs start, and fetch their cache,
-// while this one runs.
+// Two CTAs fit on an SM (at most 109 KiB of shared memory each, at 208 slots), so the next launch's
+// CTAs start, and fetch their cache, while this one runs.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -57,8 +58,9 @@ __host__ __device__ inline Layout resident_layout(int budget) {
   L.k = 0;
   L.v = budget * kRowBytes;
   L.part = 2 * budget * kRowBytes;
-  L.red = L.part + kWarps * kD * 4;   // m[kWarps], l[kWarps] (f32), key[kWarps] (u64), slot[kWarps]
-  L.tok = L.red + kWarps * 20;        // the new token's q, k_new and v_new rows
+  L.red = L.part + kWarps * kD * 4;   // m[kWarps], l[kWarps] (f32), key[kWarps] (u64), slot[kWarps],
+                                      // then a flag: some wait of this CTA gave up
+  L.tok = L.red + kWarps * 20 + 16;   // the new token's q, k_new and v_new rows
   L.bars = L.tok + 3 * kRowBytes;
   L.total = L.bars + (2 * kWarps + 1) * 8;
   return L;
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   float* red_l = red_m + kWarps;
   unsigned long long* red_key = reinterpret_cast<unsigned long long*>(red_l + kWarps);
   int32_t* red_slot = reinterpret_cast<int32_t*>(red_key + kWarps);
+  int32_t* gave_up = red_slot + kWarps;
   uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* vbar = kbar + kWarps;
   uint64_t* tbar = vbar + kWarps;  // the new token's rows
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   if (tid == 0) {
     for (int b = 0; b < 2 * kWarps + 1; ++b) mbar_init(&kbar[b], 1);
     fence_mbar_init();
+    *gave_up = 0;
   }
   __syncthreads();
 
@@ -330,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     red_key[warp] = best;
     red_slot[warp] = best_slot;
   }
-  __syncthreads();  // output partials and eviction keys complete
+  if (!ok) *gave_up = 1;
+  __syncthreads();  // output partials and eviction keys complete (and every wait of the CTA is over)
   unsigned long long vkey = ~0ull;
   int32_t victim = -1;
 #pragma unroll
@@ -370,6 +375,15 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   if (tid == 0) {
     p.evicted_slot[unit] = cache_full ? victim : -1;
     p.evicted_pos[unit] = (cache_full && victim >= 0) ? static_cast<int32_t>(vkey & 0xffffffffu) : -1;
+    // If a wait above gave up, a copy may still be landing in this CTA's shared memory: keep the CTA
+    // until every copy it issued has completed (a second bounded window).
+    if (*gave_up) {
+      for (int b = 0; b < blocks; ++b) {
+        (void)mbar_wait(&kbar[b], 0, p.err, 8000000000ull);
+        (void)mbar_wait(&vbar[b], 0, p.err, 8000000000ull);
+      }
+      (void)mbar_wait(tbar, 0, p.err, 8000000000ull);
+    }
   }
 }
 
