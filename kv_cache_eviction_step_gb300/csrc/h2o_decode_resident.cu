@@ -10,17 +10,18 @@
 // Why a kernel of its own. A launch of 256 units of 204 slots carries 27.8 MB, ~4 us of HBM time,
 // so it is bound by what happens around the previous launch: when its CTAs can start, when their
 // data arrives, and the chain of dependent steps once the query is there. Here:
-//   - the unit's K and V (n rows each, <= 208 x 256 B) are fetched by bulk copies of 32 rows with one
+//   - the unit's K and V (n rows each, <= 208 x 256 B) are fetched by bulk copies of 26 rows with one
 //     mbarrier each, issued at CTA start (before griddepcontrol.wait when the previous launch on the
 //     stream wrote none of this call's cache), and stay resident: no ring, no refill round trip;
 //   - both contractions are GEMVs (one query row) on the CUDA cores. Warp w owns slots
-//     [32 w, 32 w + 32) and waits only for their copies; a half-warp covers a 256-byte row, lane
+//     [26 w, 26 w + 26) (so all 8 warps have slots at 204-208) and waits only for their copies; a
+//     half-warp covers a 256-byte row, lane
 //     (hl, li) = (lane / 16, lane % 16) reading columns [8 li, 8 li + 8) of the rows of parity hl
 //     with one 16-byte shared load per row (conflict-free). The logits use fma.rn.f32.bf16 (bf16
-//     operands, fp32 products and sums); the 16 partial dot products of a lane are reduced across
-//     its half-warp by a butterfly reduce-scatter (8 + 4 + 2 + 1 shuffles) that leaves lane (hl, li)
-//     holding slot 32 w + 2 li + hl's logit, the slot it keeps for the softmax, the score update and
-//     the victim search. V^T w accumulates column pairs with fma.rn.f32x2;
+//     operands, fp32 products and sums); the 13 partial dot products of a lane (padded to 16) are
+//     reduced across its half-warp by a butterfly reduce-scatter (8 + 4 + 2 + 1 shuffles) that leaves
+//     lane (hl, li), li < 13, holding slot 26 w + 2 li + hl's logit, the slot it keeps for the
+//     softmax, the score update and the victim search. V^T w accumulates column pairs with fma.rn.f32x2;
 //   - the softmax needs one block barrier: each warp publishes its (max, sum of exp) pair, and every
 //     lane forms the normaliser from them with one exp and a 3-shuffle sum;
 //   - with a next-call hint (h2o_decode_step_prefetch) the CTA asks L2 for the next call's rows of
@@ -42,7 +43,9 @@ constexpr int kD = 128;
 constexpr int kRowBytes = kD * 2;            // one bf16 K or V row
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBlockRows = 32;               // slots per warp, per bulk copy and per mbarrier
+constexpr int kBlockRows = 26;               // slots per warp, per bulk copy and per mbarrier (26 x 8
+                                             // warps = 208: every warp works at the largest budgets)
+constexpr int kPairs = kBlockRows / 2;       // row pairs per warp (one per half-warp each)
 constexpr int kMaxSlots = 208;
 constexpr int kMaxBlocks = (kMaxSlots + kBlockRows - 1) / kBlockRows;
 static_assert(kMaxBlocks <= kWarps, "one warp per block of slots");
@@ -149,9 +152,10 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   const uint32_t tok = smem_u32(smem + L.tok);
   const size_t row0 = static_cast<size_t>(unit) * B;
   // Lane (hl, li) = (lane / 16, lane % 16) works on columns [8 li, 8 li + 8) of its warp's rows with
-  // parity hl, and holds slot j = 32 warp + 2 li + hl (valid if j < n).
+  // parity hl, and holds slot j = 26 warp + 2 li + hl (if li < 13 and j < n).
   const int hl = lane >> 4, li = lane & 15;
   const int j = warp * kBlockRows + 2 * li + hl;
+  const bool has_slot = li < kPairs && j < n;
   const bool mine = warp < blocks;  // this warp's block of slots holds cached rows
   const bool cache_full = n == B;
 
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   int32_t sp = 0;
   if (p.early != 0) {  // the previous launch on the stream wrote none of this call's cache arrays
     fetch();
-    if (j < n) {
+    if (has_slot) {
       sc = p.scores[row0 + j];
       sp = p.slot_pos[row0 + j];
     }
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     pdl_wait();  // the previous step's cache, scores and slot map are complete from here on
     pdl_launch_dependents();
     fetch();
-    if (j < n) {
+    if (has_slot) {
       sc = p.scores[row0 + j];
       sp = p.slot_pos[row0 + j];
     }
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   for (int off = 8; off > 0; off >>= 1) sn += __shfl_xor_sync(0xffffffffu, sn, off);  // over the 16 lanes
   const float s_new = sn * p.scale;
 
-  // D2: logits of this warp's 32 slots once their K rows have landed.
+  // D2: logits of this warp's 26 slots once their K rows have landed (row pairs past the 13th: none).
   // Rows past the block's last cached slot re-read that slot (no branch per row, every load stays
   // inside the copied rows); their logits are dropped and their weights are zero.
   const int rows = min(kBlockRows, n - warp * kBlockRows);  // >= 1 for this warp's block
@@ -248,16 +252,16 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int r = 2 * i + hl;
-      v[i] = dot8_bf16(krow[(r < rows ? r : rows - 1) * (kRowBytes / 16)], q16);
+      v[i] = i < kPairs ? dot8_bf16(krow[(r < rows ? r : rows - 1) * (kRowBytes / 16)], q16) : 0.f;
     }
     const float dot = reduce_scatter<16>(v, li);
-    if (j < n) s = dot * p.scale;
+    if (has_slot) s = dot * p.scale;
   }
 
   // D3: softmax over the n slots and the new token. Each warp publishes (its max, its sum of
   // exp(s - max)); every thread combines the pairs into the block's max m and normaliser l.
   float mw = warp_max(warp == 0 ? fmaxf(s, s_new) : s);
-  float ew = (j < n) ? expf(s - mw) : 0.f;
+  float ew = has_slot ? expf(s - mw) : 0.f;
   if (warp == 0 && lane == 0) ew += expf(s_new - mw);
   ew = warp_sum(ew);
   if (lane == 0) {
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   float l = red_l[lane % kWarps] * expf(red_m[lane % kWarps] - m);
 #pragma unroll
   for (int off = 1; off < kWarps; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  const float wj = (j < n) ? expf(s - m) : 0.f;  // slot j's unnormalised weight
+  const float wj = has_slot ? expf(s - m) : 0.f;  // slot j's unnormalised weight
   const float w_new = expf(s_new - m);
 
   // D4: this warp's share of sum_j w_j V_j: lane (hl, li) accumulates columns [8 li, 8 li + 8) over
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     if (ok) ok = mbar_wait(&vbar[warp], 0, p.err);
     const uint4* vrow = reinterpret_cast<const uint4*>(smem + L.v + warp * kBlockRows * kRowBytes) + li;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPairs; ++i) {
       const int r = 2 * i + hl;
       const float wr = __shfl_sync(0xffffffffu, wj, 16 * hl + i);  // 0 for rows past the last cached slot
       const uint4 raw = vrow[(r < rows ? r : rows - 1) * (kRowBytes / 16)];
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   const int32_t last_candidate = p.position - p.k_local;
   unsigned long long best = ~0ull;
   float ns = 0.f;
-  if (j < n) {
+  if (has_slot) {
     const float pr = wj / l;
     ns = p.policy == H2O_POLICY_TOPK ? pr : sc + pr;  // Top-K: this step's weight
     bool cand = false;
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   }
 
   // D7: the score table written back, the new token in its slot (warp 0 writes K, warp 1 V).
-  if (j < n) p.scores[row0 + j] = (j == victim) ? p_new : ns;
+  if (has_slot) p.scores[row0 + j] = (j == victim) ? p_new : ns;
   const int32_t target = cache_full ? victim : n;
   if (target >= 0 && ok) {
     const size_t trow = row0 + static_cast<size_t>(target);
