@@ -143,16 +143,16 @@ def decode_kernel(w: synth.Workload, sms: int, e4m3: bool = False) -> tuple[str,
     return "h2o_decode_step_kernel", os.path.join(CSRC, "h2o_decode.cu")
 
 
-def recorded_traffic(workload: str, kernel: str, src: str):
+def recorded_traffic(workload: str, kernel: str, src: str, units_per_launch: int):
     """DRAM bytes per decode launch from the committed ncu records, if one was taken on the current
-    source of this kernel and on this workload; otherwise None."""
+    source of this kernel, on this workload and with this many units per launch; otherwise None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         recs = json.load(f)
     for rec in recs.get("records", [recs]):
         if (rec.get("kernel") == kernel and rec.get("kernel_sha") == source_sha(src)
-                and rec.get("workload") == workload):
+                and rec.get("workload") == workload and rec.get("units_per_launch") == units_per_launch):
             return rec.get("dram_bytes_per_launch")
     return None
 
@@ -487,7 +487,7 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     kname, ksrc = decode_kernel(w.with_(layers=1), sms, e4m3)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc, U // L),
                 "kernel": kname, "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": avg_decode_s * 1e6,
                 "units_per_launch": U // L}
@@ -626,7 +626,7 @@ def workload_timing(h2o, w: synth.Workload, dev, warmup: int, reps: int, e4m3: b
            "prefill_ms": float(np.median(pre_ms)),
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": achieved / peaks["hbm_gbs"],
-                        "traffic": recorded_traffic(w.name, kname, ksrc), "kernel": kname,
+                        "traffic": recorded_traffic(w.name, kname, ksrc, U), "kernel": kname,
                         "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                         "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": us},
            "clocks": clocks.summary(), "gpu_launches_per_rep": 3 + S,
@@ -717,7 +717,7 @@ def other_launch_shapes(h2o, w, dv, calls, out, evs, evp, stream, dev, g_pre, wa
     kname, ksrc = decode_kernel(w, sms, e4m3)
     res["decode_all_layers"] = entry(
         timed(lambda s: calls.decode_all_layers(P + s, *io(s)), 1), 1, kname,
-        "h2o_decode_step_e4m3" if e4m3 else "h2o_decode_step", recorded_traffic(w.name, kname, ksrc))
+        "h2o_decode_step_e4m3" if e4m3 else "h2o_decode_step", recorded_traffic(w.name, kname, ksrc, U))
     if not e4m3:
         res["decode_per_layer_plain"] = entry(
             timed(lambda s: calls.decode(P + s, *io(s), hint=False), L), L,

@@ -2,6 +2,7 @@
 the kernel each workload's decode step dispatches to, and the oracle baseline's record."""
 
 import argparse
+import os
 
 import bench
 import synth
@@ -46,3 +47,18 @@ def test_config_names_the_workload():
     assert c["workload"].startswith("opt-6.7b") and c["units"] == 8192 and c["budget"] == 204
     assert (c["k_heavy"], c["k_local"], c["prompt_len"], c["decode_steps"]) == (102, 102, 512, 512)
     assert "model" not in c
+
+
+def test_recorded_traffic_is_keyed_by_launch_size():
+    """A DRAM-traffic record applies only to launches of the size it was captured on: the E4M3 kernel's
+    all-layers record (8192 units per launch) must not be reported for its per-layer launches."""
+    import json
+    with open(bench.TRAFFIC_FILE) as f:
+        recs = json.load(f)["records"]
+    assert recs and all(isinstance(r.get("units_per_launch"), int) for r in recs)
+    for r in recs:
+        src = os.path.join(bench.CSRC, {"h2o_decode_tc_kernel": "h2o_decode_tc.cu",
+                                        "h2o_decode_e4m3_kernel": "h2o_decode_e4m3.cu",
+                                        "h2o_decode_resident_kernel": "h2o_decode_resident.cu"}[r["kernel"]])
+        other = r["units_per_launch"] * 2
+        assert bench.recorded_traffic(r["workload"], r["kernel"], src, other) is None
