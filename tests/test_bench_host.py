@@ -62,3 +62,51 @@ def test_recorded_traffic_is_keyed_by_launch_size():
                                         "h2o_decode_resident_kernel": "h2o_decode_resident.cu"}[r["kernel"]])
         other = r["units_per_launch"] * 2
         assert bench.recorded_traffic(r["workload"], r["kernel"], src, other) is None
+
+
+def test_per_layer_calls_and_prefetch_hints():
+    """The benchmark's decode step: one call per layer on that layer's slice of every array, each
+    naming the next layer's cache arrays as the prefetch hint (layer 0's after the last layer), the
+    last launch of a job naming none; E4M3 caches: one plain E4M3 call per layer."""
+    import types
+
+    import torch
+
+    import kv_cache_eviction_step_gb300 as h2o
+    L, B, H, D, K = 3, 2, 4, 8, 5
+    dims = h2o.Dims(units_b=L * B, heads=H, head_dim=D, budget=K, k_heavy=3, k_local=2, dtype=h2o.BF16)
+    U = dims.units
+    log = []
+
+    def rec(name):
+        return lambda *a: log.append((name, a))
+
+    fake = types.SimpleNamespace(
+        next_cache=lambda k, v, s, p: ("next", k.data_ptr(), v.data_ptr(), s.data_ptr(), p.data_ptr()),
+        h2o_decode_step_prefetch=rec("prefetch"), h2o_decode_step=rec("plain"),
+        h2o_decode_step_e4m3=rec("e4m3"))
+    cache = types.SimpleNamespace(k_cache=torch.zeros(U, K, D), v_cache=torch.zeros(U, K, D),
+                                  scores=torch.zeros(U, K), slot_pos=torch.zeros(U, K, dtype=torch.int32),
+                                  k_scale=torch.zeros(U, K), v_scale=torch.zeros(U, K))
+    io = [torch.zeros(U, D) for _ in range(4)] + [torch.zeros(U, dtype=torch.int32)] * 2
+    q, kn, vn, out, evs, evp = io
+    calls = bench.Calls(fake, dims, cache, e4m3=False, layers=L)
+    ul = U // L
+    for last in (False, True):
+        log.clear()
+        calls.decode(7, q, kn, vn, out, evs, evp, 0, last=last)
+        assert [n for n, _ in log] == ["prefetch"] * L
+        for l, (_, a) in enumerate(log):
+            d, pol, t = a[0], a[1], a[2]
+            assert d.units == ul and pol is None and t == 7
+            assert a[3].data_ptr() == q[l * ul:].data_ptr() and a[6].data_ptr() == cache.k_cache[l * ul:].data_ptr()
+            nl = (l + 1) % L
+            want = ("next", cache.k_cache[nl * ul:].data_ptr(), cache.v_cache[nl * ul:].data_ptr(),
+                    cache.scores[nl * ul:].data_ptr(), cache.slot_pos[nl * ul:].data_ptr())
+            assert a[-2] == (None if last and l == L - 1 else want), (last, l)
+    log.clear()
+    calls.decode(7, q, kn, vn, out, evs, evp, 0, hint=False)
+    assert [n for n, _ in log] == ["plain"] * L
+    log.clear()
+    bench.Calls(fake, dims, cache, e4m3=True, layers=L).decode(7, q, kn, vn, out, evs, evp, 0)
+    assert [n for n, _ in log] == ["e4m3"] * L
