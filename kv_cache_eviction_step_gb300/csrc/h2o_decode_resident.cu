@@ -340,14 +340,24 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   }
   if (!ok) *gave_up = 1;
   __syncthreads();  // output partials and eviction keys complete (and every wait of the CTA is over)
-  unsigned long long vkey = ~0ull;
-  int32_t victim = -1;
+  // The smallest of the eight warp keys, as a 3-level tree over loads issued together.
+  unsigned long long tk[kWarps];
+  int32_t ts[kWarps];
 #pragma unroll
-  for (int w2 = 0; w2 < kWarps; ++w2)
-    if (red_key[w2] < vkey) {
-      vkey = red_key[w2];
-      victim = red_slot[w2];
-    }
+  for (int w2 = 0; w2 < kWarps; ++w2) {
+    tk[w2] = red_key[w2];
+    ts[w2] = red_slot[w2];
+  }
+#pragma unroll
+  for (int h = kWarps / 2; h >= 1; h >>= 1)
+#pragma unroll
+    for (int w2 = 0; w2 < h; ++w2)
+      if (tk[w2 + h] < tk[w2]) {
+        tk[w2] = tk[w2 + h];
+        ts[w2] = ts[w2 + h];
+      }
+  unsigned long long vkey = tk[0];
+  int32_t victim = ts[0];
   if (!cache_full) {
     victim = -1;
     vkey = ~0ull;
@@ -355,9 +365,15 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
     atomicCAS(p.err, H2O_DEVERR_NONE, H2O_DEVERR_NO_CANDIDATE);
   }
   const float p_new = w_new / l;
-  if (tid < kD) {  // output element tid
-    float o = 0.f;
-    for (int w2 = 0; w2 < blocks; ++w2) o += part[w2 * kD + tid];
+  if (tid < kD) {  // output element tid: the warps' partials (zero past the last block), as a tree
+    float o8[kWarps];
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) o8[w2] = w2 < blocks ? part[w2 * kD + tid] : 0.f;
+#pragma unroll
+    for (int h = kWarps / 2; h >= 1; h >>= 1)
+#pragma unroll
+      for (int w2 = 0; w2 < h; ++w2) o8[w2] += o8[w2 + h];
+    float o = o8[0];
     const float vn = bf16_lo(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(smem + L.tok + 2 * kRowBytes + 2 * tid)));
     o = fmaf(w_new, vn, o);
     static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(unit) * kD + tid] = __float2bfloat16_rn(o / l);
