@@ -159,6 +159,15 @@ __global__ void __launch_bounds__(kThreads, 2) h2o_decode_resident_kernel(const 
   const bool mine = warp < blocks;  // this warp's block of slots holds cached rows
   const bool cache_full = n == B;
 
+  // Without a next-call hint, the new token's rows are asked of L2 at once (a prefetch only: the read
+  // after griddepcontrol.wait still sees whatever the previous kernel wrote), so that read is an L2
+  // hit when they were in HBM (one layer of 256 units per launch: 6.18 -> 5.94 us). With a hint the
+  // previous launch is prefetching this launch's cache rows at this moment, and this early read,
+  // queued against them, measured slower (5.57 -> 5.71 us), so it is left out.
+  if (warp == 2 && lane < 3 && p.next_k_cache == nullptr) {
+    const void* src = lane == 0 ? p.q : lane == 1 ? p.k_new : p.v_new;
+    bulk_prefetch_l2(static_cast<const unsigned char*>(src) + static_cast<size_t>(unit) * kRowBytes, kRowBytes);
+  }
   if (tid == 0) {
     for (int b = 0; b < 2 * kWarps + 1; ++b) mbar_init(&kbar[b], 1);
     fence_mbar_init();
