@@ -9,7 +9,7 @@
 //   P1+ with an output tensor, the row-statistics pass is also the prompt's attention forward:
 //       o_i = sum_{j<=i} exp(s_ij - m_i) / l_i v_j, sharing the logits and exponentials with P1.
 //
-// One persistent kernel shape serves the three passes. A work item is one 128-row "resident" tile of
+// One persistent kernel shape serves the four passes. A work item is one 128-row "resident" tile of
 // one unit; every CTA (one per SM) walks its items (whole units when there are many, see item_at) and
 // streams, per item, 128-row tiles of the other operand, so that S = A B^T lands in tensor memory
 // with one TMEM lane per resident row:
@@ -31,6 +31,12 @@
 // moves only when a tile's maximum exceeds it by more than kLazyMax (log2 units): O and l are rescaled
 // then, rarely, and the probabilities stay below 2^kLazyMax. The warps of a row exchange their tile
 // maxima and sums through spare tensor-memory columns (shared memory is full).
+// One pass (prompts of at most four tiles, at least one unit per SM, no output tensor): the
+// row-statistics shape with four logit accumulators, so that a query tile's logits against all of
+// its key tiles sit in tensor memory at once; the epilogue takes the rows' statistics, overwrites the
+// logits with their exponentials, then weights them by their row's normaliser and sums them across
+// TMEM lanes for the column sums (onepass_epilogue). Every logit and exponential is computed once,
+// against twice in the two passes above.
 // Every wait is bounded (see mbar_wait); a CTA that gives up still frees its tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -59,12 +65,13 @@ constexpr uint32_t kOCol = 2 * kTile;
 constexpr uint32_t kXCol = 448;            // output pass: [2][kSplit] max exchange, then [2][kSplit] l
 constexpr int kPBytes = 2 * kBoxBytes;     // 128 x 128 bf16 probability tile (two 64-key boxes)
 constexpr int kAlign = 1024;               // 128-byte swizzle atoms repeat every 1024 bytes
-constexpr int kCtrlBytes = 256;            // mbarriers + TMEM address slot
+constexpr int kCtrlBytes = 384;            // mbarriers + TMEM address slot
+constexpr int kRegions = 4;                // one-pass column sums: 128-column logit regions (all of TMEM)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.f;            // output pass: rescale only when the max grows by > 2^8
 
-enum Mode { kRowStats = 0, kRowOut = 1, kColSums = 2 };
+enum Mode { kRowStats = 0, kRowOut = 1, kColSums = 2, kOnePass = 3 };
 
 struct TcParams {
   CUtensorMap tm_a;        // resident operand: Q (row stats) or K (column sums), [units][P][D]
@@ -92,10 +99,13 @@ struct TcShape {
   // Streamed ring depth. The output pass also holds V tiles and two probability tiles, so its ring
   // is shallower (it exchanges between warps through tensor memory); the other passes keep an
   // exchange area for the partial row results ([2][kSplit][128] float2) and, for column sums, each
-  // warp's query statistics ([kEpiWarps][2][kCols] float).
+  // warp's query statistics ([kEpiWarps][2][kCols] float); the one-pass column sums keep, instead,
+  // each lane quarter's column partials of two units ([2][4][kRegions * 128] float).
   static constexpr int kStages = kMode == kRowOut ? (D == 128 ? 3 : 6) : (D == 128 ? 4 : 8);
   static constexpr int kXBytes = 2 * kSplit * kTile * 8;
-  static constexpr int kHeadBytes = kCtrlBytes + (kMode == kRowOut ? 0 : kXBytes + kEpiWarps * 2 * kCols * 4);
+  static constexpr int kPartBytes = 2 * 4 * kRegions * kTile * 4;
+  static constexpr int kHeadBytes =
+      kCtrlBytes + (kMode == kRowOut ? 0 : kXBytes + (kMode == kOnePass ? kPartBytes : kEpiWarps * 2 * kCols * 4));
   static constexpr int kBodyBytes = (2 + kStages) * kTileBytes + (kMode == kRowOut ? 2 * kPBytes : 0);
   static constexpr int kSmem = kHeadBytes + kAlign + kBodyBytes;
 };
@@ -278,6 +288,68 @@ __device__ __forceinline__ float ex2(float x) {
 // like the scalar fmaf / + it stands for, so results do not change, at half the instructions.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// Store 32 fp32 columns of this warp's 32 TMEM lanes without waiting for completion (tmem_wait_st
+// orders them before a later read of the same columns).
+__device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 TMEM lanes x 32 columns of this warp's lane quarter in the 16x256b fragment shape (two loads of
+// 16 lanes, four 256-bit column groups each), so that every thread holds 4 rows x 8 columns: for
+// column group k (columns 8k..8k+7) and thread t, v[4k], v[4k+1] are row t/4, columns 8k + 2(t%4) and
+// +1; v[4k+2], v[4k+3] row t/4 + 8, the same columns; v[16 + ...] likewise rows t/4 + 16 and t/4 + 24.
+__device__ __forceinline__ void tmem_ld_rows4(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%33];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + (16u << 16))
+      : "memory");
+#pragma unroll
+  for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
+}
+
+// Sums over the 8 threads that share t % 4 (lane bits 2-4) of 8 column partials each: a butterfly
+// reduce-scatter in which, at distance d, each thread keeps the half of its values selected by lane
+// bit d, sends the other half to lane ^ d and adds what it receives. Thread t returns value
+// (t >> 2) & 7 summed over the 8 threads (7 shuffles and 7 additions per thread).
+__device__ __forceinline__ float column_sum8(float (&w)[8], int lane) {
+#pragma unroll
+  for (int half = 4, d = 16; half >= 1; half >>= 1, d >>= 1) {
+    const bool upper = (lane & d) != 0;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = upper ? w[j] : w[j + half];
+      const float keep = upper ? w[j + half] : w[j];
+      w[j] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+    }
+  }
+  return w[0];
+}
 
 // The largest of three values in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -361,13 +433,174 @@ __device__ __forceinline__ bool item_at(const TcParams& p, int n, Item* it) {
   return true;
 }
 
+// All 16 epilogue warps (named barrier 5).
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync 5, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+// Epilogue of the one-pass column sums (prompts of at most kRegions tiles; each CTA takes whole
+// units, query tiles tiles - 1 down to 0). Item = query tile i of a unit; its logit tiles against key
+// tiles 0..i stay in tensor-memory regions (g mod kRegions) until the item is done:
+//   sweep 1, per key tile t: this warp's 32 columns of row r (one row per thread); the running
+//            maximum m (log2 units) and sum l of 2^(s sl - m) over them; the logits are overwritten by
+//            e = 2^(s sl - m_t), m_t the running maximum when tile t was read;
+//   combine: the kSplit warps of the lane quarter exchange (m, l): the row's maximum M and sum L, and
+//            each row's weight for tile t, f_t = 2^(m_t - M) / L (zero for rows past the prompt);
+//   sweep 2, per key tile t: e back from tensor memory in the 16x256b shape (4 rows x 8 columns per
+//            thread; the region is then released to the MMA lane); the thread sums its 4 rows weighted
+//            by their f_t, and 8 threads add their partials per column (column_sum8).
+// On the diagonal tile a warp whose 32 keys all lie past its 32 rows has nothing to add and skips the
+// tile; one whose keys all lie before its rows needs no mask (unless the prompt ends inside them).
+// Each lane quarter's column sums go to its own shared-memory row (the unit's first item, which meets
+// every key tile, writes; later items add), and once the unit's last item is done the four rows are
+// added in a fixed order, so a column sum does not depend on warp timing.
+template <int D>
+__device__ __forceinline__ void onepass_epilogue(const TcParams& p, uint32_t tmem, int warp, int lane, float2* xh,
+                                                 float* part, uint64_t* acc_full, uint64_t* acc_empty) {
+  constexpr int kKeys = kRegions * kTile;
+  const int q = warp & 3, h = warp >> 2;
+  const int r = q * 32 + lane;
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const float sl = p.sl;
+  const int P = p.P;
+  // sweep 2: this thread's column within the warp's 32 (column_sum8's output, see tmem_ld_rows4)
+  const int vsel = (lane >> 2) & 7;
+  const int col = 8 * (vsel >> 1) + 2 * (lane & 3) + (vsel & 1);
+  bool ok = true;
+  uint32_t g = 0;  // logit tiles consumed (over all items)
+  Item it;
+  for (int k = 0; item_at<kOnePass>(p, k, &it); ++k) {
+    const int kt = k % p.tiles;       // item within the unit (0: query tile tiles - 1)
+    const int ub = (k / p.tiles) & 1;  // the unit's buffer of column partials
+    float* pq = part + (ub * 4 + q) * kKeys + h * kCols + col;
+    const int row = it.at * kTile + r;
+    // The diagonal tile for this warp: no key before any of its rows (skip), or every key before all
+    // of them and before the prompt's end (no mask).
+    const bool diag_empty = h > q;
+    const bool diag_full = h < q && P - 1 - (it.at * kTile + h * kCols) >= kCols - 1;
+    float m2 = -INFINITY, l = 0.f;
+    float mt[kRegions];
+#pragma unroll
+    for (int t = 0; t < kRegions; ++t) {
+      mt[t] = -INFINITY;
+      if (t < it.nt) {
+        const uint32_t gt = g + t, a = gt % kRegions;
+        if (ok) ok = mbar_wait(&acc_full[a], (gt / kRegions) & 1u, p.err);
+        const bool diag = t == it.at;
+        if (!(diag && diag_empty)) {
+          tc_fence_after();
+          const uint32_t taddr = lane_addr + a * kTile + h * kCols;
+          float v[kCols];
+          tmem_ld32(taddr, v);
+          if (diag && !diag_full) {  // keys j <= row and j < P
+            const int lim = min(row, P - 1) - (t * kTile + h * kCols);
+#pragma unroll
+            for (int x = 0; x < kCols; ++x) v[x] = x <= lim ? v[x] : -INFINITY;
+          }
+          const float cm = max32(v) * sl;
+          if (cm > m2) {
+            l *= ex2(m2 - cm);
+            m2 = cm;
+          }
+          mt[t] = m2;
+          if (m2 != -INFINITY) {
+            const float2 sl2 = make_float2(sl, sl), nm = make_float2(-m2, -m2);
+            float2 s01 = make_float2(0.f, 0.f), s23 = s01;
+#pragma unroll
+            for (int x = 0; x < kCols; x += 4) {
+              const float2 e01 = fma2(make_float2(v[x], v[x + 1]), sl2, nm);
+              const float2 e23 = fma2(make_float2(v[x + 2], v[x + 3]), sl2, nm);
+              v[x] = ex2(e01.x);
+              v[x + 1] = ex2(e01.y);
+              v[x + 2] = ex2(e23.x);
+              v[x + 3] = ex2(e23.y);
+              s01 = add2(s01, make_float2(v[x], v[x + 1]));
+              s23 = add2(s23, make_float2(v[x + 2], v[x + 3]));
+            }
+            l += (s01.x + s01.y) + (s23.x + s23.y);
+          } else {
+#pragma unroll
+            for (int x = 0; x < kCols; ++x) v[x] = 0.f;
+          }
+          tmem_st32_async(taddr, v);
+        }
+      }
+    }
+    tmem_wait_st();
+    // The row's maximum and normaliser over the quarter's kSplit warps (buffer by item parity: a warp
+    // rewrites it two items later, after every warp of the quarter has passed the next exchange).
+    float2* xk = xh + (k & 1) * kSplit * kTile;
+    xk[h * kTile + r] = make_float2(m2, l);
+    quarter_sync(q);
+    float mm = xk[r].x;
+#pragma unroll
+    for (int j = 1; j < kSplit; ++j) mm = fmaxf(mm, xk[j * kTile + r].x);
+    float lt = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSplit; ++j) {
+      const float2 o = xk[j * kTile + r];
+      if (o.x != -INFINITY) lt += o.y * ex2(o.x - mm);
+    }
+    const float inv = row < P ? 1.f / lt : 0.f;
+#pragma unroll
+    for (int t = 0; t < kRegions; ++t) {
+      if (t < it.nt) {
+        const uint32_t a = (g + t) % kRegions;
+        float cs = 0.f;
+        if (t == it.at && diag_empty) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        } else {
+          // row weights of the thread's four rows (lanes t/4 + 8i own them in sweep 1)
+          const float f = mt[t] == -INFINITY ? 0.f : ex2(mt[t] - mm) * inv;
+          float2 fr[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float fi = __shfl_sync(0xffffffffu, f, (lane >> 2) + 8 * i);
+            fr[i] = make_float2(fi, fi);
+          }
+          float v[kCols];
+          tmem_ld_rows4(lane_addr + a * kTile + h * kCols, v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+          float w[8];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float2 acc = mul2(make_float2(v[4 * c4], v[4 * c4 + 1]), fr[0]);
+            acc = fma2(make_float2(v[4 * c4 + 2], v[4 * c4 + 3]), fr[1], acc);
+            acc = fma2(make_float2(v[16 + 4 * c4], v[16 + 4 * c4 + 1]), fr[2], acc);
+            acc = fma2(make_float2(v[16 + 4 * c4 + 2], v[16 + 4 * c4 + 3]), fr[3], acc);
+            w[2 * c4] = acc.x;
+            w[2 * c4 + 1] = acc.y;
+          }
+          cs = column_sum8(w, lane);
+        }
+        float* dst = pq + t * kTile;
+        *dst = kt == 0 ? cs : *dst + cs;
+      }
+    }
+    g += it.nt;
+    if (kt == p.tiles - 1) {  // the unit's last item: add the four quarters' partials
+      epilogue_sync();
+      const int key = warp * 32 + lane;
+      if (key < P) {
+        const float* pb = part + ub * 4 * kKeys + key;
+        p.colsum[static_cast<size_t>(it.unit) * P + key] = (pb[0] + pb[kKeys]) + (pb[2 * kKeys] + pb[3 * kKeys]);
+      }
+    }
+  }
+}
+
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using S = TcShape<D, kMode>;
   constexpr int kStages = S::kStages;
   constexpr bool kOut = kMode == kRowOut;
   constexpr bool kCol = kMode == kColSums;
-  constexpr uint32_t kNAcc = kOut ? 2u : 3u;  // logit accumulators (the output pass keeps O at 256..)
+  // logit accumulators (the output pass keeps O at 256..; the one-pass column sums hold a query tile's
+  // logits against all of its key tiles)
+  constexpr uint32_t kNAcc = kOut ? 2u : (kMode == kOnePass ? static_cast<uint32_t>(kRegions) : 3u);
   extern __shared__ unsigned char smem_raw[];
   // head: mbarriers, TMEM slot, exchange areas; body (1024-aligned): resident x2, ring, P x2
   unsigned char* head = smem_raw;
@@ -381,18 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t* ring_full = res_empty + 2;
   uint64_t* ring_empty = ring_full + kStages;
   uint64_t* acc_full = ring_empty + kStages;
-  uint64_t* acc_empty = acc_full + 3;
-  uint64_t* p_full = acc_empty + 3;   // output pass: the epilogue wrote probability tile b
+  uint64_t* acc_empty = acc_full + kRegions;
+  uint64_t* p_full = acc_empty + kRegions;  // output pass: the epilogue wrote probability tile b
   uint64_t* p_free = p_full + 2;      // output pass: the product reading probability tile b finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + 2);
   float2* xh = reinterpret_cast<float2*>(head + kCtrlBytes);  // row stats / column sums: [2][kSplit][128]
   float* xq = reinterpret_cast<float*>(head + kCtrlBytes + S::kXBytes);  // column sums: [warps][2][kCols]
+  float* part = xq;  // one-pass column sums: [2][4][kRegions * 128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.P;
 
   if (tid == 0) {
-    for (int b = 0; b < 3; ++b) {
+    for (int b = 0; b < kRegions; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kEpiWarps);
     }
@@ -530,6 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
     }
     __syncwarp();
+  } else if constexpr (kMode == kOnePass) {
+    onepass_epilogue<D>(p, tmem, warp, lane, xh, part, acc_full, acc_empty);
   } else {
     // Epilogue: warp q + 4h owns TMEM lanes 32q.. (resident rows) and columns 32h..32h+31 of a tile.
     const int q = warp & 3, h = warp >> 2;
@@ -817,7 +1053,7 @@ cudaError_t launch_pass(const TcParams& p, cudaStream_t s) {
   }
   // Whole units per CTA once there are at least 8 per SM (so the last round idles few CTAs).
   TcParams q = p;
-  q.unit_items = p.units >= 8 * sms ? 1 : 0;
+  q.unit_items = (kMode == kOnePass || p.units >= 8 * sms) ? 1 : 0;
   const long long items = q.unit_items ? p.units : static_cast<long long>(p.units) * p.tiles;
   const int grid = items < sms ? static_cast<int>(items) : sms;
   kernel<<<grid, kThreads, kSmem, s>>>(q);
@@ -844,6 +1080,15 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
   p.last_row_only = 0;
   p.unit_items = 0;
   cudaError_t e;
+  // Prompts of at most kRegions tiles, at least one unit per SM and no output tensor: both rows in one
+  // pass (each logit and exponential computed once; the column sums reduced across TMEM lanes).
+  if (pp.out == nullptr && !pp.last_row_only && p.tiles <= kRegions) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (pp.units >= sms) return launch_pass<D, kOnePass>(p, s);
+  }
   // resident Q, streamed K (and V when the prompt's attention output is wanted)
   if (pp.out != nullptr) {
     if (!encode_operand(&p.tm_v, pp.v, pp.units, pp.P, D)) return cudaErrorInvalidValue;

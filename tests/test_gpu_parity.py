@@ -414,10 +414,9 @@ def test_prefill_between_decodes_of_different_caches(middle):
 
 @pytest.mark.parametrize("P", [100, 256, 300, 512])
 def test_prefill_with_many_units(P):
-    """At least 8 units per SM: CTAs take whole units, and with prompts of up to 4 tiles each unit's
-    streamed tiles stay in shared memory for all of its items. 1280 OPT-6.7B-shaped units with
-    prompts of 1 to 4 tiles: every column sum of 40 sampled units against the oracle's float64 sums,
-    then the kept slot maps and 8 decode steps."""
+    """At least 8 units per SM, prompts of 1 to 4 tiles: the one-pass column sums (CTAs take whole
+    units). 1280 OPT-6.7B-shaped units: every column sum of 40 sampled units against the oracle's
+    float64 sums, then the kept slot maps and 8 decode steps."""
     import torch
 
     import kv_cache_eviction_step_gb300 as h2o
