@@ -67,6 +67,7 @@ constexpr int kPBytes = 2 * kBoxBytes;     // 128 x 128 bf16 probability tile (t
 constexpr int kAlign = 1024;               // 128-byte swizzle atoms repeat every 1024 bytes
 constexpr int kCtrlBytes = 384;            // mbarriers + TMEM address slot
 constexpr int kRegions = 4;                // one-pass column sums: 128-column logit regions (all of TMEM)
+constexpr int kQuarterRows = 32;           // one-pass column sums: rows per resident TMA box (a lane quarter)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.f;            // output pass: rescale only when the max grows by > 2^8
@@ -451,6 +452,10 @@ __device__ __forceinline__ void epilogue_sync() {
 //            by their f_t, and 8 threads add their partials per column (column_sum8).
 // On the diagonal tile a warp whose 32 keys all lie past its 32 rows has nothing to add and skips the
 // tile; one whose keys all lie before its rows needs no mask (unless the prompt ends inside them).
+// That work differs between lane quarters, and the four warps of lane quarter q all run on SM
+// sub-partition q, so the resident tile's 32-row blocks are rotated by the query tile index: lane
+// quarter q holds rows 32 ((q + i) mod 4) .. of query tile i, and over a unit's items every
+// sub-partition takes each block of the diagonal once.
 // Each lane quarter's column sums go to its own shared-memory row (the unit's first item, which meets
 // every key tile, writes; later items add), and once the unit's last item is done the four rows are
 // added in a fixed order, so a column sum does not depend on warp timing.
@@ -473,11 +478,12 @@ __device__ __forceinline__ void onepass_epilogue(const TcParams& p, uint32_t tme
     const int kt = k % p.tiles;       // item within the unit (0: query tile tiles - 1)
     const int ub = (k / p.tiles) & 1;  // the unit's buffer of column partials
     float* pq = part + (ub * 4 + q) * kKeys + h * kCols + col;
-    const int row = it.at * kTile + r;
+    const int sb = (q + it.at) & 3;  // the tile's 32-row block in this lane quarter (see the TMA loads)
+    const int row = it.at * kTile + sb * kQuarterRows + lane;
     // The diagonal tile for this warp: no key before any of its rows (skip), or every key before all
     // of them and before the prompt's end (no mask).
-    const bool diag_empty = h > q;
-    const bool diag_full = h < q && P - 1 - (it.at * kTile + h * kCols) >= kCols - 1;
+    const bool diag_empty = h > sb;
+    const bool diag_full = h < sb && P - 1 - (it.at * kTile + h * kCols) >= kCols - 1;
     float m2 = -INFINITY, l = 0.f;
     float mt[kRegions];
 #pragma unroll
@@ -674,9 +680,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int rb = k & 1;
         if (k >= 2 && !mbar_wait(&res_empty[rb], static_cast<uint32_t>(k / 2 - 1) & 1u, p.err)) break;
         mbar_expect_tx(&res_full[rb], S::kTileBytes);
-        for (int b = 0; b < S::kBoxes; ++b)
-          tma_load_3d(res + rb * S::kTileBytes + b * kBoxBytes, &p.tm_a, b * kBoxCols, it.at * kTile, it.unit,
-                      &res_full[rb]);
+        if constexpr (kMode == kOnePass) {
+          // 32-row blocks, block j of query tile i at row block (j - i) mod 4, so that lane quarter q
+          // holds rows 32 ((q + i) mod 4) .. of the tile (see onepass_epilogue)
+          for (int b = 0; b < S::kBoxes; ++b)
+            for (int j = 0; j < 4; ++j)
+              tma_load_3d(res + rb * S::kTileBytes + b * kBoxBytes + ((j - it.at) & 3) * (kQuarterRows * 128),
+                          &p.tm_a, b * kBoxCols, it.at * kTile + j * kQuarterRows, it.unit, &res_full[rb]);
+        } else {
+          for (int b = 0; b < S::kBoxes; ++b)
+            tma_load_3d(res + rb * S::kTileBytes + b * kBoxBytes, &p.tm_a, b * kBoxCols, it.at * kTile, it.unit,
+                        &res_full[rb]);
+        }
         for (int t = 0; t < it.nt && ok; ++t) {
           ok = stream(&p.tm_b, (it.t_begin + t) * kTile, it.unit);
           if constexpr (kOut) {
@@ -1016,13 +1031,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [units][P][D] bf16 viewed as a 3-D tensor; boxes of 64 columns x 128 rows x 1 unit, 128-byte
 // swizzle; rows past P read as zeros.
-bool encode_operand(CUtensorMap* map, const void* base, int units, int P, int D) {
+bool encode_operand(CUtensorMap* map, const void* base, int units, int P, int D, int box_rows = kTile) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(P),
                               static_cast<cuuint64_t>(units)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(P) * D * 2};
-  const cuuint32_t box[3] = {kBoxCols, kTile, 1};
+  const cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1087,7 +1102,10 @@ cudaError_t launch_typed(const PrefillParams& pp, cudaStream_t s) {
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (pp.units >= sms) return launch_pass<D, kOnePass>(p, s);
+    if (pp.units >= sms) {
+      if (!encode_operand(&p.tm_a, pp.q, pp.units, pp.P, D, kQuarterRows)) return cudaErrorInvalidValue;
+      return launch_pass<D, kOnePass>(p, s);
+    }
   }
   // resident Q, streamed K (and V when the prompt's attention output is wanted)
   if (pp.out != nullptr) {
