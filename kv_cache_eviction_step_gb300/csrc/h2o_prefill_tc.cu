@@ -313,16 +313,16 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // 32 TMEM lanes x 32 columns of this warp's lane quarter in the 16x256b fragment shape (two loads of
 // 16 lanes, four 256-bit column groups each), so that every thread holds 4 rows x 8 columns: for
-// column group k (columns 8k..8k+7) and thread t, v[4k], v[4k+1] are row t/4, columns 8k + 2(t%4) and
-// +1; v[4k+2], v[4k+3] row t/4 + 8, the same columns; v[16 + ...] likewise rows t/4 + 16 and t/4 + 24.
-__device__ __forceinline__ void tmem_ld_rows4(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// column group k (columns 8k..8k+7) and thread t, r[4k], r[4k+1] are row t/4, columns 8k + 2(t%4) and
+// +1; r[4k+2], r[4k+3] row t/4 + 8, the same columns; r[16 + ...] likewise rows t/4 + 16 and t/4 + 24.
+// tmem_ld_rows4_start starts the loads; tmem_wait_rows4 waits for them taking r as in/out operands,
+// so that no use of r can move above the wait (work in between overlaps the loads).
+__device__ __forceinline__ void tmem_ld_rows4_start(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
       "%14, %15}, [%32];\n"
       "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%33];\n"
-      "tcgen05.wait::ld.sync.aligned;"
+      "%28, %29, %30, %31}, [%33];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
         "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
@@ -330,8 +330,16 @@ __device__ __forceinline__ void tmem_ld_rows4(uint32_t taddr, float* v) {
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr), "r"(taddr + (16u << 16))
       : "memory");
-#pragma unroll
-  for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
+}
+__device__ __forceinline__ void tmem_wait_rows4(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 
 // Sums over the 8 threads that share t % 4 (lane bits 2-4) of 8 column partials each: a butterfly
@@ -468,7 +476,7 @@ __device__ __forceinline__ void onepass_epilogue(const TcParams& p, uint32_t tme
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
   const float sl = p.sl;
   const int P = p.P;
-  // sweep 2: this thread's column within the warp's 32 (column_sum8's output, see tmem_ld_rows4)
+  // sweep 2: this thread's column within the warp's 32 (column_sum8's output, see tmem_ld_rows4_start)
   const int vsel = (lane >> 2) & 7;
   const int col = 8 * (vsel >> 1) + 2 * (lane & 3) + (vsel & 1);
   bool ok = true;
@@ -557,7 +565,10 @@ __device__ __forceinline__ void onepass_epilogue(const TcParams& p, uint32_t tme
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[a]);
         } else {
-          // row weights of the thread's four rows (lanes t/4 + 8i own them in sweep 1)
+          uint32_t rr[kCols];
+          tmem_ld_rows4_start(lane_addr + a * kTile + h * kCols, rr);
+          // row weights of the thread's four rows (lanes t/4 + 8i own them in sweep 1), while the
+          // e values load
           const float f = mt[t] == -INFINITY ? 0.f : ex2(mt[t] - mm) * inv;
           float2 fr[4];
 #pragma unroll
@@ -565,8 +576,10 @@ __device__ __forceinline__ void onepass_epilogue(const TcParams& p, uint32_t tme
             const float fi = __shfl_sync(0xffffffffu, f, (lane >> 2) + 8 * i);
             fr[i] = make_float2(fi, fi);
           }
+          tmem_wait_rows4(rr);
           float v[kCols];
-          tmem_ld_rows4(lane_addr + a * kTile + h * kCols, v);
+#pragma unroll
+          for (int x = 0; x < kCols; ++x) v[x] = __uint_as_float(rr[x]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[a]);
