@@ -143,6 +143,14 @@ def decode_kernel(w: synth.Workload, sms: int, e4m3: bool = False) -> tuple[str,
     return "h2o_decode_step_kernel", os.path.join(CSRC, "h2o_decode.cu")
 
 
+def prefill_launches(w: synth.Workload, sms: int) -> int:
+    """Launches of one H2O prefill (h2o_prefill_select / _e4m3): the score pass, then the selection.
+    The score pass is one launch (the one-pass column sums) for bf16 prompts of at most four 128-token
+    tiles with at least one unit per SM, else two (row statistics, then column sums)."""
+    one_pass = w.dtype == "bf16" and -(-w.prompt_len // 128) <= 4 and w.units >= sms
+    return (1 if one_pass else 2) + 1
+
+
 def recorded_traffic(workload: str, kernel: str, src: str, units_per_launch: int):
     """DRAM bytes per decode launch from the committed ncu records, if one was taken on the current
     source of this kernel, on this workload and with this many units per launch; otherwise None."""
@@ -328,7 +336,7 @@ def config_of(w: synth.Workload, args) -> dict:
             "kv_cache": ("E4M3 codes + float32 row scales (bf16 q/k/v/out)" if args.kv_cache == "e4m3"
                          else w.dtype),
             "l2": "no flush: KV cache and per-step inputs exceed the 129 MB L2",
-            "timing": "CUDA events between replays of CUDA graphs per job (3 prefill launches, then the "
+            "timing": "CUDA events between replays of CUDA graphs per job (the prefill's launches, then the "
                       "decode launches)",
             "decode_launch": (f"one launch per layer and step ({w.layers} launches per step of {w.batch} x "
                               f"{w.heads} = {w.units // w.layers} units each"
@@ -485,6 +493,7 @@ def main():
     avg_decode_s = float(np.mean(decode_ms)) / 1000.0 / L
     achieved = avg_bytes / avg_decode_s / 1e9
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_pre = prefill_launches(w, sms)
     kname, ksrc = decode_kernel(w.with_(layers=1), sms, e4m3)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, kname, ksrc, U // L),
@@ -500,7 +509,7 @@ def main():
             "decode_tokens_per_s": world * tokens_per_job / (sum(decode_ms) / K / 1000.0),
             "prefill_ms": float(np.mean(prefill_ms)),
             "decode_ms_per_token_step": float(np.mean(decode_ms)),
-            "gpu_launches": K * (3 + S * L),
+            "gpu_launches": K * (n_pre + S * L),
             "clocks": clocks.summary(),
             "input_generation_s": t_gen}
 
@@ -629,7 +638,8 @@ def workload_timing(h2o, w: synth.Workload, dev, warmup: int, reps: int, e4m3: b
                         "traffic": recorded_traffic(w.name, kname, ksrc, U), "kernel": kname,
                         "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                         "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_us": us},
-           "clocks": clocks.summary(), "gpu_launches_per_rep": 3 + S,
+           "clocks": clocks.summary(),
+           "gpu_launches_per_rep": prefill_launches(w, torch.cuda.get_device_properties(dev).multi_processor_count) + S,
            "how": "median over the timed replays; CUDA events around the prefill graph and around the "
                   "window's decode graphs on the launching stream" +
                   (f"; {fill} untimed decode steps before the window fill the cache" if fill else "")}

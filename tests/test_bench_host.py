@@ -34,6 +34,21 @@ def test_decode_kernel_dispatch():
     assert bench.decode_kernel(W["opt-6.7b"], 152, e4m3=True)[0] == "h2o_decode_e4m3_kernel"
 
 
+def test_prefill_launch_count():
+    """One score launch (the one-pass column sums) for bf16 prompts of <= 4 tiles with >= one unit per
+    SM, two otherwise; plus the selection."""
+    W = synth.WORKLOADS
+    n = lambda name, **kw: bench.prefill_launches(W[name].with_(**kw), 152)
+    assert n("opt-6.7b") == 2                           # 8192 units x 512 tokens
+    assert n("opt-30b") == 2                            # 1792 units x 512
+    assert n("opt-6.7b", prompt_len=513) == 3           # five tiles
+    assert n("opt-6.7b", layers=1, batch=4) == 3        # 128 units < one per SM
+    assert n("opt-6.7b", layers=1, batch=19, heads=8) == 2  # 152 units
+    assert n("llama-7b") == 3                           # 2048-token prompts
+    assert n("streaming") == 3                          # 32 units
+    assert n("tiny") == 3                               # fp32
+
+
 def test_oracle_baseline_record():
     b = bench.cpu_oracle_baseline(synth.WORKLOADS["tiny"], synth.DEFAULT_SEED, target_s=0.2)
     assert b["kind"] == "oracle" and b["unit"] == "tokens/s" and b["cores"] >= 1
