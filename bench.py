@@ -523,6 +523,10 @@ def main():
     # the step above, which builds the cache only.
     if not args.no_prefill_forward and not e4m3:
         line["prefill_forward"] = prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, args.warmup, K)
+    # The score pass of the prefill alone (its tensor-core rate), outside the step as well.
+    if w.dtype == "bf16" and not e4m3:
+        line["prefill_scores"] = prefill_scores_timing(h2o, dims, w, dv["q_prompt"], dv["k_prompt"], stream, dev,
+                                                       args.warmup, K)
 
     # The other workloads of the method's configurations, each timed on this GPU in the same run
     # (decode kernel rate with its roofline, prefill time, clocks), and the E4M3 cache on this one.
@@ -627,12 +631,15 @@ def workload_timing(h2o, w: synth.Workload, dev, warmup: int, reps: int, e4m3: b
     peaks, peak_kind = measured_peaks()
     achieved = avg_bytes / (us * 1e-6) / 1e9
     kname, ksrc = decode_kernel(w, torch.cuda.get_device_properties(dev).multi_processor_count, e4m3)
+    scores = (prefill_scores_timing(h2o, dims, w, dv["q_prompt"], dv["k_prompt"], stream, dev, warmup, reps)
+              if w.dtype == "bf16" and not e4m3 else None)
     res = {"workload": f"{w.name}: {w.note}", "units_per_launch": U,
            "kv_cache": "E4M3 codes + float32 row scales" if e4m3 else w.dtype,
            "decode_steps_timed": window, "first_timed_position": P + fill,
            "decode_us_per_step": us,
            "decode_tokens_per_s": w.batch * window / (float(np.median(win_ms)) / 1000.0),
            "prefill_ms": float(np.median(pre_ms)),
+           **({"prefill_scores": scores} if scores else {}),
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": achieved / peaks["hbm_gbs"],
                         "traffic": recorded_traffic(w.name, kname, ksrc, U), "kernel": kname,
@@ -736,6 +743,61 @@ def other_launch_shapes(h2o, w, dv, calls, out, evs, evp, stream, dev, g_pre, wa
         v["how"] = ("CUDA graphs of the decode launches, CUDA events around them; median over the timed "
                     "replays; cache rebuilt by the prefill between replays (untimed)")
     return res
+
+
+def prefill_score_kernels(w: synth.Workload, sms: int) -> str:
+    """The score kernel(s) h2o_prefill_scores launches for this workload (see prefill_launches)."""
+    if w.dtype != "bf16":
+        return "prefill_row_stats_kernel, prefill_colsum_kernel (CUDA cores)"
+    if prefill_launches(w, sms) == 2:
+        return "prefill_tc_kernel<D, one pass>"
+    return "prefill_tc_kernel<D, row stats>, prefill_tc_kernel<D, column sums>"
+
+
+def prefill_scores_timing(h2o, dims, w, q, k, stream, dev, warmup: int, reps: int) -> dict:
+    """h2o_prefill_scores (P1-P2, the tensor-core score pass) alone: one CUDA graph of the call replayed
+    back to back, CUDA events on the launching stream. Its rate counts the causal QK^T the method needs
+    once (P (P + 1) / 2 keys x D x 2 flops per unit, whatever the kernels issue) against the measured
+    bf16 peak, and its DRAM rate the algorithmic bytes Q + K (the prompts exceed L2 on every workload
+    this is reported for)."""
+    import torch
+    U, P, D = w.units, w.prompt_len, w.head_dim
+    colsum = torch.empty((U, P), dtype=torch.float32, device=dev)
+    ws = torch.empty(h2o.h2o_prefill_workspace_bytes(dims, P), dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+
+    def fn():
+        h2o.h2o_prefill_scores(dims, P, q, k, colsum, ws, sp)
+
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        ev[0].record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    if h2o.h2o_get_device_error(sp) != 0:
+        raise RuntimeError("device error word set during the prefill score timing")
+    us = ev[0].elapsed_time(ev[1]) * 1000.0 / reps
+    peaks, peak_kind = measured_peaks()
+    flops = float(U) * P * (P + 1) / 2 * D * 2
+    qk_bytes = 2.0 * U * P * D * w.elem_bytes
+    tflops = flops / (us * 1e-6) / 1e12
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    del colsum, ws
+    return {"us": us, "kernels": prefill_score_kernels(w, sms), "causal_qk_gflop": flops / 1e9,
+            "tflops": tflops, "bf16_peak_tflops": peaks["bf16_tflops"], "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "dram_gbs": qk_bytes / (us * 1e-6) / 1e9, "frac_of_hbm": qk_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "peak_source": f"{peak_kind} bf16_tflops (burst) and hbm_gbs",
+            "how": f"CUDA graph of one h2o_prefill_scores call, {reps} replays after {warmup}, CUDA events"}
 
 
 def prefill_forward_timing(h2o, dims, w, dv, cache, stream, dev, warmup: int, reps: int) -> dict:

@@ -47,6 +47,10 @@ def test_prefill_launch_count():
     assert n("llama-7b") == 3                           # 2048-token prompts
     assert n("streaming") == 3                          # 32 units
     assert n("tiny") == 3                               # fp32
+    k = lambda name, **kw: bench.prefill_score_kernels(W[name].with_(**kw), 152)
+    assert k("opt-30b") == "prefill_tc_kernel<D, one pass>"
+    assert k("llama-7b").startswith("prefill_tc_kernel<D, row stats>")
+    assert "CUDA cores" in k("tiny")
 
 
 def test_oracle_baseline_record():
