@@ -81,3 +81,25 @@ def test_one_pass_prefill_then_decode(P, budget, k_local):
                             budget=budget, k_heavy=budget - k_local, k_local=k_local)
     units = np.linspace(0, w.units - 1, 16).astype(int)
     parity.check(parity.run(w, check_units=units, state_every=8))
+
+
+@pytest.mark.parametrize("P", [1, 100, 300, 512])
+def test_one_pass_head_dim_64(P):
+    """The one-pass kernel's D = 64 shape (one 64-column TMA box per 32-row block, an 8-deep streamed
+    ring, four K steps per tile product) at one unit per SM: every column sum of 12 sampled units
+    against the oracle, a repeated call bit-identical, then the kept slot maps and 8 decode steps."""
+    import torch
+    units = _sms()
+    w = W["opt-6.7b"].with_(layers=1, batch=units, heads=1, head_dim=64, prompt_len=P, decode_steps=8,
+                            budget=64, k_heavy=32, k_local=32)
+    inp, first, colsum = _colsums(w)
+    assert torch.equal(first, colsum)
+    got = colsum.cpu().numpy().astype(np.float64)
+    sample = np.linspace(0, w.units - 1, 12).astype(int)
+    orc = oracle.Oracle(w.budget, w.k_heavy, w.k_local)
+    st = orc.new_state(len(sample), w.head_dim, synth.storage_dtype(w))
+    ref, _ = orc.prefill_select(inp.q_prompt[sample], inp.k_prompt[sample], inp.v_prompt[sample], st,
+                                want_colsum=True)
+    rel = np.abs(got[sample] - ref) / np.maximum(ref, 1e-3)
+    assert rel.max() < 2e-5, rel.max()
+    parity.check(parity.run(w, check_units=sample, state_every=4))
