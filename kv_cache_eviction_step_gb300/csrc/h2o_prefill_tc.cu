@@ -69,7 +69,6 @@ constexpr int kCtrlBytes = 384;            // mbarriers + TMEM address slot
 constexpr int kRegions = 4;                // one-pass column sums: 128-column logit regions (all of TMEM)
 constexpr int kQuarterRows = 32;           // one-pass column sums: rows per resident TMA box (a lane quarter)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.f;            // output pass: rescale only when the max grows by > 2^8
 
 enum Mode { kRowStats = 0, kRowOut = 1, kColSums = 2, kOnePass = 3 };
@@ -78,9 +77,9 @@ struct TcParams {
   CUtensorMap tm_a;        // resident operand: Q (row stats) or K (column sums), [units][P][D]
   CUtensorMap tm_b;        // streamed operand: K (row stats) or Q (column sums)
   CUtensorMap tm_v;        // output pass: V
-  const float* row_max_in; // column sums: m_i from the row-stats pass, [units][P]
-  const float* row_sum_in; // column sums: l_i
-  float* row_max;          // row stats output
+  const float* row_max_in; // column sums: m_i from the row-stats pass (log2 units), [units][P]
+  const float* row_sum_in; // column sums: l_i, taken against m_i
+  float* row_max;          // row stats output (log2 units: the largest s_ij log2(e) / sqrt(D))
   float* row_sum;
   float* colsum;           // column sums output
   __nv_bfloat16* out;      // output pass: [units][P][D]
@@ -100,13 +99,13 @@ struct TcShape {
   // Streamed ring depth. The output pass also holds V tiles and two probability tiles, so its ring
   // is shallower (it exchanges between warps through tensor memory); the other passes keep an
   // exchange area for the partial row results ([2][kSplit][128] float2) and, for column sums, each
-  // warp's query statistics ([kEpiWarps][2][kCols] float); the one-pass column sums keep, instead,
+  // warp's query statistics ([kEpiWarps][2][2][kCols] float: -m, 1/l); the one-pass column sums keep, instead,
   // each lane quarter's column partials of two units ([2][4][kRegions * 128] float).
   static constexpr int kStages = kMode == kRowOut ? (D == 128 ? 3 : 6) : (D == 128 ? 4 : 8);
   static constexpr int kXBytes = 2 * kSplit * kTile * 8;
   static constexpr int kPartBytes = 2 * 4 * kRegions * kTile * 4;
   static constexpr int kHeadBytes =
-      kCtrlBytes + (kMode == kRowOut ? 0 : kXBytes + (kMode == kOnePass ? kPartBytes : kEpiWarps * 2 * kCols * 4));
+      kCtrlBytes + (kMode == kRowOut ? 0 : kXBytes + (kMode == kOnePass ? kPartBytes : kEpiWarps * 4 * kCols * 4));
   static constexpr int kBodyBytes = (2 + kStages) * kTileBytes + (kMode == kRowOut ? 2 * kPBytes : 0);
   static constexpr int kSmem = kHeadBytes + kAlign + kBodyBytes;
 };
@@ -391,6 +390,32 @@ __device__ __forceinline__ float exp2_sum32(const float* v, float2 sl2, const fl
     } else {
       s01 = add2(s01, make_float2(ex2(e01.x), ex2(e01.y)));
       s23 = add2(s23, make_float2(ex2(e23.x), ex2(e23.y)));
+    }
+  }
+  return (s01.x + s01.y) + (s23.x + s23.y);
+}
+
+// sum_x 2^(v[x] sl + nb[x]) w[x] over 32 values, four interleaved partial sums as exp2_sum32; lanes
+// x < lo contribute nothing. Column sums: nb = -m_i (the query's maximum, so that the argument is
+// small where the weight matters) and w = 1 / l_i: the normaliser is applied as a factor rather than
+// folded into the exponent, where its magnitude (log2 l plus a maximum of hundreds) would cost fp32
+// bits of the argument.
+template <bool kMask>
+__device__ __forceinline__ float exp2_wsum32(const float* v, float2 sl2, const float4* nb4, const float4* w4, int lo) {
+  float2 s01 = make_float2(0.f, 0.f), s23 = s01;
+#pragma unroll
+  for (int x = 0; x < 32; x += 4) {
+    const float4 nb = nb4[x / 4], w = w4[x / 4];  // shared memory, read as needed
+    const float2 e01 = fma2(make_float2(v[x], v[x + 1]), sl2, make_float2(nb.x, nb.y));
+    const float2 e23 = fma2(make_float2(v[x + 2], v[x + 3]), sl2, make_float2(nb.z, nb.w));
+    if constexpr (kMask) {
+      s01 = fma2(make_float2(x >= lo ? ex2(e01.x) : 0.f, x + 1 >= lo ? ex2(e01.y) : 0.f), make_float2(w.x, w.y),
+                 s01);
+      s23 = fma2(make_float2(x + 2 >= lo ? ex2(e23.x) : 0.f, x + 3 >= lo ? ex2(e23.y) : 0.f), make_float2(w.z, w.w),
+                 s23);
+    } else {
+      s01 = fma2(make_float2(ex2(e01.x), ex2(e01.y)), make_float2(w.x, w.y), s01);
+      s23 = fma2(make_float2(ex2(e23.x), ex2(e23.y)), make_float2(w.z, w.w), s23);
     }
   }
   return (s01.x + s01.y) + (s23.x + s23.y);
@@ -803,9 +828,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     bool ok = true;
     uint32_t g = 0;  // logit tiles consumed (over all items)
     int k = 0;
-    float* xw = xq + warp * 2 * kCols;  // column sums: this warp's query statistics, [2][kCols]
-    // column sums: a query's row statistics, loaded one tile ahead of their use; its weight is
-    // 2^(s sl - b) with b = m log2(e) + log2(l) (queries past the prompt weigh nothing)
+    float* xw = xq + warp * 4 * kCols;  // column sums: this warp's query statistics, [2][-m, 1/l][kCols]
+    // column sums: a query's row statistics (m in log2 units), loaded one tile ahead of their use; its
+    // weight is 2^(s sl - m) / l (queries past the prompt weigh nothing)
     float qm = 0.f, ql = 0.f;
     auto qload = [&](int unit, int i) {
       qm = INFINITY;
@@ -829,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int x0 = (it.t_begin + t) * kTile + h * kCols;  // key (query) of this warp's column 0
         if constexpr (kCol) {
           // this tile's query statistics for this warp's columns; prefetch the next tile's
-          xw[xa * kCols + lane] = -fmaf(qm, kLog2e, log2f(ql));
+          xw[(2 * xa) * kCols + lane] = -qm;
+          xw[(2 * xa + 1) * kCols + lane] = __frcp_rn(ql);
           if (t + 1 < it.nt) qload(it.unit, (it.t_begin + t + 1) * kTile + h * kCols + lane);
           __syncwarp();
         }
@@ -858,16 +884,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             l += exp2_sum32<false>(v, make_float2(sl, sl), nm, 0);
           }
         } else if constexpr (kCol) {
-          const float4* b4 = reinterpret_cast<const float4*>(xw + xa * kCols);
-          float nb[kCols];  // this tile's negated query offsets for this warp's columns
-#pragma unroll
-          for (int x4 = 0; x4 < kCols / 4; ++x4) {
-            const float4 b = b4[x4];
-            nb[4 * x4 + 0] = b.x;
-            nb[4 * x4 + 1] = b.y;
-            nb[4 * x4 + 2] = b.z;
-            nb[4 * x4 + 3] = b.w;
-          }
+          // this tile's -m and 1/l for this warp's columns (queries), in shared memory
+          const float* nbs = xw + (2 * xa) * kCols;
+          const float* ils = xw + (2 * xa + 1) * kCols;
+          const float4* b4 = reinterpret_cast<const float4*>(nbs);
+          const float4* w4 = reinterpret_cast<const float4*>(ils);
           const float2 sl2 = make_float2(sl, sl);
           if (p.last_row_only) {
             const int xl = P - 1 - x0;  // the last query's column, if this warp holds it
@@ -875,13 +896,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               float s0 = 0.f;
 #pragma unroll
               for (int x = 0; x < kCols; ++x)
-                if (x == xl && row <= P - 1) s0 += ex2(fmaf(v[x], sl, nb[x]));
+                if (x == xl && row <= P - 1) s0 += ex2(fmaf(v[x], sl, nbs[xl])) * ils[xl];
               c += s0;
             }
           } else if (it.t_begin + t > it.at) {  // queries all after the keys
-            c += exp2_sum32<false>(v, sl2, nb, 0);
+            c += exp2_wsum32<false>(v, sl2, b4, w4, 0);
           } else {  // the diagonal tile: queries i >= row
-            c += exp2_sum32<true>(v, sl2, nb, row - x0);
+            c += exp2_wsum32<true>(v, sl2, b4, w4, row - x0);
           }
         } else {
           // Output pass. Probability tile a was last read by the product of logit tile g - 2.
@@ -966,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float2 o = xk[j * kTile + r];
             if (o.x != -INFINITY) lt += o.y * ex2(o.x - mm);
           }
-          p.row_max[ubase + row] = mm * kLn2;
+          p.row_max[ubase + row] = mm;
           p.row_sum[ubase + row] = lt;
         }
       } else if constexpr (kCol) {
@@ -1008,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             *reinterpret_cast<uint4*>(orow + c8 * 8) = w;
           }
           if (h == 0) {
-            p.row_max[ubase + row] = m2 * kLn2;
+            p.row_max[ubase + row] = m2;
             p.row_sum[ubase + row] = lt * ex2(mu - m2);  // the normaliser against the true maximum
           }
         }
