@@ -824,12 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     // (splits == 1) has both already: m = mc, l = lc (what the exchange would give: lc * exp(0)).
     float mg = mc, l = lc;
     if (splits > 1) {
-      if (tid == 0) {
-        for (int r = 0; r < splits; ++r) {
-          st_peer_f32(peer_smem(&xg->m_in[rank], r), mc);
-          st_peer_f32(peer_smem(&xg->l_in[rank], r), lc);
-          arrive_peer(peer_smem(&xbar[0], r));
-        }
+      // Thread r serves peer r, so the stores and release-arrivals to the peers go out side by side
+      // (one thread looping over them serialised one cluster-scope release per peer).
+      if (tid < splits) {
+        st_peer_f32(peer_smem(&xg->m_in[rank], tid), mc);
+        st_peer_f32(peer_smem(&xg->l_in[rank], tid), lc);
+        arrive_peer(peer_smem(&xbar[0], tid));
       }
       ok = mbar_wait_cluster(&xbar[0], 0, p.err) && ok;
       mg = -INFINITY;
@@ -893,8 +893,9 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
       st_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart);
       fence_cluster();
       epi_sync();
-      // Exchange 2: eviction keys and output slices.
-      if (tid == 0) {
+      // Exchange 2: eviction keys and output slices (the slices stored by every thread above, fenced
+      // and joined by the barrier before any arrival); thread r serves peer r.
+      if (tid < splits) {
         unsigned long long kb = kred[0];
         int32_t sb = sred[0];
         for (int w = 1; w < kEpiWarps; ++w)
@@ -902,11 +903,9 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
             kb = kred[w];
             sb = sred[w];
           }
-        for (int r = 0; r < splits; ++r) {
-          st_peer_u64(peer_smem(&xg->key_in[rank], r), kb);
-          st_peer_s32(peer_smem(&xg->slot_in[rank], r), sb);
-          arrive_peer(peer_smem(&xbar[1], r));
-        }
+        st_peer_u64(peer_smem(&xg->key_in[rank], tid), kb);
+        st_peer_s32(peer_smem(&xg->slot_in[rank], tid), sb);
+        arrive_peer(peer_smem(&xbar[1], tid));
       }
       ok = mbar_wait_cluster(&xbar[1], 0, p.err) && ok;
       for (int r = 0; r < splits; ++r)
