@@ -519,9 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_kernel(const __grid
 // weights taken relative to its own logit max so the tensor core never waits for the cluster; the
 // CTAs then exchange (1) their (max, normaliser) pairs, from which every CTA forms the common max m
 // and normaliser l, and (2) their eviction key plus a 1/splits slice of their output partial,
-// rescaled by exp(m_c - m), by writing into the peers' shared memory (st.shared::cluster) and
-// arriving on the peers' exchange mbarriers with cluster-scope release. Only the epilogue warps take
-// part, so the TMA and MMA warps never wait on the cluster.
+// rescaled by exp(m_c - m), by asynchronous stores into the peers' shared memory (st.async), each
+// counting its bytes against the receiving CTA's exchange mbarrier (complete_tx), which every CTA
+// arms with the total it expects before the cluster barrier at the start lets any peer send; thread
+// r of the sender serves peer r, so the stores to the peers go out side by side. Only the epilogue
+// warps take part, so the TMA and MMA warps never wait on the cluster.
 // CTA r finishes output elements [r 128/splits, (r+1) 128/splits); the CTA holding the victim writes
 // the new token; rank 0 writes the eviction indices. With splits == 1 (one CTA per unit, e.g. one
 // layer's 256 units per launch) there is nothing to exchange and the kernel skips both exchanges.
@@ -540,8 +542,7 @@ constexpr int kSWBytes = (kSplitMaxChunk / 64 + 1) * kNarrowBox;
 constexpr int kSXOff = kSWOff + kSWBytes;
 
 struct SplitXchg {
-  float m_in[kMaxSplitsTc];
-  float l_in[kMaxSplitsTc];
+  float2 ml_in[kMaxSplitsTc];  // (local max, local normaliser) of each rank (exchange 1, st.async)
   unsigned long long key_in[kMaxSplitsTc];
   int32_t slot_in[kMaxSplitsTc];
   float o_in[kD];  // [rank][128 / splits]: the senders' partials of this CTA's output slice
@@ -560,19 +561,28 @@ __device__ __forceinline__ uint32_t peer_smem(const void* local, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
   return out;
 }
-__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Asynchronous store of (a, b) into a peer's shared memory; on completion it counts 8 bytes
+// against the peer's mbarrier (complete_tx), which makes the data visible to the peer's waiters.
+__device__ __forceinline__ void st_async_peer_f32x2(uint32_t addr, float a, float b, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(bar_addr)
+               : "memory");
 }
-__device__ __forceinline__ void st_peer_u64(uint32_t addr, unsigned long long v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+__device__ __forceinline__ void st_async_peer_f32(uint32_t addr, float v, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(bar_addr)
+               : "memory");
 }
-__device__ __forceinline__ void st_peer_s32(uint32_t addr, int32_t v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void st_async_peer_u64(uint32_t addr, unsigned long long v, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr), "l"(v),
+               "r"(bar_addr)
+               : "memory");
 }
-__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+__device__ __forceinline__ void st_async_peer_s32(uint32_t addr, int32_t v, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar_addr)
+               : "memory");
 }
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Bounded wait with cluster-scope acquire: data that peers stored before their release-arrive on
 // this barrier is visible afterwards.
@@ -653,8 +663,16 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     mbar_init(s_full, 1);
     mbar_init(w_ready, 1);
     mbar_init(o_full, 1);
-    for (int x = 0; x < 2; ++x) mbar_init(&xbar[x], static_cast<uint32_t>(splits));
+    // Both exchanges arrive as st.async bytes against one local arrival each, armed here, before the
+    // cluster barrier below lets any peer send: exchange 1 (max, normaliser) 8 bytes per rank;
+    // exchange 2 the 128 output elements (a slice from each rank) plus a key and a slot per rank.
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     fence_mbar_init();
+    if (splits > 1) {
+      mbar_expect_tx(&xbar[0], static_cast<uint32_t>(8 * splits));
+      mbar_expect_tx(&xbar[1], static_cast<uint32_t>(kD * 4 + 12 * splits));
+    }
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -826,16 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     if (splits > 1) {
       // Thread r serves peer r, so the stores and release-arrivals to the peers go out side by side
       // (one thread looping over them serialised one cluster-scope release per peer).
-      if (tid < splits) {
-        st_peer_f32(peer_smem(&xg->m_in[rank], tid), mc);
-        st_peer_f32(peer_smem(&xg->l_in[rank], tid), lc);
-        arrive_peer(peer_smem(&xbar[0], tid));
-      }
+      if (tid < splits) st_async_peer_f32x2(peer_smem(&xg->ml_in[rank], tid), mc, lc, peer_smem(&xbar[0], tid));
       ok = mbar_wait_cluster(&xbar[0], 0, p.err) && ok;
       mg = -INFINITY;
-      for (int r = 0; r < splits; ++r) mg = fmaxf(mg, xg->m_in[r]);
+      for (int r = 0; r < splits; ++r) mg = fmaxf(mg, xg->ml_in[r].x);
       l = 0.f;
-      for (int r = 0; r < splits; ++r) l = fmaf(xg->l_in[r], expf(xg->m_in[r] - mg), l);
+      for (int r = 0; r < splits; ++r) l = fmaf(xg->ml_in[r].y, expf(xg->ml_in[r].x - mg), l);
     }
     const float w_new = expf(s_new - mg);
 
@@ -890,11 +904,11 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
         }
       o_sum += opart;
     } else {
-      st_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart);
-      fence_cluster();
+      // Exchange 2: output slices (each thread's element to the rank that finishes it) and eviction
+      // keys (thread r to peer r, once every warp's key is in kred).
+      st_async_peer_f32(peer_smem(&xg->o_in[rank * slice + tid % slice], tid / slice), opart,
+                        peer_smem(&xbar[1], tid / slice));
       epi_sync();
-      // Exchange 2: eviction keys and output slices (the slices stored by every thread above, fenced
-      // and joined by the barrier before any arrival); thread r serves peer r.
       if (tid < splits) {
         unsigned long long kb = kred[0];
         int32_t sb = sred[0];
@@ -903,9 +917,8 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
             kb = kred[w];
             sb = sred[w];
           }
-        st_peer_u64(peer_smem(&xg->key_in[rank], tid), kb);
-        st_peer_s32(peer_smem(&xg->slot_in[rank], tid), sb);
-        arrive_peer(peer_smem(&xbar[1], tid));
+        st_async_peer_u64(peer_smem(&xg->key_in[rank], tid), kb, peer_smem(&xbar[1], tid));
+        st_async_peer_s32(peer_smem(&xg->slot_in[rank], tid), sb, peer_smem(&xbar[1], tid));
       }
       ok = mbar_wait_cluster(&xbar[1], 0, p.err) && ok;
       for (int r = 0; r < splits; ++r)
@@ -950,7 +963,10 @@ __global__ void __launch_bounds__(kThreads, 1) h2o_decode_tc_split_kernel(const 
     // peer may still be on its way, so this CTA must not exit yet: thread 0 waits for all arrivals
     // on xbar[1] (a second, longer bounded window; an immediate return on the normal path), and
     // the block barrier below holds the whole CTA until then.
-    if (tid == 0 && splits > 1) (void)mbar_wait_cluster(&xbar[1], 0, p.err, 8000000000ull);
+    if (tid == 0 && splits > 1) {
+      (void)mbar_wait_cluster(&xbar[0], 0, p.err, 8000000000ull);
+      (void)mbar_wait_cluster(&xbar[1], 0, p.err, 8000000000ull);
+    }
   }
 
   tc_fence_before();
